@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Forward+backward throughput of the selective state-space scan on GB300.
+
+One step = one ``ssd_forward`` plus one ``ssd_backward`` (the whole hot path)
+over one batch of seeded synthetic inputs already resident in HBM.  Default
+workload: the Mamba-2 2.7B layer shape (b=4, T=4096, H=80, P=64, N=128, G=1,
+chunk 64; bf16 x/B/C/dy, fp32 dt/A/states).  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the float64 CPU oracle (the only other
+implementation of this method) on the host cores, on a bounded sample of the
+same workload, and reports the same metric.  Under torchrun (N > 1) every
+rank runs its own replica of the workload (weak scaling, no collective on the
+data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_ssd_gb300.configs import CONFIGS, HEADLINE, scaled, tokens  # noqa: E402
+
+METRIC = "SSD scan fwd+bwd tokens/s on 1 GB300 and % of roofline (HBM vs tensor peak)"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ------------------------------------------------------------------ models
+def _esize(cfg):
+    return 2 if cfg["dtype"] == "bf16" else 4
+
+
+def tensor_bytes(cfg):
+    """Bytes of every leaf input and output of one call pair."""
+    from selective_state_space_ssd_gb300.inputs import shapes
+    sh = shapes(cfg)
+    e = _esize(cfg)
+    n = {k: (0 if v is None else math.prod(v)) for k, v in sh.items()}
+    return {"x": n["x"] * e, "dt_raw": n["dt_raw"] * 4, "A": n["A"] * 4, "B": n["B"] * e, "C": n["C"] * e,
+            "s0": n["s0"] * 4}
+
+
+def algorithmic_bytes(cfg):
+    """Leaf inputs and outputs only; the backward re-reads the inputs it
+    recomputes from (no stashed state)."""
+    t = tensor_bytes(cfg)
+    fwd_in = t["x"] + t["dt_raw"] + t["A"] + t["B"] + t["C"] + t["s0"]
+    fwd_out = t["x"] + t["s0"]                                      # y, s_final
+    bwd_in = t["x"] + t["s0"] + fwd_in                              # dy, ds_final, leaves
+    bwd_out = t["x"] + t["dt_raw"] + t["A"] + t["B"] + t["C"] + t["s0"]
+    return fwd_in + fwd_out, bwd_in + bwd_out
+
+
+def tensor_flops(cfg):
+    """Dense tensor-core FLOPs of the chunkwise method per call pair (masked
+    L x L tiles counted dense)."""
+    v = cfg["variant"]
+    if v == "mamba1":
+        return 0.0
+    b, T, H, P, N, L, R = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "chunk", "mimo_rank"))
+    G = cfg["ngroups"] if v == "mamba2" else H
+    nc = T // L
+    LR = L * R
+    lpn, llp, lln = 2.0 * LR * P * N, 2.0 * LR * LR * P, 2.0 * LR * LR * N
+    per_head = 7 * lpn + 3 * llp          # K3, BLUE (fwd); K3 replay, BLUE dS, BLUE dC, K3 bwd x2; ORANGE, dW, dv
+    per_group = 4 * lln                   # CB (fwd), CB replay, K2 bwd x2
+    return b * nc * (H * per_head + G * per_group)
+
+
+def kernel_bytes(name, cfg):
+    """Compulsory HBM bytes of one launch of each kernel: what it must read and
+    write given its own inputs and outputs (intermediates included)."""
+    t = tensor_bytes(cfg)
+    b, T, H, P, N = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate"))
+    L = cfg["chunk"]
+    nc = T // L
+    states = b * H * nc * P * N * 4
+    small = b * H * nc * 4
+    dtb = t["dt_raw"]
+    m2 = cfg["variant"] == "mamba2"
+    part = b * T * H * N * 4 if m2 else 0
+    dvws = b * T * H * P * 4 if m2 else 0
+    table = {
+        "k_chunk_state": t["x"] + dtb + t["B"] + states + small,
+        "k_state_pass": 2 * states + small + 2 * t["s0"],
+        "k_chunk_out": t["x"] + dtb + t["B"] + t["C"] + states + t["x"],
+        "k_dS_blue": t["x"] + dtb + t["C"] + states,
+        "k_bwd_pass": 3 * states + small + 2 * t["s0"],
+        "k_chunk_bwd": (2 * t["x"] + dtb + t["B"] + t["C"] + 2 * states + small + 2 * dvws + t["x"] + dtb
+                        + (2 * part if m2 else t["B"] + t["C"]) + small),
+        "k_group_sum": part + t["B"],
+        "k_dA_sum": small + t["A"],
+        "k_m1_forward": 2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 2 * t["s0"],
+        "k_m1_backward": 2 * t["x"] + 2 * dtb + t["A"] + t["B"] + t["C"] + 3 * t["s0"] + t["x"]
+                         + 2 * b * T * H * N * 4 + b * H * N * 4 + b * H * (T // L) * N * 4,
+        "k_m1_channel_sum": b * T * H * N * 4 + t["B"],
+        "k_m1_dA_sum": b * H * N * 4 + t["A"],
+    }
+    return table.get(name)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def ncu_traffic(kernel, workload):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel, if
+    it was taken on the current sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(f"{kernel}@{workload}")
+    if not rec or rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def source_hash():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "selective_state_space_ssd_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi (every 200 ms)
+    while the timed region runs; the summary keeps samples taken under load."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        ids = [v.strip() for v in vis.split(",")] if vis else []
+        self.gpu = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)  # let the sampler start before the timed region
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), float(f[3]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        busy = [r for r in rows if r[2] > 0] or rows
+        reasons = sorted({nm for r in busy for nm, v in zip(self.NAMES, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": busy[0][1], "reasons": reasons,
+                "samples": len(busy)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def _oracle_sample(cfg, frac_t=1.0):
+    """A bounded sample of the workload for the float64 oracle: one batch
+    element, at most 64 heads (channels: at most 3072), T scaled by frac_t.
+    Returns (sample cfg, fraction of the full workload's units x steps)."""
+    over = {"batch": 1}
+    if cfg["variant"] == "mamba1":
+        over["nheads"] = min(cfg["nheads"], 1536)
+    else:
+        over["nheads"] = min(cfg["nheads"], 64 if cfg["variant"] == "mamba2" else 16)
+        if cfg["variant"] == "mamba2":
+            g = cfg["ngroups"]
+            over["ngroups"] = g if over["nheads"] % g == 0 else 1
+        else:
+            over["ngroups"] = over["nheads"]
+    T = max(cfg["chunk"], int(cfg["seqlen"] * frac_t) // cfg["chunk"] * cfg["chunk"])
+    over["seqlen"] = T
+    s = scaled(cfg, **over)
+    frac = (s["batch"] * s["nheads"] * s["seqlen"]) / (cfg["batch"] * cfg["nheads"] * cfg["seqlen"])
+    return s, frac
+
+
+def time_oracle(cfg, frac_t=1.0, inputs=None):
+    import oracle
+    from selective_state_space_ssd_gb300 import inputs as synth
+    s, frac = _oracle_sample(cfg, frac_t)
+    inp = inputs if inputs is not None else synth.as_float64(synth.make_inputs(s, seed=0))
+    nthreads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.forward(s["variant"], inp, nthreads=nthreads)
+    oracle.backward(s["variant"], inp, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    if s["variant"] == "mamba2":
+        tasks = s["batch"] * s["ngroups"] * math.ceil(s["nheads"] / s["ngroups"] / 4)
+    elif s["variant"] == "mamba1":
+        tasks = s["batch"] * math.ceil(s["nheads"] / 16)
+    else:
+        tasks = s["batch"] * s["nheads"]
+    cores = min(nthreads, tasks)
+    value = tokens(cfg) / (dt / frac)
+    desc = (f"batch {s['batch']} of {cfg['batch']}, {s['nheads']} of {cfg['nheads']} heads, T {s['seqlen']} of "
+            f"{cfg['seqlen']} ({100 * frac:.2f}% of the workload); tokens/s extrapolated linearly")
+    return value, dt, cores, desc, s, inp
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    from selective_state_space_ssd_gb300 import binding
+    from selective_state_space_ssd_gb300 import inputs as synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    binding.load()
+    cpu = synth.make_inputs(cfg, seed=0)
+    t = {k: (None if v is None else v.to(dev)) for k, v in cpu.items()}
+    prob = binding.problem(cfg)
+    nf, nb = binding.ssd_workspace_size(prob, False), binding.ssd_workspace_size(prob, True)
+    wsf = torch.empty(max(nf, 16), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(t["x"])
+    sf = torch.empty_like(t["ds_final"])
+    g = {"dx": torch.empty_like(t["x"]), "ddt_raw": torch.empty_like(t["dt_raw"]),
+         "dA": None if t["A"] is None else torch.empty_like(t["A"]), "dB": torch.empty_like(t["B"]),
+         "dC": torch.empty_like(t["C"]), "ds0": torch.empty_like(t["ds_final"])}
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)  # 516 MB > L2
+
+    def step(inp):
+        binding.ssd_forward(prob, inp["x"], inp["dt_raw"], inp["A"], inp["B"], inp["C"], inp["s0"], y, sf, wsf, nf,
+                            stream)
+        binding.ssd_backward(prob, inp["dy"], inp["ds_final"], inp["x"], inp["dt_raw"], inp["A"], inp["B"], inp["C"],
+                             inp["s0"], g["dx"], g["ddt_raw"], g["dA"], g["dB"], g["dC"], g["ds0"], wsb, nb, stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step(t)
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        for k in range(args.steps):
+            flush.zero_()                                 # L2 flush, outside the timed interval
+            starts[k].record(stream)
+            step(t)
+            ends[k].record(stream)
+        barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    clocks = clk.summary()
+
+    # per-kernel event timing over the same number of steps (separate pass)
+    binding.ssd_profile_start(1 << 16)
+    for k in range(args.steps):
+        flush.zero_()
+        step(t)
+    torch.cuda.synchronize(dev)
+    recs = binding.ssd_profile_stop(1 << 16)
+    per = {}
+    for name, ms in recs:
+        a = per.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += ms
+    launches_per_step = len(recs) / max(1, args.steps)
+
+    # end to end through the public API with host buffers (pinned)
+    host_in = {k: (None if v is None else v.pin_memory()) for k, v in cpu.items()}
+    host_out = {"y": torch.empty(y.shape, dtype=y.dtype, pin_memory=True),
+                "s_final": torch.empty(sf.shape, dtype=sf.dtype, pin_memory=True)}
+    for k, v in g.items():
+        if v is not None:
+            host_out[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k, v in host_in.items():
+            if v is not None:
+                t[k].copy_(v, non_blocking=True)
+        step(t)
+        host_out["y"].copy_(y, non_blocking=True)
+        host_out["s_final"].copy_(sf, non_blocking=True)
+        for k, v in g.items():
+            if v is not None:
+                host_out[k].copy_(v, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 10))
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    return {"total_ms": total_ms, "step_ms": step_ms, "clocks": clocks, "per_kernel": per,
+            "launches_per_step": launches_per_step, "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "h2d": h2d, "d2h": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = CONFIGS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wdesc = {"workload": f"{args.workload}: {cfg['variant']} b={cfg['batch']} T={cfg['seqlen']} H={cfg['nheads']} "
+                         f"P={cfg['headdim']} N={cfg['dstate']} G={cfg['ngroups']} chunk={cfg['chunk']} "
+                         f"R={cfg['mimo_rank']} io={cfg['dtype']}",
+             "global_batch": cfg["batch"] * world, "seq_len": cfg["seqlen"],
+             "parallelism": "replicas" if world > 1 else "single"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        times = []
+        inp = None
+        for i in range(args.warmup + args.steps):
+            value, dt, cores, desc, s, inp = time_oracle(cfg, frac_t=0.25, inputs=inp)
+            if i >= args.warmup:
+                times.append(dt)
+        _, frac = _oracle_sample(cfg, 0.25)
+        total = sum(times)
+        value = tokens(cfg) * len(times) / (total / frac)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times) / frac,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded; the recipe of the pages' workloads)", "config": wdesc,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": desc + "; each step = one forward + backward of that sample"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    r = run_ours(args, cfg, rank, world, local_rank)
+    fb, bb = algorithmic_bytes(cfg)
+    flops = tensor_flops(cfg)
+    pk = peaks()
+    tok = tokens(cfg)
+    value = world * tok * args.steps / (r["total_ms"] / 1e3)
+    ms_per_step = r["total_ms"] / args.steps
+    # dominant kernel: largest share of the profiled time
+    per = r["per_kernel"]
+    dom = max(per.items(), key=lambda kv: kv[1][1])[0] if per else None
+    dom_launches, dom_ms = per[dom] if dom else (0, 0.0)
+    dom_avg_ms = dom_ms / max(1, dom_launches)
+    dom_bytes = kernel_bytes(dom, cfg) if dom else None
+    achieved = (dom_bytes / (dom_avg_ms / 1e3) / 1e9) if dom_bytes and dom_avg_ms > 0 else None
+    tot_prof = sum(v[1] for v in per.values()) or 1.0
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+                "traffic": ncu_traffic(dom, args.workload), "peak_source": pk["source"],
+                "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_avg_ms,
+                "share_of_step": dom_ms / tot_prof}
+    step_s = ms_per_step / 1e3
+    t_hbm = (fb + bb) / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12) if flops else 0.0
+    roof_step = {"bytes": fb + bb, "tensor_flops": flops, "t_hbm_us": 1e6 * t_hbm, "t_tensor_us": 1e6 * t_tc,
+                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "roofline_tokens_per_s": tok / max(t_hbm, t_tc),
+                 "frac": max(t_hbm, t_tc) / step_s}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; the recipe of the pages' workloads)",
+            "config": dict(wdesc, l2="flushed before every timed step (516 MB write, outside the timed interval)"),
+            "roofline": roofline, "roofline_step": roof_step,
+            "per_kernel_ms": {k: {"launches": v[0], "total_ms": v[1]} for k, v in sorted(per.items())},
+            "gpu_launches": int(round(r["launches_per_step"] * args.steps)),
+            "clocks": r["clocks"],
+            "e2e": {"value": world * tok * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, cores, desc, _, _ = time_oracle(cfg, frac_t=1.0)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+                                "seconds": dt}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,192 @@
+/*
+ * ssd.h — C ABI of the GB300 (sm_103a) selective state-space scan library.
+ *
+ * The library computes one selective state-space scan and its vector-Jacobian
+ * product (VJP) on the GPU, for three forms of the recurrence:
+ *
+ *   Mamba-2 (SSD_MAMBA2), one scalar decay per head, B and C shared by the
+ *   heads of a group:
+ *       dt'_t = softplus(dt_raw_t)
+ *       s_t   = exp(dt'_t * A_h) * s_{t-1} + dt'_t * x_t (outer) B_t
+ *       y_t   = s_t . C_t                     (the updated state s_t)
+ *   Mamba-1 (SSD_MAMBA1), one decay per state:
+ *       s_t[n] = exp(dt'_t * A[d,n]) * s_{t-1}[n] + dt'_t * x_t * B_t[n]
+ *       y_t    = sum_n s_t[n] * C_t[n]
+ *   MIMO rank R (SSD_MIMO), the form of one pass of the Mamba-3 scan:
+ *       s_t     = exp(da_t) * s_{t-1} + sum_r v_{t,r} (outer) B_{t,r}
+ *       y_{t,r} = s_t . C_{t,r}
+ *
+ * Sources (the pages the method is taken from):
+ *   - "S1-31: SSM_SCAN_BACK — Mamba has a backward" (llama.cpp PR text),
+ *     opening paragraph: the reverse recurrence, the Mamba-2 and Mamba-1
+ *     branches and the five gradients; "Two things that are easy to get
+ *     wrong", item 1: the final-state gradient is a nonzero seed; item 2:
+ *     the backward needs s_{t-1} and recomputes the states; verification
+ *     table: the softplus derivative belongs in d(dt_raw).
+ *   - burn-mamba "combined_backward.rs" (Mamba-3 double-SSD, serial
+ *     recalculated): CombinedGrads (one gradient per input, including the
+ *     initial state), the chunkwise K1..K5 forward and the recompute backward
+ *     (replay K1..K4 from the saved leaf inputs, reverse per-chunk loop
+ *     fusing the K5 and K4 backwards, then batched K3/K2/K1 backwards).
+ *
+ * Conventions for every call:
+ *   - All tensor arguments are DEVICE pointers to contiguous row-major
+ *     arrays owned by the caller.  The library allocates nothing: scratch
+ *     memory is the caller's workspace, sized by ssd_workspace_size().
+ *   - Work is enqueued asynchronously on `cuda_stream` (a cudaStream_t; NULL
+ *     is the legacy default stream).  A call returns once its kernels are
+ *     enqueued.  Buffers must stay valid until the stream reaches them.
+ *   - Arguments are validated before anything is launched; on any error no
+ *     kernel runs and no output is written.
+ *   - Results are bitwise reproducible: the same inputs on the same GPU give
+ *     the same bits on every call (all reductions run in a fixed order; no
+ *     floating-point atomics).
+ *   - Calls on different streams with different buffers (including different
+ *     workspaces) may run concurrently.  A workspace must not be shared by
+ *     calls that may overlap on the GPU.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* NULL where a buffer is required, unknown enum, negative size */
+  SSD_ERR_SHAPE = 2,       /* sizes the method does not allow (T % chunk, H % G, limits) */
+  SSD_ERR_DTYPE = 3,       /* io dtype not supported for this variant */
+  SSD_ERR_ALIGNMENT = 4,   /* a pointer is not 16-byte aligned */
+  SSD_ERR_WORKSPACE = 5,   /* ws_bytes smaller than ssd_workspace_size() */
+  SSD_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+  SSD_ERR_TIMEOUT = 7,     /* reserved: a bounded device-side wait gave up */
+  SSD_ERR_INTERNAL = 8     /* a device-side consistency check failed */
+} ssd_status;
+
+typedef enum { SSD_MAMBA2 = 0, SSD_MAMBA1 = 1, SSD_MIMO = 2 } ssd_variant;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/*
+ * Problem description.
+ *   variant    ssd_variant.
+ *   io_dtype   ssd_dtype of x, B, C, y, dy, dx, dB, dC (and of v, dv for
+ *              MIMO).  dt_raw, A, s0, s_final, ds_final, ds0, ddt_raw, dA are
+ *              always fp32.  Mamba-1 supports SSD_F32 only.
+ *   batch      b >= 1 independent sequences.
+ *   seqlen     T >= 1 steps.
+ *   nheads     H heads (Mamba-2, MIMO) or D channels (Mamba-1).
+ *   headdim    P (Mamba-2, MIMO); must be 1 for Mamba-1.
+ *   dstate     N state size.
+ *   ngroups    G groups of consecutive heads sharing B and C (Mamba-2;
+ *              H % G == 0, head h reads group h / (H/G)).  Ignored for
+ *              Mamba-1 (B, C are shared by all channels) and MIMO (B, C are
+ *              per head).
+ *   chunk      L, the chunk length of the chunkwise algorithm (Mamba-2,
+ *              MIMO): T % L == 0 is required (the chunked layout builds T as
+ *              nchunks * chunk_len).  For Mamba-1 it is the replay segment of
+ *              the backward and must also divide T.
+ *   mimo_rank  R (MIMO); must be 1 for the other variants.
+ * Limits of this build: P <= 256, N <= 256, L * R <= 256 (Mamba-2, MIMO);
+ * N <= 32 (Mamba-1).  Larger sizes return SSD_ERR_SHAPE.
+ */
+typedef struct {
+  int32_t variant;
+  int32_t io_dtype;
+  int64_t batch;
+  int64_t seqlen;
+  int64_t nheads;
+  int64_t headdim;
+  int64_t dstate;
+  int64_t ngroups;
+  int64_t chunk;
+  int64_t mimo_rank;
+} ssd_problem;
+
+/*
+ * Bytes of device workspace that ssd_forward (backward == 0) or ssd_backward
+ * (backward != 0) needs for `prob`.  Writes *bytes and returns SSD_OK, or
+ * returns a validation error and leaves *bytes untouched.  Host-only; touches
+ * no device.
+ */
+ssd_status ssd_workspace_size(const ssd_problem* prob, int backward, size_t* bytes);
+
+/*
+ * Forward scan: y and s_final from (x, dt_raw, A, B, C, s0).
+ *
+ * Layouts (row-major):
+ *   Mamba-2: x, y [b,T,H,P]; dt_raw [b,T,H]; A [H]; B, C [b,T,G,N];
+ *            s0, s_final [b,H,P,N].
+ *   Mamba-1: x, y, dt_raw [b,T,D]; A [D,N]; B, C [b,T,N]; s0, s_final [b,D,N].
+ *   MIMO:    the x slot carries v [b,T,R,H,P]; the dt_raw slot carries the
+ *            pre-combined decay exponent da [b,T,H] (no softplus is applied);
+ *            A must be NULL; B, C [b,T,R,H,N]; y [b,T,R,H,P];
+ *            s0, s_final [b,H,P,N].
+ * s0 may be NULL (a zero initial state).  Every other pointer is required
+ * (except A for MIMO) and must be 16-byte aligned.
+ * ws / ws_bytes: caller-owned device workspace of at least
+ * ssd_workspace_size(prob, 0) bytes (ws may be NULL when that size is 0).
+ */
+ssd_status ssd_forward(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
+                       const void* B, const void* C, const float* s0, void* y, float* s_final, void* ws,
+                       size_t ws_bytes, void* cuda_stream);
+
+/*
+ * Backward (VJP) of ssd_forward.  Inputs: the upstream gradients dy (layout
+ * and dtype of y) and ds_final (fp32, layout of s_final; required, it is the
+ * nonzero seed of the reverse recurrence), and the saved leaf inputs of the
+ * forward (x, dt_raw, A, B, C, s0 exactly as passed to ssd_forward).  No
+ * forward intermediate is needed: the backward recomputes the chunk states.
+ *
+ * Outputs (each takes its primal's layout and dtype):
+ *   dx [like x], ddt_raw [like dt_raw, fp32], dA [like A, fp32],
+ *   dB [like B], dC [like C], ds0 [like s0, fp32].
+ * dB, dC (Mamba-2: over the heads of each group; Mamba-1: over all
+ * channels) and dA (over batch and time) are full reductions written once.
+ * MIMO: dx returns dv, ddt_raw returns d(da), and dA must be NULL.
+ * s0 may be NULL (zero initial state); ds0 is still written.
+ * ws / ws_bytes: at least ssd_workspace_size(prob, 1) bytes.
+ */
+ssd_status ssd_backward(const ssd_problem* prob, const void* dy, const float* ds_final, const void* x,
+                        const float* dt_raw, const float* A, const void* B, const void* C, const float* s0,
+                        void* dx, float* ddt_raw, float* dA, void* dB, void* dC, float* ds0, void* ws,
+                        size_t ws_bytes, void* cuda_stream);
+
+/*
+ * Per-launch timing, for diagnostics and roofline measurement.
+ *
+ * ssd_profile_start(capacity): every later ssd_forward / ssd_backward call
+ * (from any host thread) records a pair of CUDA events around each kernel it
+ * enqueues, on that call's stream, for up to `capacity` launches.  Returns
+ * SSD_ERR_INVALID_ARG if capacity < 1.  Events are created with
+ * cudaEventCreate on the current device; no device memory is allocated.
+ *
+ * ssd_profile_stop(out, capacity, count): waits for the recorded events,
+ * writes one {kernel name, milliseconds} record per launch in launch order
+ * (at most `capacity`), sets *count to the number written, destroys the
+ * events and turns recording off.  The names are static strings.  Returns
+ * SSD_ERR_CUDA if an event query fails.
+ */
+typedef struct {
+  const char* kernel;
+  float ms;
+} ssd_kernel_time;
+
+ssd_status ssd_profile_start(int capacity);
+ssd_status ssd_profile_stop(ssd_kernel_time* out, int capacity, int* count);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* ssd_status_string(ssd_status status);
+
+/* Version of this library as MAJOR*10000 + MINOR*100 + PATCH. */
+int ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

@@ -176,6 +176,7 @@ static void m2_backward_task(void* vctx, int64_t task, double* scratch) {
   double* S = scratch;                 /* [(T+1)][P][N] */
   double* dS = S + (T + 1) * P * N;    /* [P][N] */
   double* u = dS + P * N;              /* [P] */
+  double* acc_n = u + P;               /* [N] */
   double* dBp = c->dB_part + ((b * G + g) * nblk + k) * T * N;
   double* dCp = c->dC_part + ((b * G + g) * nblk + k) * T * N;
   memset(dBp, 0, sizeof(double) * T * N);
@@ -217,11 +218,10 @@ static void m2_backward_task(void* vctx, int64_t task, double* scratch) {
           for (int64_t n = 0; n < N; ++n) dS[p * N + n] += dyt[p] * Ct[n];
       /* dC_t = sum_p dy_t[p] s_t[p, :] */
       const double* s_for_dC = (mut == 4) ? s_prev : s_cur;
-      for (int64_t n = 0; n < N; ++n) {
-        double acc = 0.0;
-        for (int64_t p = 0; p < P; ++p) acc += dyt[p] * s_for_dC[p * N + n];
-        dCp[t * N + n] += acc;
-      }
+      for (int64_t n = 0; n < N; ++n) acc_n[n] = 0.0;
+      for (int64_t p = 0; p < P; ++p)       /* per n, p ascending */
+        for (int64_t n = 0; n < N; ++n) acc_n[n] += dyt[p] * s_for_dC[p * N + n];
+      for (int64_t n = 0; n < N; ++n) dCp[t * N + n] += acc_n[n];
       /* s_t = a s_{t-1} + d x_t (outer) B_t */
       double dd = 0.0; /* d J / d dt' */
       for (int64_t p = 0; p < P; ++p) {
@@ -231,11 +231,10 @@ static void m2_backward_task(void* vctx, int64_t task, double* scratch) {
         c->dx[((b * T + t) * H + h) * P + p] = d * acc;
         dd += acc * xt[p];
       }
-      for (int64_t n = 0; n < N; ++n) {
-        double acc = 0.0;
-        for (int64_t p = 0; p < P; ++p) acc += dS[p * N + n] * xt[p];
-        dBp[t * N + n] += d * acc;
-      }
+      for (int64_t n = 0; n < N; ++n) acc_n[n] = 0.0;
+      for (int64_t p = 0; p < P; ++p)
+        for (int64_t n = 0; n < N; ++n) acc_n[n] += dS[p * N + n] * xt[p];
+      for (int64_t n = 0; n < N; ++n) dBp[t * N + n] += d * acc_n[n];
       /* the decay path: a = exp(d A), d a / d(dA) = a */
       double dda = 0.0;
       for (int64_t i = 0; i < P * N; ++i) dda += dS[i] * s_prev[i];
@@ -282,7 +281,7 @@ int oracle_m2_backward(int64_t b, int64_t T, int64_t H, int64_t P, int64_t N, in
   c.dA_part = (double*)malloc(sizeof(double) * (size_t)(b * H) + 8);
   int rc = -1;
   if (c.dB_part && c.dC_part && c.dA_part) {
-    rc = parallel_for(b * G * c.nblk, nthreads, (size_t)((T + 2) * P * N + P), m2_backward_task, &c);
+    rc = parallel_for(b * G * c.nblk, nthreads, (size_t)((T + 2) * P * N + P + N), m2_backward_task, &c);
     if (rc == 0) {
       /* fixed-order reductions: head blocks ascending, then batches ascending */
       for (int64_t bb = 0; bb < b; ++bb)
@@ -537,11 +536,9 @@ static void mimo_backward_task(void* vctx, int64_t task, double* scratch) {
       if (mut != 3)
         for (int64_t p = 0; p < P; ++p)
           for (int64_t n = 0; n < N; ++n) dS[p * N + n] += dyt[p] * Ct[n];
-      for (int64_t n = 0; n < N; ++n) {
-        double acc = 0.0;
-        for (int64_t p = 0; p < P; ++p) acc += dyt[p] * s_for_dC[p * N + n];
-        dCt[n] = acc;
-      }
+      for (int64_t n = 0; n < N; ++n) dCt[n] = 0.0;
+      for (int64_t p = 0; p < P; ++p)       /* per n, p ascending */
+        for (int64_t n = 0; n < N; ++n) dCt[n] += dyt[p] * s_for_dC[p * N + n];
     }
     /* s_t = a s_{t-1} + sum_r v_r (outer) B_r */
     for (int64_t r = 0; r < R; ++r) {
@@ -554,11 +551,9 @@ static void mimo_backward_task(void* vctx, int64_t task, double* scratch) {
         for (int64_t n = 0; n < N; ++n) acc += dS[p * N + n] * Bt[n];
         dvt[p] = acc;
       }
-      for (int64_t n = 0; n < N; ++n) {
-        double acc = 0.0;
-        for (int64_t p = 0; p < P; ++p) acc += dS[p * N + n] * vt[p];
-        dBt[n] = acc;
-      }
+      for (int64_t n = 0; n < N; ++n) dBt[n] = 0.0;
+      for (int64_t p = 0; p < P; ++p)
+        for (int64_t n = 0; n < N; ++n) dBt[n] += dS[p * N + n] * vt[p];
     }
     double dda = 0.0;
     for (int64_t i = 0; i < P * N; ++i) dda += dS[i] * s_prev[i];

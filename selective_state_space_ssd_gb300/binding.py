@@ -1,0 +1,181 @@
+"""Thin ctypes binding of the C ABI in ``include/ssd.h``.
+
+The functions carry the C names (``ssd_workspace_size``, ``ssd_forward``,
+``ssd_backward``, ``ssd_status_string``) and only marshal arguments: torch
+tensors become device pointers, the torch stream becomes a ``cudaStream_t``,
+and a non-OK status becomes an :class:`SSDError`.  Every step of the scan runs
+in the library's kernels; there is no fallback of any kind.  If the library
+cannot be loaded the call raises.
+
+Convenience wrappers :func:`forward` and :func:`backward` allocate outputs
+and the workspace with torch (device memory only) and call the ABI.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+VARIANTS = {"mamba2": 0, "mamba1": 1, "mimo": 2}
+DTYPES = {"f32": 0, "bf16": 1}
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+SSD_OK = 0
+
+
+class SSDError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {ssd_status_string(status)} (status {status})")
+
+
+class ssd_problem(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int32), ("io_dtype", ctypes.c_int32), ("batch", ctypes.c_int64),
+                ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("chunk", ctypes.c_int64),
+                ("mimo_rank", ctypes.c_int64)]
+
+
+EXPORTS = ("ssd_workspace_size", "ssd_forward", "ssd_backward", "ssd_profile_start", "ssd_profile_stop",
+           "ssd_status_string", "ssd_version")
+
+
+class ssd_kernel_time(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_char_p), ("ms", ctypes.c_float)]
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the in-tree shared library."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.build()
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library missing: {p}")
+        lib = ctypes.CDLL(p)
+        vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        lib.ssd_workspace_size.argtypes = [ctypes.POINTER(ssd_problem), i32, ctypes.POINTER(sz)]
+        lib.ssd_workspace_size.restype = i32
+        lib.ssd_forward.argtypes = [ctypes.POINTER(ssd_problem)] + [vp] * 8 + [vp, sz, vp]
+        lib.ssd_forward.restype = i32
+        lib.ssd_backward.argtypes = [ctypes.POINTER(ssd_problem)] + [vp] * 14 + [vp, sz, vp]
+        lib.ssd_backward.restype = i32
+        lib.ssd_status_string.argtypes = [i32]
+        lib.ssd_status_string.restype = ctypes.c_char_p
+        lib.ssd_profile_start.argtypes = [i32]
+        lib.ssd_profile_start.restype = i32
+        lib.ssd_profile_stop.argtypes = [ctypes.POINTER(ssd_kernel_time), i32, ctypes.POINTER(i32)]
+        lib.ssd_profile_stop.restype = i32
+        lib.ssd_version.argtypes = []
+        lib.ssd_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def problem(cfg: dict) -> ssd_problem:
+    """An ``ssd_problem`` from a config dict (see ``configs.py``)."""
+    return ssd_problem(VARIANTS[cfg["variant"]], DTYPES[cfg["dtype"]], cfg["batch"], cfg["seqlen"], cfg["nheads"],
+                       cfg["headdim"], cfg["dstate"], cfg["ngroups"], cfg["chunk"], cfg["mimo_rank"])
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def ssd_status_string(status: int) -> str:
+    return load().ssd_status_string(int(status)).decode()
+
+
+def ssd_workspace_size(prob: ssd_problem, backward: bool) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().ssd_workspace_size(ctypes.byref(prob), int(bool(backward)), ctypes.byref(out))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_workspace_size")
+    return out.value
+
+
+def ssd_forward(prob, x, dt_raw, A, B, C, s0, y, s_final, ws, ws_bytes, stream=None) -> None:
+    st = load().ssd_forward(ctypes.byref(prob), _ptr(x), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(s0),
+                            _ptr(y), _ptr(s_final), _ptr(ws), int(ws_bytes), _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_forward")
+
+
+def ssd_backward(prob, dy, ds_final, x, dt_raw, A, B, C, s0, dx, ddt_raw, dA, dB, dC, ds0, ws, ws_bytes,
+                 stream=None) -> None:
+    st = load().ssd_backward(ctypes.byref(prob), _ptr(dy), _ptr(ds_final), _ptr(x), _ptr(dt_raw), _ptr(A), _ptr(B),
+                             _ptr(C), _ptr(s0), _ptr(dx), _ptr(ddt_raw), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(ds0),
+                             _ptr(ws), int(ws_bytes), _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_backward")
+
+
+def ssd_profile_start(capacity: int) -> None:
+    st = load().ssd_profile_start(int(capacity))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_profile_start")
+
+
+def ssd_profile_stop(capacity: int = 1 << 16) -> list:
+    """Returns [(kernel name, ms)] for every launch recorded since start."""
+    buf = (ssd_kernel_time * capacity)()
+    n = ctypes.c_int(0)
+    st = load().ssd_profile_stop(buf, int(capacity), ctypes.byref(n))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_profile_stop")
+    return [(buf[i].kernel.decode(), float(buf[i].ms)) for i in range(n.value)]
+
+
+# ---------------------------------------------------------------- conveniences
+def _workspace(prob, backward, device):
+    n = ssd_workspace_size(prob, backward)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device), n
+
+
+def forward(cfg: dict, x, dt_raw, A, B, C, s0=None, stream=None, workspace=None):
+    """Allocate y and s_final, run ``ssd_forward``; returns (y, s_final)."""
+    prob = problem(cfg)
+    dev = x.device
+    y = torch.empty_like(x)
+    sf_shape = (cfg["batch"], cfg["nheads"], cfg["dstate"]) if cfg["variant"] == "mamba1" else \
+        (cfg["batch"], cfg["nheads"], cfg["headdim"], cfg["dstate"])
+    s_final = torch.empty(sf_shape, dtype=torch.float32, device=dev)
+    ws, n = workspace if workspace is not None else _workspace(prob, False, dev)
+    ssd_forward(prob, x, dt_raw, A, B, C, s0, y, s_final, ws, n, stream)
+    return y, s_final
+
+
+def backward(cfg: dict, dy, ds_final, x, dt_raw, A, B, C, s0=None, stream=None, workspace=None):
+    """Allocate the gradients, run ``ssd_backward``; returns a dict with
+    dx, ddt_raw, dA (None for MIMO), dB, dC, ds0."""
+    prob = problem(cfg)
+    dev = x.device
+    out = {"dx": torch.empty_like(x), "ddt_raw": torch.empty_like(dt_raw),
+           "dA": None if A is None else torch.empty_like(A), "dB": torch.empty_like(B), "dC": torch.empty_like(C),
+           "ds0": torch.empty_like(ds_final)}
+    ws, n = workspace if workspace is not None else _workspace(prob, True, dev)
+    ssd_backward(prob, dy, ds_final, x, dt_raw, A, B, C, s0, out["dx"], out["ddt_raw"], out["dA"], out["dB"],
+                 out["dC"], out["ds0"], ws, n, stream)
+    return out

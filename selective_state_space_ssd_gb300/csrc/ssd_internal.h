@@ -1,0 +1,91 @@
+// Internal host/device interface of the scan library (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+enum Variant { kMamba2 = 0, kMamba1 = 1, kMimo = 2 };
+
+// Validated sizes of one problem.  All counts fit in int; element offsets are
+// computed in size_t.
+struct Dims {
+  int variant;
+  bool bf16;  // io dtype
+  int b, T, H, P, N, G, L, R;
+  int nc;   // T / L
+  int LR;   // fused chunk length L * R
+  int hpg;  // heads per group (Mamba-2)
+};
+
+struct FwdArgs {
+  const void* x;
+  const float* dt_raw;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* s0;
+  void* y;
+  float* s_final;
+};
+
+struct BwdArgs {
+  const void* dy;
+  const float* ds_final;
+  const void* x;
+  const float* dt_raw;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* s0;
+  void* dx;
+  float* ddt_raw;
+  float* dA;
+  void* dB;
+  void* dC;
+  float* ds0;
+};
+
+// Carves a caller-owned workspace into 256-byte aligned pieces.  The same
+// code sizes the workspace (base == nullptr) and hands out the pointers.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+// Chunked SIMT path (Mamba-2 and MIMO; fp32 arithmetic, fp32 or bf16 io).
+size_t simt_forward_ws(const Dims& d);
+size_t simt_backward_ws(const Dims& d);
+cudaError_t simt_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
+cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
+
+// Mamba-1 path (fp32).
+size_t m1_forward_ws(const Dims& d);
+size_t m1_backward_ws(const Dims& d);
+cudaError_t m1_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
+cudaError_t m1_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
+
+// Per-launch event timing (see ssd_profile_start in ssd.h).  SSD_LAUNCH wraps
+// every kernel launch of the library.
+void prof_begin(const char* name, cudaStream_t st);
+void prof_end(cudaStream_t st);
+
+}  // namespace ssd
+
+#define SSD_LAUNCH(name, st, ...)     \
+  do {                                \
+    ::ssd::prof_begin((name), (st));  \
+    __VA_ARGS__;                      \
+    ::ssd::prof_end((st));            \
+  } while (0)

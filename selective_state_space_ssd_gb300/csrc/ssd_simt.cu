@@ -1,0 +1,537 @@
+// Chunked scan on CUDA cores (fp32 arithmetic; fp32 or bf16 io) for the
+// Mamba-2 and MIMO forms.  It follows the chunkwise algebra of the burn-mamba
+// page "combined_backward.rs" (Mamba-3 double-SSD, serial recalculated):
+//
+//   forward   K1 in-chunk cumsum of da, K3 chunk-end state from a zero start,
+//             K4 state passing across chunks, K5 = BLUE (state read-out
+//             exp(cumA_t) C S_c^T) + ORANGE (intra-chunk (CB o decay o mask) v);
+//   backward  replay K1, K3, K4 from the leaf inputs; BLUE's dS term; the
+//             reverse chunk loop carrying dS from the ds_final seed (K4
+//             backward); per chunk the ORANGE, BLUE-dC, K3 and K2 backwards;
+//             K1 backward as a suffix sum; the chain rule to dt_raw and A
+//             (Mamba-2) and fixed-order reductions over heads and batches.
+//
+// Mamba-2 enters as the R = 1 case with v = dt' x, da = dt' A_h and B, C read
+// from the head's group.  This is the fp32 path and the reference structure
+// for the tensor-core kernels; every reduction runs in a fixed order.
+#include "ssd_device.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Read-only view of one problem's inputs with the variant's index maps.
+template <typename TIn, bool MIMO>
+struct Seq {
+  const TIn* x;       // Mamba-2 x [b,T,H,P] | MIMO v [b,T,R,H,P]
+  const float* dt;    // Mamba-2 dt_raw [b,T,H] | MIMO da [b,T,H]
+  const float* A;     // Mamba-2 [H] | MIMO unused
+  const TIn* B;       // Mamba-2 [b,T,G,N] | MIMO [b,T,R,H,N]
+  const TIn* C;
+  int T, H, P, N, G, L, R, LR, nc, hpg;
+
+  __device__ size_t xi(int b, int t, int r, int h, int p) const {
+    return MIMO ? ((((size_t)b * T + t) * R + r) * H + h) * P + p : (((size_t)b * T + t) * H + h) * P + p;
+  }
+  __device__ size_t bi(int b, int t, int r, int h, int n) const {
+    return MIMO ? ((((size_t)b * T + t) * R + r) * H + h) * N + n
+                : (((size_t)b * T + t) * G + h / hpg) * N + n;
+  }
+  __device__ size_t ti(int b, int t, int h) const { return ((size_t)b * T + t) * H + h; }
+  // v at fused position (t, r): MIMO reads it, Mamba-2 forms dt' x.
+  __device__ float v(int b, int t, int r, int h, int p, float dtp) const {
+    return MIMO ? ld(x, xi(b, t, r, h, p)) : dtp * ld(x, xi(b, t, r, h, p));
+  }
+  __device__ float Bm(int b, int t, int r, int h, int n) const { return ld(B, bi(b, t, r, h, n)); }
+  __device__ float Cm(int b, int t, int r, int h, int n) const { return ld(C, bi(b, t, r, h, n)); }
+};
+
+// K1 for one chunk: s_dtp[l] = dt' (1 for MIMO), s_cum[l] = inclusive cumsum
+// of da over the chunk (serial, so every kernel gets the same bits).
+template <typename TIn, bool MIMO>
+__device__ void chunk_scalars(const Seq<TIn, MIMO>& s, int b, int h, int c, float* s_cum, float* s_dtp) {
+  for (int l = threadIdx.x; l < s.L; l += blockDim.x) {
+    const int t = c * s.L + l;
+    const float z = s.dt[s.ti(b, t, h)];
+    if (MIMO) {
+      s_dtp[l] = 1.f;
+      s_cum[l] = z;
+    } else {
+      const float d = softplus_f(z);
+      s_dtp[l] = d;
+      s_cum[l] = d * s.A[h];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float acc = 0.f;
+    for (int l = 0; l < s.L; ++l) {
+      acc += s_cum[l];
+      s_cum[l] = acc;
+    }
+  }
+  __syncthreads();
+}
+
+// K3: intra[p,n] = sum_i exp(cum_end - cum_i) v[i,p] B[i,n] over the fused
+// positions i = l*R + r of chunk c; also records cum_end.
+template <typename TIn, bool MIMO>
+__global__ void __launch_bounds__(kThreads) k_chunk_state(Seq<TIn, MIMO> s, float* states, float* cum_end) {
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  extern __shared__ float sm[];
+  float* s_cum = sm;
+  float* s_dtp = sm + s.L;
+  float* s_dec = s_dtp + s.L;
+  chunk_scalars(s, b, h, c, s_cum, s_dtp);
+  for (int l = threadIdx.x; l < s.L; l += blockDim.x) s_dec[l] = expf(s_cum[s.L - 1] - s_cum[l]);
+  if (threadIdx.x == 0) cum_end[((size_t)b * s.H + h) * s.nc + c] = s_cum[s.L - 1];
+  __syncthreads();
+  const int PN = s.P * s.N;
+  float* out = states + (((size_t)b * s.H + h) * s.nc + c) * PN;
+  for (int e = threadIdx.x; e < PN; e += blockDim.x) {
+    const int p = e / s.N, n = e % s.N;
+    float acc = 0.f;
+    for (int i = 0; i < s.LR; ++i) {
+      const int l = i / s.R, r = i % s.R, t = c * s.L + l;
+      acc += s_dec[l] * s.v(b, t, r, h, p, s_dtp[l]) * s.Bm(b, t, r, h, n);
+    }
+    out[e] = acc;
+  }
+}
+
+// K4: walks the chunks in order; replaces each chunk's intra state by the
+// chunk-input state S_c and writes s_final.
+__global__ void __launch_bounds__(kThreads) k_state_pass(float* states, const float* cum_end, const float* s0,
+                                                         float* s_final, int H, int nc, int PN) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const size_t unit = (size_t)b * H + h;
+  for (int e = threadIdx.x; e < PN; e += blockDim.x) {
+    float S = s0 ? s0[unit * PN + e] : 0.f;
+    for (int c = 0; c < nc; ++c) {
+      const size_t idx = (unit * nc + c) * PN + e;
+      const float intra = states[idx];
+      states[idx] = S;
+      S = expf(cum_end[unit * nc + c]) * S + intra;
+    }
+    s_final[unit * PN + e] = S;
+  }
+}
+
+// K5: y[i,p] = exp(cum_i) sum_n C[i,n] S_c[p,n] + sum_{j: l_j <= l_i} CB[i,j] exp(cum_i - cum_j) v[j,p].
+template <typename TIn, bool MIMO>
+__global__ void __launch_bounds__(kThreads) k_chunk_out(Seq<TIn, MIMO> s, const float* states, TIn* y) {
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  extern __shared__ float sm[];
+  float* s_cum = sm;
+  float* s_dtp = sm + s.L;
+  float* s_w = s_dtp + s.L;  // [LR]
+  chunk_scalars(s, b, h, c, s_cum, s_dtp);
+  const float* Sc = states + (((size_t)b * s.H + h) * s.nc + c) * s.P * s.N;
+  for (int i = 0; i < s.LR; ++i) {
+    const int li = i / s.R, ri = i % s.R, ti = c * s.L + li;
+    for (int j = threadIdx.x; j < s.LR; j += blockDim.x) {
+      const int lj = j / s.R, rj = j % s.R, tj = c * s.L + lj;
+      float w = 0.f;
+      if (lj <= li) {  // mask before the exponential
+        float cb = 0.f;
+        for (int n = 0; n < s.N; ++n) cb += s.Cm(b, ti, ri, h, n) * s.Bm(b, tj, rj, h, n);
+        w = cb * expf(s_cum[li] - s_cum[lj]);
+      }
+      s_w[j] = w;
+    }
+    __syncthreads();
+    const float eci = expf(s_cum[li]);
+    const int jmax = (li + 1) * s.R;
+    for (int p = threadIdx.x; p < s.P; p += blockDim.x) {
+      float off = 0.f;
+      for (int n = 0; n < s.N; ++n) off += s.Cm(b, ti, ri, h, n) * Sc[p * s.N + n];
+      float diag = 0.f;
+      for (int j = 0; j < jmax; ++j) {
+        const int lj = j / s.R, rj = j % s.R;
+        diag += s_w[j] * s.v(b, c * s.L + lj, rj, h, p, s_dtp[lj]);
+      }
+      st(y, s.xi(b, ti, ri, h, p), eci * off + diag);
+    }
+    __syncthreads();
+  }
+}
+
+// BLUE's state gradient per chunk: dSb[p,n] = sum_i dy[i,p] exp(cum_i) C[i,n].
+template <typename TIn, bool MIMO>
+__global__ void __launch_bounds__(kThreads) k_dS_blue(Seq<TIn, MIMO> s, const TIn* dy, float* dsx) {
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  extern __shared__ float sm[];
+  float* s_cum = sm;
+  float* s_dtp = sm + s.L;
+  float* s_e = s_dtp + s.L;
+  chunk_scalars(s, b, h, c, s_cum, s_dtp);
+  for (int l = threadIdx.x; l < s.L; l += blockDim.x) s_e[l] = expf(s_cum[l]);
+  __syncthreads();
+  const int PN = s.P * s.N;
+  float* out = dsx + (((size_t)b * s.H + h) * s.nc + c) * PN;
+  for (int e = threadIdx.x; e < PN; e += blockDim.x) {
+    const int p = e / s.N, n = e % s.N;
+    float acc = 0.f;
+    for (int i = 0; i < s.LR; ++i) {
+      const int l = i / s.R, r = i % s.R, t = c * s.L + l;
+      acc += ld(dy, s.xi(b, t, r, h, p)) * s_e[l] * s.Cm(b, t, r, h, n);
+    }
+    out[e] = acc;
+  }
+}
+
+// K4 backward: dS_nc = ds_final; for c = nc-1..0:
+//   d cum_end_c += exp(cum_end_c) <dS_{c+1}, S_c>;  dsx[c] <- dS_{c+1};
+//   dS_c = exp(cum_end_c) dS_{c+1} + dSb_c.  ds0 = dS_0.
+__global__ void __launch_bounds__(kThreads) k_bwd_pass(const float* states, float* dsx, const float* cum_end,
+                                                       const float* ds_final, float* ds0, float* dcum_end4, int H,
+                                                       int nc, int PN) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  __shared__ float red[32];
+  const size_t unit = (size_t)b * H + h;
+  float* dS = ds0 + unit * PN;  // running state gradient lives in the output
+  for (int e = threadIdx.x; e < PN; e += blockDim.x) dS[e] = ds_final[unit * PN + e];
+  for (int c = nc - 1; c >= 0; --c) {
+    const float a = expf(cum_end[unit * nc + c]);
+    const float* Sc = states + (unit * nc + c) * PN;
+    float* dx_c = dsx + (unit * nc + c) * PN;
+    float part = 0.f;
+    for (int e = threadIdx.x; e < PN; e += blockDim.x) part += dS[e] * Sc[e];
+    const float tot = block_sum_t0(part, red);
+    if (threadIdx.x == 0) dcum_end4[unit * nc + c] = a * tot;
+    for (int e = threadIdx.x; e < PN; e += blockDim.x) {
+      const float blue = dx_c[e];
+      const float d = dS[e];
+      dx_c[e] = d;
+      dS[e] = a * d + blue;
+    }
+  }
+}
+
+// Everything else of one chunk's backward, given S_c and dS_{c+1}:
+//   rows i:    dCB[i,:] = dW o decay, d_diff = dW o CB o decay (row sums),
+//              dC[i,:] = dCB[i,:] B + exp(cum_i) dy[i,:] S_c (+ BLUE d cum)
+//   columns j: dv[j,:] = W[:,j]^T dy + exp(cum_end - cum_j) B[j,:] dS^T,
+//              dB[j,:] = dCB[:,j]^T C + exp(cum_end - cum_j) v[j,:] dS,
+//              column sums of d_diff, K3's decay gradient
+//   then K1 backward (suffix sums) and the chain rule to the leaves.
+template <typename TIn, bool MIMO>
+__global__ void __launch_bounds__(kThreads)
+    k_chunk_bwd(Seq<TIn, MIMO> s, const TIn* dy, const float* states, const float* dsx, const float* dcum_end4,
+                float* dv_ws, TIn* dx, float* ddt_or_dda, float* dB_dst, float* dC_dst, TIn* dB_io, TIn* dC_io,
+                float* dA_part) {
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int L = s.L, R = s.R, LR = s.LR, P = s.P, N = s.N;
+  extern __shared__ float sm[];
+  float* s_cum = sm;
+  float* s_dtp = s_cum + L;
+  float* s_dec = s_dtp + L;      // exp(cum_end - cum_l)
+  float* s_dcumf = s_dec + L;    // d cum per fused position [LR]
+  float* s_row = s_dcumf + LR;   // [LR]
+  float* s_row2 = s_row + LR;    // [LR]
+  float* s_red = s_row2 + LR;    // [max(P, N, 32)]
+  float* s_dda = s_red + 256;    // [L]
+  chunk_scalars(s, b, h, c, s_cum, s_dtp);
+  for (int l = threadIdx.x; l < L; l += blockDim.x) s_dec[l] = expf(s_cum[L - 1] - s_cum[l]);
+  for (int i = threadIdx.x; i < LR; i += blockDim.x) s_dcumf[i] = 0.f;
+  __syncthreads();
+  const size_t unit = (size_t)b * s.H + h;
+  const float* Sc = states + (unit * s.nc + c) * P * N;
+  const float* dSn = dsx + (unit * s.nc + c) * P * N;
+  auto t_of = [&](int i) { return c * L + i / R; };
+
+  // ---- rows: ORANGE's dCB and d_diff, BLUE's dC, K2's dC
+  float col_diff = 0.f;  // column sum of d_diff for j = threadIdx.x
+  for (int i = 0; i < LR; ++i) {
+    const int li = i / R, ri = i % R, ti = t_of(i);
+    const int j = threadIdx.x;
+    if (j < LR) {
+      const int lj = j / R, rj = j % R, tj = t_of(j);
+      float dcb = 0.f, dd = 0.f;
+      if (lj <= li) {
+        float dW = 0.f, cb = 0.f;
+        for (int p = 0; p < P; ++p) dW += ld(dy, s.xi(b, ti, ri, h, p)) * s.v(b, tj, rj, h, p, s_dtp[lj]);
+        for (int n = 0; n < N; ++n) cb += s.Cm(b, ti, ri, h, n) * s.Bm(b, tj, rj, h, n);
+        const float dec = expf(s_cum[li] - s_cum[lj]);
+        dcb = dW * dec;
+        dd = dcb * cb;
+      }
+      s_row[j] = dcb;
+      s_row2[j] = dd;
+      col_diff += dd;
+    }
+    __syncthreads();
+    const float eci = expf(s_cum[li]);
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      float k2 = 0.f;
+      for (int jj = 0; jj < (li + 1) * R; ++jj) k2 += s_row[jj] * s.Bm(b, t_of(jj), jj % R, h, n);
+      float blue = 0.f;
+      for (int p = 0; p < P; ++p) blue += ld(dy, s.xi(b, ti, ri, h, p)) * Sc[p * N + n];
+      blue *= eci;
+      const float v = k2 + blue;
+      if (MIMO) st(dC_io, s.bi(b, ti, ri, h, n), v);
+      else dC_dst[(((size_t)b * s.T + ti) * s.H + h) * N + n] = v;
+      s_red[n] = s.Cm(b, ti, ri, h, n) * blue;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float acc = 0.f;
+      for (int jj = 0; jj < LR; ++jj) acc += s_row2[jj];
+      for (int n = 0; n < N; ++n) acc += s_red[n];
+      s_dcumf[i] += acc;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < LR) s_dcumf[threadIdx.x] -= col_diff;
+  __syncthreads();
+
+  // ---- columns: ORANGE's dv, K3's dv and dB, K2's dB, K3's decay gradient
+  float d_last = 0.f;  // thread 0: gradient of cum_end from K3
+  for (int j = 0; j < LR; ++j) {
+    const int lj = j / R, rj = j % R, tj = t_of(j);
+    const int i = threadIdx.x;
+    if (i < LR) {
+      const int li = i / R, ri = i % R, ti = t_of(i);
+      float w = 0.f, dcb = 0.f;
+      if (lj <= li) {
+        float dW = 0.f, cb = 0.f;
+        for (int p = 0; p < P; ++p) dW += ld(dy, s.xi(b, ti, ri, h, p)) * s.v(b, tj, rj, h, p, s_dtp[lj]);
+        for (int n = 0; n < N; ++n) cb += s.Cm(b, ti, ri, h, n) * s.Bm(b, tj, rj, h, n);
+        const float dec = expf(s_cum[li] - s_cum[lj]);
+        w = cb * dec;
+        dcb = dW * dec;
+      }
+      s_row[i] = w;
+      s_row2[i] = dcb;
+    }
+    __syncthreads();
+    const float dec_end = s_dec[lj];
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+      float dvo = 0.f;
+      for (int ii = lj * R; ii < LR; ++ii) dvo += s_row[ii] * ld(dy, s.xi(b, t_of(ii), ii % R, h, p));
+      float ddv = 0.f;  // d decayed_v
+      for (int n = 0; n < N; ++n) ddv += s.Bm(b, tj, rj, h, n) * dSn[p * N + n];
+      const float dvv = dvo + dec_end * ddv;
+      if (MIMO) st(dx, s.xi(b, tj, rj, h, p), dvv);
+      else dv_ws[s.xi(b, tj, rj, h, p)] = dvv;
+      s_red[p] = ddv * s.v(b, tj, rj, h, p, s_dtp[lj]);
+    }
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      float k2 = 0.f;
+      for (int ii = lj * R; ii < LR; ++ii) k2 += s_row2[ii] * s.Cm(b, t_of(ii), ii % R, h, n);
+      float k3 = 0.f;
+      for (int p = 0; p < P; ++p) k3 += s.v(b, tj, rj, h, p, s_dtp[lj]) * dSn[p * N + n];
+      const float v = k2 + dec_end * k3;
+      if (MIMO) st(dB_io, s.bi(b, tj, rj, h, n), v);
+      else dB_dst[(((size_t)b * s.T + tj) * s.H + h) * N + n] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float acc = 0.f;
+      for (int p = 0; p < P; ++p) acc += s_red[p];
+      const float dd = acc * dec_end;  // d(cum_end - cum_j)
+      s_dcumf[j] -= dd;
+      d_last += dd;
+    }
+    __syncthreads();
+  }
+
+  // ---- fold fused positions onto steps, add K4's term, K1 backward
+  if (threadIdx.x == 0) {
+    for (int l = 0; l < L; ++l) {
+      float acc = 0.f;
+      for (int r = 0; r < R; ++r) acc += s_dcumf[l * R + r];
+      s_dda[l] = acc;
+    }
+    s_dda[L - 1] += d_last + dcum_end4[unit * s.nc + c];
+    float suf = 0.f;
+    for (int l = L - 1; l >= 0; --l) {
+      suf += s_dda[l];
+      s_dda[l] = suf;
+    }
+  }
+  __syncthreads();
+
+  // ---- leaves
+  if (MIMO) {
+    for (int l = threadIdx.x; l < L; l += blockDim.x) ddt_or_dda[s.ti(b, c * L + l, h)] = s_dda[l];
+  } else {
+    for (int e = threadIdx.x; e < L * P; e += blockDim.x) {
+      const int l = e / P, p = e % P;
+      const size_t idx = s.xi(b, c * L + l, 0, h, p);
+      st(dx, idx, s_dtp[l] * dv_ws[idx]);
+    }
+    for (int l = threadIdx.x; l < L; l += blockDim.x) {
+      const int t = c * L + l;
+      float acc = 0.f;
+      for (int p = 0; p < P; ++p) {
+        const size_t idx = s.xi(b, t, 0, h, p);
+        acc += dv_ws[idx] * ld(s.x, idx);
+      }
+      const float ddtp = acc + s.A[h] * s_dda[l];
+      const float z = s.dt[s.ti(b, t, h)];
+      ddt_or_dda[s.ti(b, t, h)] = ddtp * sigmoid_f(z);
+    }
+    if (threadIdx.x == 0) {
+      float acc = 0.f;
+      for (int l = 0; l < L; ++l) acc += s_dda[l] * s_dtp[l];
+      dA_part[unit * s.nc + c] = acc;
+    }
+  }
+}
+
+// dB[b,t,g,n] = sum over the heads of g, ascending, of the per-head parts.
+template <typename TIn>
+__global__ void k_group_sum(const float* part, TIn* out, int b, int T, int H, int G, int N) {
+  const size_t total = (size_t)b * T * G * N;
+  const int hpg = H / G;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int n = e % N;
+    const size_t bt = e / N / G;
+    const int g = (e / N) % G;
+    float acc = 0.f;
+    for (int k = 0; k < hpg; ++k) acc += part[(bt * H + g * hpg + k) * N + n];
+    st(out, e, acc);
+  }
+}
+
+// dA[h] = sum over b (ascending), then chunks (ascending), of the parts.
+__global__ void k_dA_sum(const float* part, float* dA, int b, int H, int nc) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= H) return;
+  float acc = 0.f;
+  for (int bb = 0; bb < b; ++bb)
+    for (int c = 0; c < nc; ++c) acc += part[((size_t)bb * H + h) * nc + c];
+  dA[h] = acc;
+}
+
+template <typename TIn, bool MIMO>
+Seq<TIn, MIMO> make_seq(const Dims& d, const void* x, const float* dt, const float* A, const void* B,
+                        const void* C) {
+  Seq<TIn, MIMO> s;
+  s.x = static_cast<const TIn*>(x);
+  s.dt = dt;
+  s.A = A;
+  s.B = static_cast<const TIn*>(B);
+  s.C = static_cast<const TIn*>(C);
+  s.T = d.T; s.H = d.H; s.P = d.P; s.N = d.N; s.G = d.G; s.L = d.L; s.R = d.R; s.LR = d.LR; s.nc = d.nc;
+  s.hpg = d.hpg;
+  return s;
+}
+
+struct FwdWs {
+  float* states;   // [b,H,nc,P,N]
+  float* cum_end;  // [b,H,nc]
+};
+
+FwdWs carve_fwd(const Dims& d, Carver& cv) {
+  FwdWs w;
+  w.states = cv.take<float>((size_t)d.b * d.H * d.nc * d.P * d.N);
+  w.cum_end = cv.take<float>((size_t)d.b * d.H * d.nc);
+  return w;
+}
+
+struct BwdWs {
+  FwdWs f;
+  float* dsx;        // [b,H,nc,P,N]
+  float* dcum_end4;  // [b,H,nc]
+  float* dv;         // Mamba-2 [b,T,H,P]
+  float* dB_part;    // Mamba-2 [b,T,H,N]
+  float* dC_part;
+  float* dA_part;    // [b,H,nc]
+};
+
+BwdWs carve_bwd(const Dims& d, Carver& cv) {
+  BwdWs w;
+  w.f = carve_fwd(d, cv);
+  w.dsx = cv.take<float>((size_t)d.b * d.H * d.nc * d.P * d.N);
+  w.dcum_end4 = cv.take<float>((size_t)d.b * d.H * d.nc);
+  const bool m2 = d.variant == kMamba2;
+  w.dv = cv.take<float>(m2 ? (size_t)d.b * d.T * d.H * d.P : 0);
+  w.dB_part = cv.take<float>(m2 ? (size_t)d.b * d.T * d.H * d.N : 0);
+  w.dC_part = cv.take<float>(m2 ? (size_t)d.b * d.T * d.H * d.N : 0);
+  w.dA_part = cv.take<float>((size_t)d.b * d.H * d.nc);
+  return w;
+}
+
+template <typename TIn, bool MIMO>
+cudaError_t forward_impl(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st) {
+  Carver cv(ws);
+  FwdWs w = carve_fwd(d, cv);
+  auto s = make_seq<TIn, MIMO>(d, a.x, a.dt_raw, a.A, a.B, a.C);
+  const dim3 gc(d.nc, d.H, d.b);
+  SSD_LAUNCH("k_chunk_state", st,
+             k_chunk_state<TIn, MIMO><<<gc, kThreads, 3 * d.L * sizeof(float), st>>>(s, w.states, w.cum_end));
+  SSD_LAUNCH("k_state_pass", st,
+             k_state_pass<<<dim3(d.H, d.b), kThreads, 0, st>>>(w.states, w.cum_end, a.s0, a.s_final, d.H, d.nc, d.P * d.N));
+  SSD_LAUNCH("k_chunk_out", st,
+             k_chunk_out<TIn, MIMO><<<gc, kThreads, (2 * d.L + d.LR) * sizeof(float), st>>>(s, w.states,
+                                                                                  static_cast<TIn*>(a.y)));
+  return cudaGetLastError();
+}
+
+template <typename TIn, bool MIMO>
+cudaError_t backward_impl(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st) {
+  Carver cv(ws);
+  BwdWs w = carve_bwd(d, cv);
+  auto s = make_seq<TIn, MIMO>(d, a.x, a.dt_raw, a.A, a.B, a.C);
+  const dim3 gc(d.nc, d.H, d.b);
+  const int PN = d.P * d.N;
+  // replay K1, K3, K4 from the leaf inputs
+  SSD_LAUNCH("k_chunk_state", st,
+             k_chunk_state<TIn, MIMO><<<gc, kThreads, 3 * d.L * sizeof(float), st>>>(s, w.f.states, w.f.cum_end));
+  SSD_LAUNCH("k_dS_blue", st,
+             k_dS_blue<TIn, MIMO><<<gc, kThreads, 3 * d.L * sizeof(float), st>>>(s, static_cast<const TIn*>(a.dy), w.dsx));
+  // the K4 replay writes s_final into ds0, which k_bwd_pass then overwrites with the real ds0
+  SSD_LAUNCH("k_state_pass", st,
+             k_state_pass<<<dim3(d.H, d.b), kThreads, 0, st>>>(w.f.states, w.f.cum_end, a.s0, a.ds0, d.H, d.nc, PN));
+  SSD_LAUNCH("k_bwd_pass", st,
+             k_bwd_pass<<<dim3(d.H, d.b), kThreads, 0, st>>>(w.f.states, w.dsx, w.f.cum_end, a.ds_final, a.ds0, w.dcum_end4,
+                                                  d.H, d.nc, PN));
+  const size_t smem = (3 * d.L + 3 * d.LR + 256 + d.L) * sizeof(float);
+  SSD_LAUNCH("k_chunk_bwd", st,
+             k_chunk_bwd<TIn, MIMO><<<gc, kThreads, smem, st>>>(
+      s, static_cast<const TIn*>(a.dy), w.f.states, w.dsx, w.dcum_end4, w.dv, static_cast<TIn*>(a.dx), a.ddt_raw,
+      w.dB_part, w.dC_part, static_cast<TIn*>(a.dB), static_cast<TIn*>(a.dC), w.dA_part));
+  if (!MIMO) {
+    const size_t tot = (size_t)d.b * d.T * d.G * d.N;
+    const int blocks = (int)((tot + 255) / 256 < 65535 ? (tot + 255) / 256 : 65535);
+    SSD_LAUNCH("k_group_sum", st,
+               k_group_sum<TIn><<<blocks, 256, 0, st>>>(w.dB_part, static_cast<TIn*>(a.dB), d.b, d.T, d.H, d.G, d.N));
+    SSD_LAUNCH("k_group_sum", st,
+               k_group_sum<TIn><<<blocks, 256, 0, st>>>(w.dC_part, static_cast<TIn*>(a.dC), d.b, d.T, d.H, d.G, d.N));
+    SSD_LAUNCH("k_dA_sum", st,
+               k_dA_sum<<<(d.H + 127) / 128, 128, 0, st>>>(w.dA_part, a.dA, d.b, d.H, d.nc));
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t simt_forward_ws(const Dims& d) {
+  Carver cv(nullptr);
+  carve_fwd(d, cv);
+  return cv.off;
+}
+
+size_t simt_backward_ws(const Dims& d) {
+  Carver cv(nullptr);
+  carve_bwd(d, cv);
+  return cv.off;
+}
+
+cudaError_t simt_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st) {
+  if (d.variant == kMimo)
+    return d.bf16 ? forward_impl<__nv_bfloat16, true>(d, a, ws, st) : forward_impl<float, true>(d, a, ws, st);
+  return d.bf16 ? forward_impl<__nv_bfloat16, false>(d, a, ws, st) : forward_impl<float, false>(d, a, ws, st);
+}
+
+cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st) {
+  if (d.variant == kMimo)
+    return d.bf16 ? backward_impl<__nv_bfloat16, true>(d, a, ws, st) : backward_impl<float, true>(d, a, ws, st);
+  return d.bf16 ? backward_impl<__nv_bfloat16, false>(d, a, ws, st) : backward_impl<float, false>(d, a, ws, st);
+}
+
+}  // namespace ssd

@@ -1,0 +1,119 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+symbol the header declares, and validates its arguments on the host (no
+kernel is launched by any call here: every call fails validation first)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from selective_state_space_ssd_gb300 import binding
+from selective_state_space_ssd_gb300.configs import CONFIGS, scaled
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_loads_and_exports_every_declared_symbol(cuda_lib):
+    for name in declared_functions():
+        assert hasattr(cuda_lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (ssd_[a-z_]+)\b", out))
+    assert set(declared_functions()) <= exported
+    assert cuda_lib.ssd_version() >= 100
+
+
+def test_library_is_built_for_sm_103a():
+    out = subprocess.run(["cuobjdump", "--list-elf", binding.library_path()], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_status_strings(cuda_lib):
+    for code in range(0, 9):
+        s = binding.ssd_status_string(code)
+        assert s.startswith("SSD_")
+    assert binding.ssd_status_string(99) == "SSD_ERR_UNKNOWN"
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_workspace_query_accepts_every_config(cuda_lib, name):
+    p = binding.problem(CONFIGS[name])
+    fwd = binding.ssd_workspace_size(p, False)
+    bwd = binding.ssd_workspace_size(p, True)
+    assert fwd >= 0 and bwd > 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(seqlen=100), 2),                  # T % chunk != 0
+    (dict(ngroups=3), 2),                   # H % G != 0
+    (dict(headdim=0), 2),
+    (dict(dstate=300), 2),                  # beyond this build's limit
+    (dict(chunk=128), 2),                   # chunk > T is not allowed (T = 64)
+])
+def test_shape_validation(cuda_lib, over, code):
+    cfg = scaled(CONFIGS["mamba2_tiny_fp32"], **over)
+    p = binding.problem(cfg)
+    n = ctypes.c_size_t(0)
+    assert cuda_lib.ssd_workspace_size(ctypes.byref(p), 0, ctypes.byref(n)) == code
+
+
+def test_variant_specific_validation(cuda_lib):
+    n = ctypes.c_size_t(0)
+    m1 = binding.problem(scaled(CONFIGS["mamba1_fp32"], dtype="bf16"))
+    assert cuda_lib.ssd_workspace_size(ctypes.byref(m1), 1, ctypes.byref(n)) == 3  # SSD_ERR_DTYPE
+    m1 = binding.problem(scaled(CONFIGS["mamba1_fp32"], headdim=2))
+    assert cuda_lib.ssd_workspace_size(ctypes.byref(m1), 1, ctypes.byref(n)) == 2
+    bad = binding.problem(CONFIGS["mamba2_tiny_fp32"])
+    bad.variant = 7
+    assert cuda_lib.ssd_workspace_size(ctypes.byref(bad), 1, ctypes.byref(n)) == 1
+    assert cuda_lib.ssd_workspace_size(None, 1, ctypes.byref(n)) == 1
+
+
+def test_pointer_validation_launches_nothing(cuda_lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("uses fake device addresses; host-only check")
+    p = binding.problem(CONFIGS["mamba2_tiny_fp32"])
+    fake = 1 << 20  # never dereferenced: validation rejects the call first
+    # NULL required buffer
+    st = cuda_lib.ssd_forward(ctypes.byref(p), None, fake, fake, fake, fake, None, fake, fake, fake, 1 << 30, None)
+    assert st == 1
+    # misaligned buffer
+    st = cuda_lib.ssd_forward(ctypes.byref(p), fake + 4, fake, fake, fake, fake, None, fake, fake, fake, 1 << 30,
+                              None)
+    assert st == 4
+    # workspace too small
+    need = binding.ssd_workspace_size(p, False)
+    st = cuda_lib.ssd_forward(ctypes.byref(p), fake, fake, fake, fake, fake, None, fake, fake, fake, need - 1, None)
+    assert st == 5
+    # MIMO requires A == NULL and dA == NULL
+    pm = binding.problem(CONFIGS["mimo_r4_bf16"])
+    st = cuda_lib.ssd_forward(ctypes.byref(pm), fake, fake, fake, fake, fake, None, fake, fake, fake, 1 << 40, None)
+    assert st == 1
+    need = binding.ssd_workspace_size(p, True)
+    # prob, dy, ds_final, x, dt_raw, A, B, C, s0, dx, ddt_raw, dA, dB, dC, ds0, ws, ws_bytes, stream
+    st = cuda_lib.ssd_backward(ctypes.byref(p), fake, None, fake, fake, fake, fake, fake, None,
+                               fake, fake, fake, fake, fake, fake, fake, need, None)
+    assert st == 1  # ds_final is required: it is the seed of the reverse recurrence
+    st = cuda_lib.ssd_backward(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, None,
+                               fake, fake, fake, fake, fake, fake, fake, need - 1, None)
+    assert st == 5

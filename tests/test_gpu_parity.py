@@ -1,0 +1,142 @@
+"""Parity of the CUDA library (called through its C ABI) with the float64
+oracle on the same seeded inputs, element by element, for every output.
+
+Small cases span several chunks and ragged sizes (head/state widths that are
+not multiples of any tile, odd head counts, several groups); the full-size
+cases run the five workloads exactly as the benchmark launches them.
+"""
+import numpy as np
+import pytest
+import torch
+
+from selective_state_space_ssd_gb300 import binding
+from selective_state_space_ssd_gb300 import inputs as synth
+from selective_state_space_ssd_gb300.configs import CONFIGS, scaled
+
+from parity import compare, run_gpu, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+M2_BF16 = CONFIGS["mamba2_130m_bf16"]
+MIMO = CONFIGS["mimo_r4_bf16"]
+M1 = CONFIGS["mamba1_fp32"]
+
+SMALL = {
+    "tiny_fp32": CONFIGS["mamba2_tiny_fp32"],
+    "m2_fp32_ragged_groups": dict(variant="mamba2", dtype="f32", batch=2, seqlen=96, nheads=6, headdim=5, dstate=7,
+                                  ngroups=3, chunk=32, mimo_rank=1),
+    "m2_bf16_tiles": scaled(M2_BF16, batch=2, seqlen=256, nheads=4, ngroups=2),
+    "m2_bf16_ragged": scaled(M2_BF16, batch=1, seqlen=192, nheads=3, headdim=24, dstate=40, ngroups=1),
+    "m2_bf16_single_chunk": scaled(M2_BF16, batch=1, seqlen=64, nheads=2),
+    "m1_small": scaled(M1, batch=2, seqlen=256, nheads=40),
+    "m1_ragged": scaled(M1, batch=1, seqlen=96, nheads=37, dstate=5, chunk=32),
+    "mimo_bf16_tiles": scaled(MIMO, batch=1, seqlen=256, nheads=3, ngroups=3),
+    "mimo_ragged": scaled(MIMO, batch=2, seqlen=48, nheads=2, ngroups=2, headdim=20, dstate=24, chunk=16,
+                          mimo_rank=3),
+    "mimo_fp32": scaled(MIMO, dtype="f32", batch=1, seqlen=128, nheads=2, ngroups=2, headdim=16, dstate=32,
+                        chunk=32),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return cuda_lib
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_parity_small(name):
+    cfg = SMALL[name]
+    cpu = synth.make_inputs(cfg, seed=1)
+    gpu = run_gpu(cfg, to_device(cpu))
+    compare(cfg, gpu, run_oracle(cfg, cpu))
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "m2_bf16_tiles", "m1_small", "mimo_bf16_tiles"])
+def test_null_s0_equals_zero_state(name):
+    cfg = SMALL[name]
+    cpu = synth.make_inputs(cfg, seed=2, zero_s0=True)
+    dev = to_device(cpu)
+    a = run_gpu(cfg, dev, s0_null=True)
+    b = run_gpu(cfg, dev, s0_null=False)
+    for k in a:
+        if a[k] is not None:
+            assert torch.equal(a[k], b[k]), k
+    compare(cfg, a, run_oracle(cfg, cpu))
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "m2_bf16_tiles", "m1_small", "mimo_bf16_tiles"])
+def test_backward_is_bitwise_deterministic(name):
+    cfg = SMALL[name]
+    dev = to_device(synth.make_inputs(cfg, seed=3))
+    a = run_gpu(cfg, dev)
+    b = run_gpu(cfg, dev)
+    for k in a:
+        if a[k] is not None:
+            assert torch.equal(a[k], b[k]), k
+
+
+def test_zero_seed_and_zero_dy():
+    """dy = 0 leaves only the decayed seed: ds0 = exp(sum da) ds_final, dC = 0."""
+    cfg = SMALL["m2_bf16_tiles"]
+    cpu = synth.make_inputs(cfg, seed=4)
+    cpu["dy"] = torch.zeros_like(cpu["dy"])
+    gpu = run_gpu(cfg, to_device(cpu))
+    assert torch.count_nonzero(gpu["dC"]) == 0
+    compare(cfg, gpu, run_oracle(cfg, cpu))
+
+
+def test_chaining_two_calls_equals_one():
+    """Splitting T at a chunk boundary and chaining s_final -> s0 (forward) and
+    ds0 -> ds_final (backward) reproduces one call."""
+    cfg = SMALL["m2_bf16_tiles"]
+    cpu = synth.make_inputs(cfg, seed=5)
+    dev = to_device(cpu)
+    T0 = cfg["seqlen"] // 2
+    half = scaled(cfg, seqlen=T0)
+
+    def cut(t, lo, hi):
+        return t[:, lo:hi].contiguous()
+
+    first = {k: (v if k in ("A", "s0", "ds_final") else cut(v, 0, T0)) for k, v in dev.items()}
+    second = {k: (v if k in ("A", "s0", "ds_final") else cut(v, T0, cfg["seqlen"])) for k, v in dev.items()}
+    y1, s1 = binding.forward(half, first["x"], first["dt_raw"], first["A"], first["B"], first["C"], first["s0"])
+    y2, s2 = binding.forward(half, second["x"], second["dt_raw"], second["A"], second["B"], second["C"], s1)
+    g2 = binding.backward(half, second["dy"], second["ds_final"], second["x"], second["dt_raw"], second["A"],
+                          second["B"], second["C"], s1)
+    g1 = binding.backward(half, first["dy"], g2["ds0"], first["x"], first["dt_raw"], first["A"], first["B"],
+                          first["C"], first["s0"])
+    torch.cuda.synchronize()
+    chained = {"y": torch.cat([y1, y2], 1), "s_final": s2, "dx": torch.cat([g1["dx"], g2["dx"]], 1),
+               "ddt_raw": torch.cat([g1["ddt_raw"], g2["ddt_raw"]], 1), "dA": g1["dA"] + g2["dA"],
+               "dB": torch.cat([g1["dB"], g2["dB"]], 1), "dC": torch.cat([g1["dC"], g2["dC"]], 1),
+               "ds0": g1["ds0"]}
+    compare(cfg, chained, run_oracle(cfg, cpu))
+
+
+def _inner(a, b):
+    return float((a.double() * b.double()).sum())
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_full_size_parity(name):
+    """The workloads at their full sizes, in the configuration the benchmark
+    launches, against the oracle on every output.  MIMO compares batch 0 (its
+    sequences are independent and nothing is reduced across them); the others
+    run the whole oracle."""
+    cfg = CONFIGS[name]
+    cpu = synth.make_inputs(cfg, seed=0)
+    gpu = run_gpu(cfg, to_device(cpu))
+    if cfg["variant"] == "mimo":
+        one = scaled(cfg, batch=1)
+        ref = run_oracle(one, {k: (None if v is None else v[:1]) for k, v in cpu.items()})
+        gpu = {k: (None if v is None else v[:1]) for k, v in gpu.items()}
+        compare(one, gpu, ref)
+    else:
+        compare(cfg, gpu, run_oracle(cfg, cpu))
+    # homogeneity identities hold for any correct VJP at any size
+    dev = to_device(cpu)
+    lhs = _inner(dev["dy"], gpu["y"]) if cfg["variant"] != "mimo" else None
+    if lhs is not None:
+        scale = float((dev["dy"].double().abs() * gpu["y"].double().abs()).sum())
+        assert abs(lhs - _inner(gpu["dC"], dev["C"])) < 3e-2 * scale
