@@ -100,6 +100,9 @@ def kernel_bytes(name, cfg):
                         + (2 * part if m2 else t["B"] + t["C"]) + small),
         "k_group_sum": part + t["B"],
         "k_dA_sum": small + t["A"],
+        # tensor-core kernels: the leaf inputs and outputs of the call they serve
+        "k_tc_fwd": t["x"] + dtb + t["A"] + t["B"] + t["C"] + t["s0"] + t["x"] + t["s0"],
+        "k_tc_bwd": 3 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 3 * t["s0"] + dtb,
         "k_m1_forward": 2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 2 * t["s0"],
         "k_m1_backward": 2 * t["x"] + 2 * dtb + t["A"] + t["B"] + t["C"] + 3 * t["s0"] + t["x"]
                          + 2 * b * T * H * N * 4 + b * H * N * 4 + b * H * (T // L) * N * 4,
@@ -107,6 +110,15 @@ def kernel_bytes(name, cfg):
         "k_m1_dA_sum": b * H * N * 4 + t["A"],
     }
     return table.get(name)
+
+
+def path_dtype(cfg):
+    """Arithmetic type of the timed path: bf16 tensor-core MMAs (fp32
+    accumulate) for the Mamba-2 bf16 shapes the tcgen05 kernels serve, fp32
+    CUDA-core arithmetic otherwise."""
+    tc = (cfg["variant"] == "mamba2" and cfg["dtype"] == "bf16" and cfg["chunk"] == 64 and cfg["headdim"] == 64
+          and cfg["dstate"] == 128)
+    return "bf16" if tc else "f32"
 
 
 def peaks():
@@ -429,7 +441,7 @@ def main():
                  "frac": max(t_hbm, t_tc) / step_s}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32",
+            "vs_baseline": None, "dtype": path_dtype(cfg),
             "data": "synthetic (seeded; the recipe of the pages' workloads)",
             "config": dict(wdesc, l2="flushed before every timed step (516 MB write, outside the timed interval)"),
             "roofline": roofline, "roofline_step": roof_step,

@@ -129,7 +129,11 @@ ssd_status ssd_workspace_size(const ssd_problem* prob, int backward, size_t* byt
  * s0 may be NULL (a zero initial state).  Every other pointer is required
  * (except A for MIMO) and must be 16-byte aligned.
  * ws / ws_bytes: caller-owned device workspace of at least
- * ssd_workspace_size(prob, 0) bytes (ws may be NULL when that size is 0).
+ * ssd_workspace_size(prob, 0) bytes (always >= 256, never NULL).  Its first
+ * 4 bytes are a device status word (int32): the call resets it to 0, and a
+ * kernel whose bounded wait on an internal barrier gives up writes a nonzero
+ * code there (the outputs are then invalid).  Read it after the stream
+ * reaches the call if that check is wanted.
  */
 ssd_status ssd_forward(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
                        const void* B, const void* C, const float* s0, void* y, float* s_final, void* ws,
@@ -149,7 +153,8 @@ ssd_status ssd_forward(const ssd_problem* prob, const void* x, const float* dt_r
  * channels) and dA (over batch and time) are full reductions written once.
  * MIMO: dx returns dv, ddt_raw returns d(da), and dA must be NULL.
  * s0 may be NULL (zero initial state); ds0 is still written.
- * ws / ws_bytes: at least ssd_workspace_size(prob, 1) bytes.
+ * ws / ws_bytes: at least ssd_workspace_size(prob, 1) bytes, with the same
+ * device status word in its first 4 bytes as for ssd_forward.
  */
 ssd_status ssd_backward(const ssd_problem* prob, const void* dy, const float* ds_final, const void* x,
                         const float* dt_raw, const float* A, const void* B, const void* C, const float* s0,

@@ -69,6 +69,8 @@ ssd_status make_dims(const ssd_problem* pr, Dims* d) {
 
 size_t ws_bytes(const Dims& d, bool backward) {
   if (d.variant == kMamba1) return backward ? m1_backward_ws(d) : m1_forward_ws(d);
+  if (!backward && tc_forward_supported(d)) return tc_forward_ws(d);
+  if (backward && tc_backward_supported(d)) return tc_backward_ws(d);
   return backward ? simt_backward_ws(d) : simt_forward_ws(d);
 }
 
@@ -191,13 +193,14 @@ ssd_status ssd_forward(const ssd_problem* prob, const void* x, const float* dt_r
   if (s != SSD_OK) return s;
   const size_t need = ws_bytes(d, false);
   if (ws_bytes_given < need) return SSD_ERR_WORKSPACE;
-  if (need > 0) {
-    if (!ws) return SSD_ERR_INVALID_ARG;
-    if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
-  }
+  if (!ws) return SSD_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
   FwdArgs a{x, dt_raw, A, B, C, s0, y, s_final};
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  cudaError_t e = d.variant == kMamba1 ? m1_forward(d, a, ws, st) : simt_forward(d, a, ws, st);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  cudaError_t e = d.variant == kMamba1        ? m1_forward(d, a, ws, st)
+                  : tc_forward_supported(d) ? tc_forward(d, a, ws, st)
+                                            : simt_forward(d, a, ws, st);
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
@@ -217,13 +220,14 @@ ssd_status ssd_backward(const ssd_problem* prob, const void* dy, const float* ds
   if (s != SSD_OK) return s;
   const size_t need = ws_bytes(d, true);
   if (ws_bytes_given < need) return SSD_ERR_WORKSPACE;
-  if (need > 0) {
-    if (!ws) return SSD_ERR_INVALID_ARG;
-    if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
-  }
+  if (!ws) return SSD_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
   BwdArgs a{dy, ds_final, x, dt_raw, A, B, C, s0, dx, ddt_raw, dA, dB, dC, ds0};
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  cudaError_t e = d.variant == kMamba1 ? m1_backward(d, a, ws, st) : simt_backward(d, a, ws, st);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  cudaError_t e = d.variant == kMamba1         ? m1_backward(d, a, ws, st)
+                  : tc_backward_supported(d) ? tc_backward(d, a, ws, st)
+                                             : simt_backward(d, a, ws, st);
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

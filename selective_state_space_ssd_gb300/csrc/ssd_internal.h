@@ -1,6 +1,7 @@
 // Internal host/device interface of the scan library (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -49,11 +50,17 @@ struct BwdArgs {
   float* ds0;
 };
 
-// Carves a caller-owned workspace into 256-byte aligned pieces.  The same
-// code sizes the workspace (base == nullptr) and hands out the pointers.
+// The first kStatusBytes of every workspace hold the device status word
+// (int32 at offset 0): each call resets it to 0, and a kernel whose bounded
+// wait gives up writes a nonzero code there.
+constexpr size_t kStatusBytes = 256;
+
+// Carves a caller-owned workspace into 256-byte aligned pieces after the
+// status word.  The same code sizes the workspace (base == nullptr) and hands
+// out the pointers.
 struct Carver {
   char* base;
-  size_t off = 0;
+  size_t off = kStatusBytes;
   explicit Carver(void* b) : base(static_cast<char*>(b)) {}
   template <typename T>
   T* take(size_t count) {
@@ -69,6 +76,20 @@ size_t simt_forward_ws(const Dims& d);
 size_t simt_backward_ws(const Dims& d);
 cudaError_t simt_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
+
+// Tensor-core path (Mamba-2, bf16 io, L = 64, P = 64, N = 128).
+bool tc_forward_supported(const Dims& d);
+size_t tc_forward_ws(const Dims& d);
+cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
+bool tc_backward_supported(const Dims& d);
+size_t tc_backward_ws(const Dims& d);
+cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
+
+// TMA tensor maps over bf16 tensors with 128-byte swizzle (tma_host.cu).
+cudaError_t make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                              uint32_t box_outer);
+cudaError_t make_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+                              uint32_t b1, uint32_t b2);
 
 // Mamba-1 path (fp32).
 size_t m1_forward_ws(const Dims& d);

@@ -180,7 +180,7 @@ M1Ws carve_m1(const Dims& d, Carver& cv) {
 
 }  // namespace
 
-size_t m1_forward_ws(const Dims&) { return 0; }
+size_t m1_forward_ws(const Dims&) { return kStatusBytes; }
 
 size_t m1_backward_ws(const Dims& d) {
   Carver cv(nullptr);

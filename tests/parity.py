@@ -19,12 +19,26 @@ def to_device(inp: dict, device="cuda") -> dict:
     return {k: (None if v is None else v.to(device)) for k, v in inp.items()}
 
 
+def zero_workspace(cfg: dict, backward: bool, device="cuda"):
+    prob = binding.problem(cfg)
+    n = binding.ssd_workspace_size(prob, backward)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device), n
+
+
+def status_word(ws) -> int:
+    """The device status word kept in the first 4 bytes of the workspace."""
+    return int(ws[:4].view(torch.int32).item())
+
+
 def run_gpu(cfg: dict, dev_inputs: dict, s0_null: bool = False) -> dict:
     t = dev_inputs
     s0 = None if s0_null else t["s0"]
-    y, sf = binding.forward(cfg, t["x"], t["dt_raw"], t["A"], t["B"], t["C"], s0)
-    g = binding.backward(cfg, t["dy"], t["ds_final"], t["x"], t["dt_raw"], t["A"], t["B"], t["C"], s0)
+    wsf = zero_workspace(cfg, False)
+    wsb = zero_workspace(cfg, True)
+    y, sf = binding.forward(cfg, t["x"], t["dt_raw"], t["A"], t["B"], t["C"], s0, workspace=wsf)
+    g = binding.backward(cfg, t["dy"], t["ds_final"], t["x"], t["dt_raw"], t["A"], t["B"], t["C"], s0, workspace=wsb)
     torch.cuda.synchronize()
+    assert status_word(wsf[0]) == 0 and status_word(wsb[0]) == 0, "a device-side bounded wait gave up"
     out = {"y": y, "s_final": sf}
     out.update(g)
     return out
