@@ -64,7 +64,8 @@ typedef enum {
   SSD_ERR_WORKSPACE = 5,   /* ws_bytes smaller than ssd_workspace_size() */
   SSD_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
   SSD_ERR_TIMEOUT = 7,     /* reserved: a bounded device-side wait gave up */
-  SSD_ERR_INTERNAL = 8     /* a device-side consistency check failed */
+  SSD_ERR_INTERNAL = 8,    /* a device-side consistency check failed */
+  SSD_ERR_TOO_LARGE = 9    /* ssd_forward_static: the problem needs more scratch than its fixed array */
 } ssd_status;
 
 typedef enum { SSD_MAMBA2 = 0, SSD_MAMBA1 = 1, SSD_MIMO = 2 } ssd_variant;
@@ -160,6 +161,36 @@ ssd_status ssd_backward(const ssd_problem* prob, const void* dy, const float* ds
                         const float* dt_raw, const float* A, const void* B, const void* C, const float* s0,
                         void* dx, float* ddt_raw, float* dA, void* dB, void* dC, float* ds0, void* ws,
                         size_t ws_bytes, void* cuda_stream);
+
+/*
+ * Forward scan without a caller workspace, for callers that cannot allocate
+ * device memory.  (The pages describe no such call; it is an addition of this
+ * library.)
+ *
+ * Who needs it: code that runs where device allocation is not available or
+ * not allowed once it has started, for example an inference engine or plugin
+ * whose host framework owns all GPU memory and hands out only the tensors, or
+ * a latency-critical loop that has a rule of no allocation after start-up.
+ * ssd_forward needs a workspace from ssd_workspace_size(); this call takes
+ * none.  Its scratch is one fixed array of 32 MiB in device memory, declared
+ * at file scope in the library, so every GPU that loads the library keeps
+ * those 32 MiB until the process exits.
+ *
+ * Arguments, layouts, results and validation are those of ssd_forward,
+ * without ws / ws_bytes.  A problem whose ssd_workspace_size(prob, 0) exceeds
+ * 32 MiB is rejected with SSD_ERR_TOO_LARGE before anything runs.  The call
+ * allocates nothing (no cudaMalloc, no allocating library routine).
+ *
+ * The first call on each device looks up that device's address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array, which keeps the
+ * last call's contents (the status word in its first 4 bytes is reset by
+ * every call): calls that may overlap on the GPU, on any streams, race on it
+ * and must be serialized by the caller.
+ */
+ssd_status ssd_forward_static(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
+                              const void* B, const void* C, const float* s0, void* y, float* s_final,
+                              void* cuda_stream);
 
 /*
  * Per-launch timing, for diagnostics and roofline measurement.

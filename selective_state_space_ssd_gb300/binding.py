@@ -40,8 +40,8 @@ class ssd_problem(ctypes.Structure):
                 ("mimo_rank", ctypes.c_int64)]
 
 
-EXPORTS = ("ssd_workspace_size", "ssd_forward", "ssd_backward", "ssd_profile_start", "ssd_profile_stop",
-           "ssd_status_string", "ssd_version")
+EXPORTS = ("ssd_workspace_size", "ssd_forward", "ssd_backward", "ssd_forward_static", "ssd_profile_start",
+           "ssd_profile_stop", "ssd_status_string", "ssd_version")
 
 
 class ssd_kernel_time(ctypes.Structure):
@@ -74,6 +74,8 @@ def load(path: str | None = None):
         lib.ssd_backward.restype = i32
         lib.ssd_status_string.argtypes = [i32]
         lib.ssd_status_string.restype = ctypes.c_char_p
+        lib.ssd_forward_static.argtypes = [ctypes.POINTER(ssd_problem)] + [vp] * 8 + [vp]
+        lib.ssd_forward_static.restype = i32
         lib.ssd_profile_start.argtypes = [i32]
         lib.ssd_profile_start.restype = i32
         lib.ssd_profile_stop.argtypes = [ctypes.POINTER(ssd_kernel_time), i32, ctypes.POINTER(i32)]
@@ -121,6 +123,15 @@ def ssd_forward(prob, x, dt_raw, A, B, C, s0, y, s_final, ws, ws_bytes, stream=N
                             _ptr(y), _ptr(s_final), _ptr(ws), int(ws_bytes), _stream(stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_forward")
+
+
+def ssd_forward_static(prob, x, dt_raw, A, B, C, s0, y, s_final, stream=None) -> None:
+    """Forward without a workspace: the library's fixed 32 MiB device array is
+    the scratch (see include/ssd.h).  Raises SSDError on a non-OK status."""
+    st = load().ssd_forward_static(ctypes.byref(prob), _ptr(x), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(s0),
+                                   _ptr(y), _ptr(s_final), _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_forward_static")
 
 
 def ssd_backward(prob, dy, ds_final, x, dt_raw, A, B, C, s0, dx, ddt_raw, dA, dB, dC, ds0, ws, ws_bytes,

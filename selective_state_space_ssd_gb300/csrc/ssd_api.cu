@@ -165,6 +165,8 @@ const char* ssd_status_string(ssd_status s) {
     case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
     case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded device-side wait gave up";
     case SSD_ERR_INTERNAL: return "SSD_ERR_INTERNAL: device-side consistency check failed";
+    case SSD_ERR_TOO_LARGE:
+      return "SSD_ERR_TOO_LARGE: the problem needs more scratch than the fixed 32 MiB array of ssd_forward_static";
   }
   return "SSD_ERR_UNKNOWN";
 }

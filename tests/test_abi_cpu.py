@@ -44,7 +44,7 @@ def test_library_is_built_for_sm_103a():
 
 
 def test_status_strings(cuda_lib):
-    for code in range(0, 9):
+    for code in range(0, 10):
         s = binding.ssd_status_string(code)
         assert s.startswith("SSD_")
     assert binding.ssd_status_string(99) == "SSD_ERR_UNKNOWN"
