@@ -81,6 +81,11 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_
 bool tc_forward_supported(const Dims& d);
 size_t tc_forward_ws(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
+size_t tc_fwd2_ws(const Dims& d);
+cudaError_t tc_forward2(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
+cudaError_t tc_cb_prepass(const Dims& d, const void* B, const void* C, float* CB, cudaStream_t st);
+cudaError_t tc_replay_states(const Dims& d, const void* x, const float* dt_raw, const float* A, const void* B,
+                             const float* s0, __nv_bfloat16* states, int* status, cudaStream_t st);
 bool tc_backward_supported(const Dims& d);
 size_t tc_backward_ws(const Dims& d);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);

@@ -7,8 +7,8 @@
 // chunk by chunk in the same pass.
 //
 // One CTA owns one (batch, head).
-//   replay:  K1, K3, K4 per chunk in order; each chunk-input state S_c is
-//            written (bf16) to the workspace by TMA store.
+//   replay:  a separate launch (the pipelined forward kernel in its states
+//            mode) writes every chunk-input state S_c (bf16) to the workspace.
 //   reverse: for c = nc-1 .. 0, with dS = dS_{c+1} (fp32 in registers):
 //     dS_blue^T = C^T dch          dch = exp(cum_t) dy     (BLUE: d state)
 //     dC        = dch S_c + dCB B                         (BLUE + K2)
@@ -183,65 +183,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t sbase = unit * kP * kN;
   uint32_t ph_in = 0, ph_s = 0, ph1 = 0, ph2 = 0;
   bool ok = true;
-
-  // ================================================================ replay
-#pragma unroll
-  for (int i = 0; i < 32; ++i) R[i] = prm.s0 ? prm.s0[sbase + (size_t)(p0 + i) * kN + n_own] : 0.f;
-  for (int c = 0; c < nc; ++c) {
-    if (tid == 0) {
-      fence_proxy_async();
-      mbar_expect_tx(&sm.bar_in, kTileLP + kTileLN);
-      tma_load_2d(sm.x, &tm_x, h * kP, row0 + c * kL, &sm.bar_in);
-      for (int a = 0; a < 2; ++a) tma_load_3d(sm.B + a * (kTileLN / 2), &tm_B, a * 64, g, row0 + c * kL, &sm.bar_in);
-    }
-    if (tid == 128) tma_store_wait_read0();  // previous S tile read out
-    chunk_scalars(sm, prm, row0, h, c, A_h);
-    // S_c (chunk input) -> bf16 tile -> workspace
-    store_row_bf16(sm.S, n_own, 4 * hh, R, 4);
-    ok = mbar_wait(&sm.bar_in, ph_in, prm.status, 11);
-    ph_in ^= 1;
-    for (int ch = tid; ch < kL * 8; ch += kThreads) {
-      const int t = ch >> 3, j = ch & 7;
-      float f[8];
-      load_chunk(sm.x, t, j, f);
-      const float d = sm.dtp[t] * sm.dec[t];
-      uint4 w;
-      w.x = pack_bf16(d * f[0], d * f[1]);
-      w.y = pack_bf16(d * f[2], d * f[3]);
-      w.z = pack_bf16(d * f[4], d * f[5]);
-      w.w = pack_bf16(d * f[6], d * f[7]);
-      *reinterpret_cast<uint4*>(sm.dvd + sw128_chunk(t, j)) = w;
-    }
-    fence_proxy_async();
-    if (__syncthreads_or(!ok)) break;
-    if (tid == 0) {
-      tc_fence_after();
-      constexpr uint32_t id = idesc_bf16(128, 64, true, true);
-#pragma unroll
-      for (int kk = 0; kk < kL; kk += 16) mma_bf16(T1, mdesc(sm.B, kL, kk), mdesc(sm.dvd, kL, kk), id, kk > 0);
-      mma_commit(&sm.bar_mma1);
-    }
-    if (tid == 128) {
-      tma_store_2d(&tm_S, sm.S, 0, srow0 + c * kN);
-      tma_store_commit();
-    }
-    ok = mbar_wait(&sm.bar_mma1, ph1, prm.status, 12);
-    ph1 ^= 1;
-    tc_fence_after();
-    {
-      float iv[32];
-      tmem_ld32(taddr(T1, 32 * q, p0), iv);
-      const float a = expf(sm.wsum[0] + sm.wsum[1]);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) R[i] = a * R[i] + iv[i];
-    }
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-  }
-  if (tid == 128) tma_store_wait0();
-  // states written by TMA are read back by TMA below
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  __syncthreads();
 
   // ================================================================ reverse
   // dS = ds_final (fp32 registers) and its bf16 tile
@@ -576,7 +517,8 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   TcBwdWs w = carve(d, cv);
   const uint64_t rows = (uint64_t)d.b * d.T;
   CUtensorMap tx, tdy, tdx, tb, tcm, ts;
-  cudaError_t e = make_tmap_2d_bf16(&tx, a.x, (uint64_t)d.H * kP, rows, 64, 64);
+  cudaError_t e = tc_replay_states(d, a.x, a.dt_raw, a.A, a.B, a.s0, w.states, static_cast<int*>(ws), st);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tx, a.x, (uint64_t)d.H * kP, rows, 64, 64);
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdy, a.dy, (uint64_t)d.H * kP, rows, 64, 64);
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdx, a.dx, (uint64_t)d.H * kP, rows, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d_bf16(&tb, a.B, d.N, d.G, rows, 64, 1, 64);

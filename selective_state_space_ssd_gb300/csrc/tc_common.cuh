@@ -160,5 +160,43 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t w) {
   return __bfloat1622float2(h);
 }
 
+// ------------------------------------------------------------ shared helpers
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// Named barrier that also ORs a predicate over the participating threads, so
+// a role's threads always agree on whether to stop after a bounded wait.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Descriptor of a K-major SW128 tile with `rows` rows at K offset kk.
+__device__ __forceinline__ uint64_t kdesc(const void* tile, int rows, int kk) {
+  return sdesc_sw128(smem_u32(tile) + (kk >> 6) * rows * 128 + (kk & 63) * 2, 0, 1024);
+}
+// Descriptor of an MN-major SW128 tile with `krows` K rows at K offset kk.
+__device__ __forceinline__ uint64_t mdesc(const void* tile, int krows, int kk) {
+  return sdesc_sw128(smem_u32(tile) + kk * 128, krows * 128, 1024);
+}
+
+// Stores nchunks x 8 floats as bf16 into row `row` of a SW128 tile, from
+// 16-byte chunk chunk0 on.
+__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int row, int chunk0, const float* v, int nchunks) {
+#pragma unroll
+  for (int j = 0; j < nchunks; ++j) {
+    uint4 w;
+    w.x = pack_bf16(v[8 * j + 0], v[8 * j + 1]);
+    w.y = pack_bf16(v[8 * j + 2], v[8 * j + 3]);
+    w.z = pack_bf16(v[8 * j + 4], v[8 * j + 5]);
+    w.w = pack_bf16(v[8 * j + 6], v[8 * j + 7]);
+    *reinterpret_cast<uint4*>(tile + sw128_chunk(row, chunk0 + j)) = w;
+  }
+}
+
+
 }  // namespace tc
 }  // namespace ssd
