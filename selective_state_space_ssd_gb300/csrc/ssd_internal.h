@@ -79,16 +79,14 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_
 
 // Tensor-core path (Mamba-2, bf16 io, L = 64, P = 64, N = 128).
 bool tc_forward_supported(const Dims& d);
-size_t tc_forward_ws(const Dims& d);
-cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
 size_t tc_fwd2_ws(const Dims& d);
 cudaError_t tc_forward2(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
 cudaError_t tc_cb_prepass(const Dims& d, const void* B, const void* C, float* CB, cudaStream_t st);
 cudaError_t tc_replay_states(const Dims& d, const void* x, const float* dt_raw, const float* A, const void* B,
                              const float* s0, __nv_bfloat16* states, int* status, cudaStream_t st);
+size_t tc_backward2_ws(const Dims& d);
+cudaError_t tc_backward2(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
 bool tc_backward_supported(const Dims& d);
-size_t tc_backward_ws(const Dims& d);
-cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
 
 // TMA tensor maps over bf16 tensors with 128-byte swizzle (tma_host.cu).
 cudaError_t make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,

@@ -1,0 +1,735 @@
+// Warp-specialized recompute backward of the Mamba-2 scan on tcgen05 tensor
+// cores (bf16 io, chunk L = 64, head dim P = 64, state N = 128).
+//
+// It follows the recompute backward of the burn-mamba page
+// "combined_backward.rs": the chunk-input states S_c are replayed from the
+// saved leaf inputs (a separate launch of the forward kernel in its states
+// mode writes them, bf16, to the workspace), then the chunks are walked in
+// reverse carrying the state gradient dS from the nonzero ds_final seed, with
+// the K5 (BLUE + ORANGE), K4, K3 and K2 backwards of each chunk fused:
+//
+//   batch 1 (chunk-local):  dS_blue^T = C^T dch,  dC^T = S_c dch^T,
+//                           dW~ = dy x^T,  Y = C S_c^T        (dch = e^cum dy)
+//   between:  W = CB o decay, dW = dW~ o dt'_s, dCB = dW o decay,
+//             d_diff = dCB o CB (ORANGE, mask before exp);
+//             d cum_blue = sum_p dch Y;  K4: e^cum_end <dS_{c+1}, S_c>;
+//             dS_c = e^cum_end dS_{c+1} + dS_blue            (K4)
+//   batch 2:  ddv = B dS_{c+1}^T,  dB^T = dS_{c+1} dvd^T + C^T dCB,
+//             dC^T += B^T dCB^T,   dv_or = W^T dy
+//   outputs:  dv = dv_or + e^(cum_end - cum_s) ddv,  dx = dt' dv (TMA store),
+//             dB^T, dC^T per head (fp32, summed over the group afterwards),
+//             d cum -> suffix sums (K1 backward) -> ddt_raw, dA parts.
+// Here dvd = e^(cum_end - cum_s) dt' x and decay = exp(cum_t - cum_s)[s <= t].
+//
+// Warp roles (480 threads), all on different chunks at once:
+//   warps 0-3   S: the dS chain (thread n owns dS[n][0..63] in fp32), the K4
+//               term, d cum_blue, and the bf16 dS tile of the next chunk.
+//   warps 4-7   O: dC^T and dB^T rows out, dv -> dx, sum_p dv x, dv_k3 terms.
+//   warps 8-11  T: the dch and dvd tiles of the next chunk; W, dCB and the
+//               ORANGE row / column sums of d_diff from dW.
+//   warp 12     K1 scalars up to four chunks ahead, and per chunk the d cum
+//               assembly, suffix sums, ddt_raw and the dA part.
+//   warp 13     TMA producer (x, dy, B, C, S_c), two stages.
+//   warp 14     MMA issuer and TMEM owner; TMEM holds two chunks' accumulators
+//               so batch 1 of chunk c-1 overlaps the epilogues of chunk c.
+// Every wait is bounded and every role agrees on stopping through voting
+// barriers; on a timeout the kernel records a code in the workspace status
+// word.
+#include "ssd_device.cuh"
+#include "ssd_internal.h"
+#include "tc_common.cuh"
+
+namespace ssd {
+namespace {
+using namespace tc;
+
+constexpr int kL = 64, kP = 64, kN = 128;
+constexpr int kStages = 2, kScal = 4;
+constexpr int kThreads = 480;
+constexpr int kWarpO0 = 4, kWarpT0 = 8, kWarpScal = 12, kWarpTma = 13, kWarpMma = 14;
+constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
+constexpr uint32_t kTileLN = kL * kN * 2;  // 16 KB
+constexpr uint32_t kTileNP = kN * kP * 2;  // 16 KB
+constexpr uint32_t kStageBytes = 2 * kTileLP + 2 * kTileLN + kTileNP;  // 64 KB
+constexpr uint32_t kTmemCols = 512;
+
+struct alignas(1024) Bwd2Smem {
+  struct Stage {
+    uint8_t x[kTileLP];   // [t][p]
+    uint8_t dy[kTileLP];  // [t][p]
+    uint8_t B[kTileLN];   // [n atom][t][64]
+    uint8_t C[kTileLN];
+    uint8_t S[kTileNP];   // S_c^T bf16 [n][p]
+  } st[kStages];
+  uint8_t dch[2][kTileLP];  // exp(cum) dy [t][p]
+  uint8_t dvd[2][kTileLP];  // exp(cum_end - cum) dt' x [s][p]
+  uint8_t W[kTileLP];       // [t][s]
+  uint8_t dCB[kTileLP];     // [t][s]
+  uint8_t dS[kTileNP];      // dS_{c+1}^T bf16 [n][p], rewritten once batch 2 has read it
+  uint8_t dx[2][kTileLP];   // dx staging [s][p]
+  // K1 scalars, ring of kScal chunks (see ssd_tc_fwd2.cu for E and G)
+  float cum[kScal][kL], ecum[kScal][kL], dec[kScal][kL], dtp[kScal][kL], z[kScal][kL], G[kScal][kL];
+  float E[kScal][kL][4];
+  float aend[kScal];
+  // per-chunk partial sums for the d cum assembly, two slots
+  float drow[2][kL], dcolp[2][4][kL], dcb[2][kL], dde[2][kL], dvx[2][kL], k4p[2][4];
+  uint64_t full[kStages], empty[kStages], sc_ready[kScal], sc_free[kScal];
+  uint64_t pre_done[2], b1_done[2], e1a_done[2], e1b_done[2], b2_done[2], e2_done[2], fin_done[2];
+  uint64_t ds_ready;  // completes once per dS tile (ds_final, then dS_c after each batch 2)
+  uint32_t tmem_slot;
+};
+
+struct Bwd2Params {
+  const float* dt_raw;
+  const float* A;
+  const float* ds_final;
+  const float* CB;  // [b, nc, G, L, L] fp32
+  float* ddt_raw;
+  float* ds0;
+  float* dB_part;  // [b,T,H,N]
+  float* dC_part;  // [b,T,H,N]
+  float* dA_part;  // [b,H,nc]
+  int* status;
+  int T, H, G, hpg, nc;
+};
+
+__device__ __forceinline__ void load_row8(const uint8_t* tile, int r, int j, float* out) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(tile + sw128_chunk(r, j));
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = unpack_bf16(w[e]);
+    out[2 * e] = f.x;
+    out[2 * e + 1] = f.y;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_bwd2(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+              const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_B,
+              const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_S, Bwd2Params prm) {
+  extern __shared__ uint8_t smem_raw[];
+  Bwd2Smem& sm = *reinterpret_cast<Bwd2Smem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int T = prm.T, H = prm.H, nc = prm.nc;
+  const int g = h / prm.hpg;
+  const int row0 = b * T;
+  const size_t unit = (size_t)b * H + h;
+  int* status = prm.status;
+  auto chunk_of = [&](int r) { return nc - 1 - r; };  // iteration r walks chunk nc-1-r
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 4);  // T, S, O warps + MMA commit
+    }
+    for (int j = 0; j < kScal; ++j) {
+      mbar_init(&sm.sc_ready[j], 1);
+      mbar_init(&sm.sc_free[j], 3);  // T, S, O warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.pre_done[i], 1);
+      mbar_init(&sm.b1_done[i], 1);
+      mbar_init(&sm.e1a_done[i], 1);
+      mbar_init(&sm.e1b_done[i], 1);
+      mbar_init(&sm.b2_done[i], 1);
+      mbar_init(&sm.e2_done[i], 1);
+      mbar_init(&sm.fin_done[i], 1);
+    }
+    mbar_init(&sm.ds_ready, 1);
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) tmem_alloc(&sm.tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  auto TA = [&](int i) { return tmem + 256u * i; };         // dS_blue^T (M=128), then ddv (M=64)
+  auto TB = [&](int i) { return tmem + 256u * i + 64u; };   // dC^T (M=128)
+  auto TC = [&](int i) { return tmem + 256u * i + 128u; };  // dW~ (M=64), then dv_or (M=64)
+  auto TY = [&](int i) { return tmem + 256u * i + 192u; };  // Y (M=64), then dB^T (M=128)
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_x);
+      prefetch_tmap(&tm_dy);
+      prefetch_tmap(&tm_B);
+      prefetch_tmap(&tm_C);
+      prefetch_tmap(&tm_S);
+      for (int r = 0; r < nc; ++r) {
+        const int s = r % kStages, c = chunk_of(r);
+        if (r >= kStages && !mbar_wait(&sm.empty[s], (r / kStages - 1) & 1, status, 41)) break;
+        Bwd2Smem::Stage& sg = sm.st[s];
+        mbar_expect_tx(&sm.full[s], kStageBytes);
+        tma_load_2d(sg.x, &tm_x, h * kP, row0 + c * kL, &sm.full[s]);
+        tma_load_2d(sg.dy, &tm_dy, h * kP, row0 + c * kL, &sm.full[s]);
+        for (int a = 0; a < 2; ++a) {
+          tma_load_3d(sg.B + a * (kTileLN / 2), &tm_B, a * 64, g, row0 + c * kL, &sm.full[s]);
+          tma_load_3d(sg.C + a * (kTileLN / 2), &tm_C, a * 64, g, row0 + c * kL, &sm.full[s]);
+        }
+        tma_load_2d(sg.S, &tm_S, 0, (int)((unit * nc + c) * kN), &sm.full[s]);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto batch1 = [&](int r) -> bool {
+        const int s = r % kStages, i = r & 1;
+        if (!mbar_wait(&sm.pre_done[i], (r >> 1) & 1, status, 42)) return false;  // implies the stage landed
+        if (r >= 2 && !mbar_wait(&sm.e2_done[i], ((r >> 1) - 1) & 1, status, 43)) return false;
+        tc_fence_after();
+        const Bwd2Smem::Stage& sg = sm.st[s];
+#pragma unroll
+        for (int kk = 0; kk < kL; kk += 16)  // dS_blue^T[n][p] = sum_t C[t][n] dch[t][p]
+          mma_bf16(TA(i), mdesc(sg.C, kL, kk), mdesc(sm.dch[i], kL, kk), idesc_bf16(128, 64, true, true), kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kP; kk += 16)  // dC^T[n][t] = sum_p S[n][p] dch[t][p]
+          mma_bf16(TB(i), kdesc(sg.S, kN, kk), kdesc(sm.dch[i], kL, kk), idesc_bf16(128, 64, false, false), kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kP; kk += 16)  // dW~[t][s] = sum_p dy[t][p] x[s][p]
+          mma_bf16(TC(i), kdesc(sg.dy, kL, kk), kdesc(sg.x, kL, kk), idesc_bf16(64, 64, false, false), kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kN; kk += 16)  // Y[t][p] = sum_n C[t][n] S[n][p]
+          mma_bf16(TY(i), kdesc(sg.C, kL, kk), mdesc(sg.S, kN, kk), idesc_bf16(64, 64, false, true), kk > 0);
+        mma_commit(&sm.b1_done[i]);
+        return true;
+      };
+      auto batch2 = [&](int r) -> bool {
+        const int s = r % kStages, i = r & 1;
+        bool ok = mbar_wait(&sm.e1a_done[i], (r >> 1) & 1, status, 44);
+        ok = ok && mbar_wait(&sm.e1b_done[i], (r >> 1) & 1, status, 45);
+        ok = ok && mbar_wait(&sm.ds_ready, r & 1, status, 64);  // the dS_{c+1} tile
+        if (!ok) return false;
+        tc_fence_after();
+        const Bwd2Smem::Stage& sg = sm.st[s];
+#pragma unroll
+        for (int kk = 0; kk < kN; kk += 16)  // ddv[s][p] = sum_n B[s][n] dS[n][p]
+          mma_bf16(TA(i), kdesc(sg.B, kL, kk), mdesc(sm.dS, kN, kk), idesc_bf16(64, 64, false, true), kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kP; kk += 16)  // dB^T[n][s] = sum_p dS[n][p] dvd[s][p]
+          mma_bf16(TY(i), kdesc(sm.dS, kN, kk), kdesc(sm.dvd[i], kL, kk), idesc_bf16(128, 64, false, false),
+                   kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kL; kk += 16)  //          + sum_t C[t][n] dCB[t][s]
+          mma_bf16(TY(i), mdesc(sg.C, kL, kk), mdesc(sm.dCB, kL, kk), idesc_bf16(128, 64, true, true), true);
+#pragma unroll
+        for (int kk = 0; kk < kL; kk += 16)  // dC^T[n][t] += sum_s B[s][n] dCB[t][s]
+          mma_bf16(TB(i), mdesc(sg.B, kL, kk), kdesc(sm.dCB, kL, kk), idesc_bf16(128, 64, true, false), true);
+#pragma unroll
+        for (int kk = 0; kk < kL; kk += 16)  // dv_or[s][p] = sum_t W[t][s] dy[t][p]
+          mma_bf16(TC(i), mdesc(sm.W, kL, kk), mdesc(sg.dy, kL, kk), idesc_bf16(64, 64, true, true), kk > 0);
+        mma_commit(&sm.b2_done[i]);
+        mma_commit(&sm.empty[s]);
+        return true;
+      };
+      if (batch1(0)) {
+        for (int r = 0; r < nc; ++r) {
+          if (!batch2(r)) break;
+          if (r + 1 < nc && !batch1(r + 1)) break;
+        }
+      }
+    }
+  } else if (warp == kWarpScal) {
+    // ------------------------------------------------------------ K1 scalars + d cum assembly
+    const float A_h = prm.A[h];
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    auto scalars = [&](int r) {
+      const int j = r % kScal, c = chunk_of(r);
+      const size_t rr = (size_t)row0 + c * kL + t0;
+      const float z0 = prm.dt_raw[rr * H + h], z1 = prm.dt_raw[(rr + 1) * H + h];
+      const float d0 = softplus_f(z0), d1 = softplus_f(z1);
+      const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
+      float inc = a1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      const float c0 = inc - a1 + a0, c1 = inc;
+      const float cend = __shfl_sync(0xffffffffu, inc, 31);
+      sm.cum[j][t0] = c0;
+      sm.cum[j][t1] = c1;
+      sm.dtp[j][t0] = d0;
+      sm.dtp[j][t1] = d1;
+      sm.z[j][t0] = z0;
+      sm.z[j][t1] = z1;
+      sm.ecum[j][t0] = expf(c0);
+      sm.ecum[j][t1] = expf(c1);
+      sm.dec[j][t0] = expf(cend - c0);
+      sm.dec[j][t1] = expf(cend - c1);
+      if (lane == 0) sm.aend[j] = expf(cend);
+      const float e0 = __shfl_sync(0xffffffffu, c1, 7), e1 = __shfl_sync(0xffffffffu, c1, 15);
+      const float e2 = __shfl_sync(0xffffffffu, c1, 23), e3 = __shfl_sync(0xffffffffu, c1, 31);
+      const int blk = t0 >> 4;
+      const float my_end = blk == 0 ? e0 : (blk == 1 ? e1 : (blk == 2 ? e2 : e3));
+      sm.G[j][t0] = expf(my_end - c0);  // pure decay to the end of the 16-block
+      sm.G[j][t1] = expf(my_end - c1);
+      const float ends[4] = {e0, e1, e2, e3};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        sm.E[j][t0][q] = (q < blk) ? expf(c0 - ends[q]) : 0.f;
+        sm.E[j][t1][q] = (q < blk) ? expf(c1 - ends[q]) : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.sc_ready[j]);
+    };
+    for (int r = 0; r < kScal && r < nc; ++r) scalars(r);
+    for (int r = 0; r < nc; ++r) {
+      const int i = r & 1, j = r % kScal, c = chunk_of(r);
+      bool ok = mbar_wait(&sm.e1a_done[i], (r >> 1) & 1, status, 46);
+      ok = ok && mbar_wait(&sm.e1b_done[i], (r >> 1) & 1, status, 47);
+      ok = ok && mbar_wait(&sm.e2_done[i], (r >> 1) & 1, status, 48);
+      if (!ok) break;
+      // d cum per position: ORANGE row - column sums, BLUE, K3; K3's and K4's chunk-end terms at t = 63
+      const float dec0 = sm.dec[j][t0], dec1 = sm.dec[j][t1];
+      const float k3_0 = sm.dde[i][t0] * dec0, k3_1 = sm.dde[i][t1] * dec1;
+      float dc0 = sm.drow[i][t0] - (sm.dcolp[i][0][t0] + sm.dcolp[i][1][t0] + sm.dcolp[i][2][t0] + sm.dcolp[i][3][t0]) +
+                  sm.dcb[i][t0] - k3_0;
+      float dc1 = sm.drow[i][t1] - (sm.dcolp[i][0][t1] + sm.dcolp[i][1][t1] + sm.dcolp[i][2][t1] + sm.dcolp[i][3][t1]) +
+                  sm.dcb[i][t1] - k3_1;
+      float k3sum = k3_0 + k3_1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) k3sum += __shfl_xor_sync(0xffffffffu, k3sum, o);
+      const float k4 = sm.aend[j] * (sm.k4p[i][0] + sm.k4p[i][1] + sm.k4p[i][2] + sm.k4p[i][3]);
+      if (lane == 31) dc1 += k3sum + k4;
+      // suffix sums (K1 backward): dda[t] = sum_{u >= t} d cum[u]
+      const float pair = dc0 + dc1;
+      float suf = pair;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += u;
+      }
+      const float dda0 = suf, dda1 = suf - dc0;
+      const size_t rr = (size_t)row0 + c * kL + t0;
+      prm.ddt_raw[rr * H + h] = (sm.dvx[i][t0] + A_h * dda0) * sigmoid_f(sm.z[j][t0]);
+      prm.ddt_raw[(rr + 1) * H + h] = (sm.dvx[i][t1] + A_h * dda1) * sigmoid_f(sm.z[j][t1]);
+      float dAp = dda0 * sm.dtp[j][t0] + dda1 * sm.dtp[j][t1];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
+      if (lane == 0) prm.dA_part[unit * nc + c] = dAp;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.fin_done[i]);
+      // the scalars of iteration r + kScal reuse slot j once T, S and O released it
+      if (r + kScal < nc) {
+        if (!mbar_wait(&sm.sc_free[j], (r / kScal) & 1, status, 49)) break;
+        scalars(r + kScal);
+      }
+    }
+  } else if (warp >= kWarpT0) {
+    // ------------------------------------------------------------ T warps 8-11
+    const int pt = tid - 32 * kWarpT0;  // 0..127
+    const int q = warp & 3;
+    auto pre = [&](int r) -> bool {
+      const int s = r % kStages, i = r & 1, j = r % kScal;
+      bool ok = mbar_wait(&sm.sc_ready[j], (r / kScal) & 1, status, 50);
+      ok = ok && mbar_wait(&sm.full[s], (r / kStages) & 1, status, 51);
+      // tiles i: dch last read by batch 1, dvd by batch 2 of r-2
+      if (ok && r >= 2) ok = mbar_wait(&sm.b2_done[i], ((r >> 1) - 1) & 1, status, 52);
+      if (named_bar_or(2, 128, !ok)) return false;
+      const Bwd2Smem::Stage& sg = sm.st[s];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int ch = pt + 128 * rr;
+        const int t = ch >> 3, jj = ch & 7;
+        const uint32_t off = sw128_chunk(t, jj);
+        const uint4 rx = *reinterpret_cast<const uint4*>(sg.x + off);
+        const uint4 ry = *reinterpret_cast<const uint4*>(sg.dy + off);
+        const float fx = sm.dec[j][t] * sm.dtp[j][t], fy = sm.ecum[j][t];
+        const uint32_t ix[4] = {rx.x, rx.y, rx.z, rx.w}, iy[4] = {ry.x, ry.y, ry.z, ry.w};
+        uint32_t ox[4], oy[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 vx = unpack_bf16(ix[e]), vy = unpack_bf16(iy[e]);
+          ox[e] = pack_bf16(fx * vx.x, fx * vx.y);
+          oy[e] = pack_bf16(fy * vy.x, fy * vy.y);
+        }
+        *reinterpret_cast<uint4*>(sm.dvd[i] + off) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+        *reinterpret_cast<uint4*>(sm.dch[i] + off) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+      }
+      fence_proxy_async();
+      named_bar(2, 128);
+      if (pt == 0) {
+        mbar_arrive(&sm.pre_done[i]);
+        mbar_arrive(&sm.empty[s]);
+      }
+      return true;
+    };
+    bool run = pre(0);
+    for (int r = 0; r < nc && run; ++r) {
+      const int i = r & 1, j = r % kScal, c = chunk_of(r);
+      // ---- E1a: W, dCB, d_diff sums from dW~ (TC, M = 64).  Row t = 16q + (lane & 15):
+      //      lanes 0-15 take columns 0-31, lanes 16-31 columns 32-63 of the same rows.
+      const int hl = lane >> 4, t = 16 * q + (lane & 15), cs0 = 32 * hl;
+      const float4* cbrow = reinterpret_cast<const float4*>(prm.CB + ((((size_t)b * nc + c) * prm.G + g) * kL + t) * kL + cs0);
+      float4 cbq[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) cbq[e] = __ldg(cbrow + e);
+      bool ok = mbar_wait(&sm.b1_done[i], (r >> 1) & 1, status, 54);
+      // W and dCB (single tiles) were last read by batch 2 of r-1; the partial slot i by the assembly of r-2
+      if (ok && r >= 1) ok = mbar_wait(&sm.b2_done[(r - 1) & 1], ((r - 1) >> 1) & 1, status, 55);
+      if (ok && r >= 2) ok = mbar_wait(&sm.fin_done[i], ((r >> 1) - 1) & 1, status, 56);
+      if (named_bar_or(2, 128, !ok)) break;
+      tc_fence_after();
+      float dw[32];
+      {
+        uint32_t lo[32], hi[32];
+        tmem_ld32_nowait(taddr(TC(i), 32 * q, 0), lo);
+        tmem_ld32_nowait(taddr(TC(i), 32 * q, 32), hi);
+        tmem_wait_ld();
+        // rows live in lanes 0-15; lanes 16-31 fetch the upper half of their row
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float up = __shfl_sync(0xffffffffu, __uint_as_float(hi[e]), lane & 15);
+          dw[e] = hl ? up : __uint_as_float(lo[e]);
+        }
+      }
+      const int tb = t >> 4;
+      const float ct = sm.cum[j][t];
+      float cbv[32];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cbv[4 * e + 0] = cbq[e].x;
+        cbv[4 * e + 1] = cbq[e].y;
+        cbv[4 * e + 2] = cbq[e].z;
+        cbv[4 * e + 3] = cbq[e].w;
+      }
+      float wrow[32], dcbrow[32];
+#pragma unroll
+      for (int bk = 0; bk < 2; ++bk) {
+        const int sb = 2 * hl + bk, s0 = 16 * sb;
+        if (sb < tb) {
+          const float f = sm.E[j][t][sb];  // exp(cum_t - cum at the end of block sb)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int ss = s0 + e, k = 16 * bk + e;
+            const float dec = f * sm.G[j][ss];  // exp(cum_t - cum_s)
+            wrow[k] = cbv[k] * dec;
+            dcbrow[k] = dw[k] * sm.dtp[j][ss] * dec;
+          }
+        } else if (sb == tb) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int ss = s0 + e, k = 16 * bk + e;
+            const float ex = (ss <= t) ? expf(fminf(ct - sm.cum[j][ss], 0.f)) : 0.f;
+            wrow[k] = cbv[k] * ex;
+            dcbrow[k] = dw[k] * sm.dtp[j][ss] * ex;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            wrow[16 * bk + e] = 0.f;
+            dcbrow[16 * bk + e] = 0.f;
+          }
+        }
+      }
+      float dd[32];
+      float rowsum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        dd[k] = dcbrow[k] * cbv[k];  // d_diff = dW o decay o CB
+        rowsum += dd[k];
+      }
+      store_row_bf16(sm.W, t, 4 * hl, wrow, 4);
+      store_row_bf16(sm.dCB, t, 4 * hl, dcbrow, 4);
+      rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
+      if (lane < 16) sm.drow[i][t] = rowsum;
+      // column sums over the 16 rows of this quadrant: butterfly over lanes with the same half
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const bool up = lane & 8;
+        const float send = up ? dd[k] : dd[k + 16], keep = up ? dd[k + 16] : dd[k];
+        dd[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const bool up = lane & 4;
+        const float send = up ? dd[k] : dd[k + 8], keep = up ? dd[k + 8] : dd[k];
+        dd[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool up = lane & 2;
+        const float send = up ? dd[k] : dd[k + 4], keep = up ? dd[k + 4] : dd[k];
+        dd[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const bool up = lane & 1;
+        const float send = up ? dd[k] : dd[k + 2], keep = up ? dd[k + 2] : dd[k];
+        dd[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+      }
+      {
+        // lane now holds the sums of columns cs0 + 16(l&8?1:0) + 8(l&4?1:0) + 4(l&2?1:0) + 2(l&1) + {0, 1}
+        const int col = cs0 + ((lane & 8) ? 16 : 0) + ((lane & 4) ? 8 : 0) + ((lane & 2) ? 4 : 0) + ((lane & 1) ? 2 : 0);
+        sm.dcolp[i][q][col] = dd[0];
+        sm.dcolp[i][q][col + 1] = dd[1];
+      }
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(2, 128);
+      if (pt == 0) {
+        mbar_arrive(&sm.e1a_done[i]);
+        mbar_arrive(&sm.sc_free[j]);
+      }
+      if (r + 1 < nc && !pre(r + 1)) break;
+    }
+  } else if (warp >= kWarpO0) {
+    // ------------------------------------------------------------ O warps 4-7
+    const int ot = tid - 32 * kWarpO0;  // 0..127
+    const int q = warp & 3;
+    const int n = 32 * q + lane;
+    for (int r = 0; r < nc; ++r) {
+      const int s = r % kStages, i = r & 1, j = r % kScal, c = chunk_of(r);
+      bool ok = mbar_wait(&sm.b2_done[i], (r >> 1) & 1, status, 57);
+      ok = ok && mbar_wait(&sm.sc_ready[j], (r / kScal) & 1, status, 58);
+      if (ok && r >= 2) ok = mbar_wait(&sm.fin_done[i], ((r >> 1) - 1) & 1, status, 59);
+      if (ot == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // dx slot i (chunk r-2) read out
+      if (named_bar_or(3, 128, !ok)) break;
+      tc_fence_after();
+      const Bwd2Smem::Stage& sg = sm.st[s];
+      const size_t trow = (size_t)row0 + c * kL;
+      // dC^T (TB) and dB^T (TY), M = 128: lane n holds 64 columns (t or s)
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t vc[32], vb[32];
+        tmem_ld32_nowait(taddr(TB(i), 32 * q, 32 * part), vc);
+        tmem_ld32_nowait(taddr(TY(i), 32 * q, 32 * part), vb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          prm.dC_part[((trow + 32 * part + e) * H + h) * kN + n] = __uint_as_float(vc[e]);
+          prm.dB_part[((trow + 32 * part + e) * H + h) * kN + n] = __uint_as_float(vb[e]);
+        }
+      }
+      // dv = dv_or + exp(cum_end - cum_s) ddv  (TC, TA; M = 64: row s = 16q + lane), 32 columns at a time
+      {
+        const int srow = 16 * q + lane;
+        const float e = (lane < 16) ? sm.dec[j][srow] : 0.f, d = (lane < 16) ? sm.dtp[j][srow] : 0.f;
+        float sx = 0.f, sd = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t ro[32], rd[32];
+          tmem_ld32_nowait(taddr(TC(i), 32 * q, 32 * hf), ro);
+          tmem_ld32_nowait(taddr(TA(i), 32 * q, 32 * hf), rd);
+          tmem_wait_ld();
+          float dvo[32], ddv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            dvo[e] = __uint_as_float(ro[e]);
+            ddv[e] = __uint_as_float(rd[e]);
+          }
+          if (lane < 16) {
+            float dxv[32];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              float xv[8];
+              load_row8(sg.x, srow, 4 * hf + jj, xv);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int p = 8 * jj + u;
+                const float dv = dvo[p] + e * ddv[p];
+                sx += dv * xv[u];
+                sd += ddv[p] * xv[u];
+                dxv[p] = d * dv;
+              }
+            }
+            store_row_bf16(sm.dx[i], srow, 4 * hf, dxv, 4);
+          }
+        }
+        if (lane < 16) {
+          sm.dvx[i][srow] = sx;
+          sm.dde[i][srow] = sd * d;  // sum_p ddv[s][p] v[s][p]
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(3, 128);
+      if (ot == 0) {
+        tma_store_2d(&tm_dx, sm.dx[i], h * kP, row0 + c * kL);
+        tma_store_commit();
+        mbar_arrive(&sm.e2_done[i]);
+        mbar_arrive(&sm.sc_free[j]);
+        mbar_arrive(&sm.empty[s]);
+      }
+    }
+    if (ot == 0) tma_store_wait0();
+  } else {
+    // ------------------------------------------------------------ S warps 0-3
+    const int n = tid;  // dS row owned by this thread
+    const size_t sbase = unit * kP * kN;
+    float dS[kP];
+#pragma unroll
+    for (int p = 0; p < kP; ++p) dS[p] = prm.ds_final[sbase + (size_t)p * kN + n];
+    store_row_bf16(sm.dS, n, 0, dS, 8);  // dS_{nc} = ds_final, read by batch 2 of iteration 0
+    fence_proxy_async();
+    named_bar(1, 128);
+    if (n == 0) mbar_arrive(&sm.ds_ready);
+    for (int r = 0; r < nc; ++r) {
+      const int s = r % kStages, i = r & 1, j = r % kScal;
+      bool ok = mbar_wait(&sm.b1_done[i], (r >> 1) & 1, status, 60);
+      ok = ok && mbar_wait(&sm.sc_ready[j], (r / kScal) & 1, status, 61);
+      if (ok && r >= 2) ok = mbar_wait(&sm.fin_done[i], ((r >> 1) - 1) & 1, status, 62);
+      if (named_bar_or(1, 128, !ok)) break;
+      tc_fence_after();
+      const Bwd2Smem::Stage& sg = sm.st[s];
+      // K4: <dS_{c+1}, S_c> (S_c from its bf16 tile)
+      {
+        float part = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          float sv[8];
+          load_row8(sg.S, n, jj, sv);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) part += dS[8 * jj + u] * sv[u];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) sm.k4p[i][warp] = part;
+      }
+      // dS_c = exp(cum_end) dS_{c+1} + dS_blue
+      {
+        const float a = sm.aend[j];
+        uint32_t b0[32], b1[32];
+        tmem_ld32_nowait(taddr(TA(i), 32 * warp, 0), b0);
+        tmem_ld32_nowait(taddr(TA(i), 32 * warp, 32), b1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int p = 0; p < 32; ++p) {
+          dS[p] = a * dS[p] + __uint_as_float(b0[p]);
+          dS[32 + p] = a * dS[32 + p] + __uint_as_float(b1[p]);
+        }
+      }
+      // BLUE d cum: sum_p exp(cum_t) dy[t][p] Y[t][p]  (Y: M = 64, row t = 16 warp + lane)
+      {
+        const int t = 16 * warp + lane;
+        float acc = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float yv[32];
+          tmem_ld32(taddr(TY(i), 32 * warp, 32 * hf), yv);
+          if (lane < 16) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              float gv[8];
+              load_row8(sg.dy, t, 4 * hf + jj, gv);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) acc += gv[u] * yv[8 * jj + u];
+            }
+          }
+        }
+        if (lane < 16) sm.dcb[i][t] = acc * sm.ecum[j][t];
+      }
+      tc_fence_before();
+      named_bar(1, 128);
+      if (n == 0) {
+        mbar_arrive(&sm.e1b_done[i]);
+        mbar_arrive(&sm.sc_free[j]);
+        mbar_arrive(&sm.empty[s]);
+      }
+      // the dS_c tile for batch 2 of r+1, once batch 2 of r has read dS_{c+1}
+      if (r + 1 < nc) {
+        ok = mbar_wait(&sm.b2_done[i], (r >> 1) & 1, status, 63);
+        if (named_bar_or(1, 128, !ok)) break;
+        store_row_bf16(sm.dS, n, 0, dS, 8);
+        fence_proxy_async();
+        named_bar(1, 128);
+        if (n == 0) mbar_arrive(&sm.ds_ready);
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < kP; ++p) prm.ds0[sbase + (size_t)p * kN + n] = dS[p];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename TOut>
+__global__ void k_bwd2_group_sum(const float* part, TOut* out, int b, int T, int H, int G, int N) {
+  const size_t total = (size_t)b * T * G * N;
+  const int hpg = H / G;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int n = e % N;
+    const size_t bt = e / N / G;
+    const int gg = (e / N) % G;
+    float acc = 0.f;
+    for (int k = 0; k < hpg; ++k) acc += part[(bt * H + gg * hpg + k) * N + n];
+    st(out, e, acc);
+  }
+}
+
+__global__ void k_bwd2_dA_sum(const float* part, float* dA, int b, int H, int nc) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= H) return;
+  float acc = 0.f;
+  for (int bb = 0; bb < b; ++bb)
+    for (int c = 0; c < nc; ++c) acc += part[((size_t)bb * H + h) * nc + c];
+  dA[h] = acc;
+}
+
+struct Bwd2Ws {
+  __nv_bfloat16* states;  // [b,H,nc][N][P]
+  float* CB;              // [b,nc,G,L,L]
+  float* dB_part;
+  float* dC_part;
+  float* dA_part;
+};
+
+Bwd2Ws carve(const Dims& d, Carver& cv) {
+  Bwd2Ws w;
+  w.states = cv.take<__nv_bfloat16>((size_t)d.b * d.H * d.nc * kN * kP);
+  w.CB = cv.take<float>((size_t)d.b * d.nc * d.G * kL * kL);
+  w.dB_part = cv.take<float>((size_t)d.b * d.T * d.H * kN);
+  w.dC_part = cv.take<float>((size_t)d.b * d.T * d.H * kN);
+  w.dA_part = cv.take<float>((size_t)d.b * d.H * d.nc);
+  return w;
+}
+
+}  // namespace
+
+size_t tc_backward2_ws(const Dims& d) {
+  Carver cv(nullptr);
+  carve(d, cv);
+  return cv.off;
+}
+
+cudaError_t tc_backward2(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st) {
+  Carver cv(ws);
+  Bwd2Ws w = carve(d, cv);
+  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, st);
+  if (e == cudaSuccess) e = tc_replay_states(d, a.x, a.dt_raw, a.A, a.B, a.s0, w.states, static_cast<int*>(ws), st);
+  if (e != cudaSuccess) return e;
+  const uint64_t rows = (uint64_t)d.b * d.T;
+  CUtensorMap tx, tdy, tdx, tb, tcm, ts;
+  e = make_tmap_2d_bf16(&tx, a.x, (uint64_t)d.H * kP, rows, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdy, a.dy, (uint64_t)d.H * kP, rows, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdx, a.dx, (uint64_t)d.H * kP, rows, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tb, a.B, d.N, d.G, rows, 64, 1, 64);
+  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tcm, a.C, d.N, d.G, rows, 64, 1, 64);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, w.states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, kN);
+  if (e != cudaSuccess) return e;
+  Bwd2Params prm{a.dt_raw, a.A, a.ds_final, w.CB, a.ddt_raw, a.ds0, w.dB_part, w.dC_part, w.dA_part,
+                 static_cast<int*>(ws), d.T, d.H, d.G, d.hpg, d.nc};
+  const int smem = (int)sizeof(Bwd2Smem) + 1024;
+  e = cudaFuncSetAttribute(k_tc_bwd2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  SSD_LAUNCH("k_tc_bwd2", st, k_tc_bwd2<<<dim3(d.H, d.b), kThreads, smem, st>>>(tx, tdy, tdx, tb, tcm, ts, prm));
+  const size_t tot = (size_t)d.b * d.T * d.G * d.N;
+  const int blocks = (int)((tot + 255) / 256 < 65535 ? (tot + 255) / 256 : 65535);
+  SSD_LAUNCH("k_tc_group_sum", st,
+             k_bwd2_group_sum<__nv_bfloat16><<<blocks, 256, 0, st>>>(w.dB_part, static_cast<__nv_bfloat16*>(a.dB), d.b,
+                                                                     d.T, d.H, d.G, d.N));
+  SSD_LAUNCH("k_tc_group_sum", st,
+             k_bwd2_group_sum<__nv_bfloat16><<<blocks, 256, 0, st>>>(w.dC_part, static_cast<__nv_bfloat16*>(a.dC), d.b,
+                                                                     d.T, d.H, d.G, d.N));
+  SSD_LAUNCH("k_tc_dA_sum", st, k_bwd2_dA_sum<<<(d.H + 127) / 128, 128, 0, st>>>(w.dA_part, a.dA, d.b, d.H, d.nc));
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

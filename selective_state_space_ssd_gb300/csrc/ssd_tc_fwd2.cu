@@ -434,6 +434,14 @@ __global__ void __launch_bounds__(256) k_cb(const __nv_bfloat16* B, const __nv_b
 
 }  // namespace
 
+// The tensor-core kernels serve Mamba-2 with bf16 io, chunk 64, head dim 64
+// and state 128 (the 130M and 2.7B layer shapes); everything else runs on the
+// CUDA-core kernels.
+bool tc_forward_supported(const Dims& d) {
+  return d.variant == kMamba2 && d.bf16 && d.L == kL && d.P == kP && d.N == kN;
+}
+bool tc_backward_supported(const Dims& d) { return tc_forward_supported(d); }
+
 size_t tc_fwd2_ws(const Dims& d) {
   Carver cv(nullptr);
   cv.take<float>((size_t)d.b * d.nc * d.G * kL * kL);
