@@ -84,6 +84,13 @@ cudaError_t tc_forward2(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t 
 cudaError_t tc_cb_prepass(const Dims& d, const void* B, const void* C, float* CB, cudaStream_t st);
 cudaError_t tc_replay_states(const Dims& d, const void* x, const float* dt_raw, const float* A, const void* B,
                              const float* s0, __nv_bfloat16* states, int* status, cudaStream_t st);
+// Sequential state scans (ssd_tc_scan.cu): forward writes S_c for every chunk
+// (bf16 [b,H,nc][N][P]) and S_nc into fin (if not null); reverse writes
+// dS_{c+1} for every chunk and dS_0 into fin.  u = x or dy, k = B or C,
+// init = s0 (may be null) or ds_final.
+size_t tc_scan_states_bytes(const Dims& d);
+cudaError_t tc_scan(const Dims& d, bool reverse, const void* u, const void* k, const float* dt_raw, const float* A,
+                    const float* init, float* fin, __nv_bfloat16* states, int* status, cudaStream_t st);
 size_t tc_backward2_ws(const Dims& d);
 cudaError_t tc_backward2(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
 bool tc_backward_supported(const Dims& d);

@@ -703,7 +703,8 @@ cudaError_t tc_backward2(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t
   Carver cv(ws);
   Bwd2Ws w = carve(d, cv);
   cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, st);
-  if (e == cudaSuccess) e = tc_replay_states(d, a.x, a.dt_raw, a.A, a.B, a.s0, w.states, static_cast<int*>(ws), st);
+  if (e == cudaSuccess)
+    e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, nullptr, w.states, static_cast<int*>(ws), st);
   if (e != cudaSuccess) return e;
   const uint64_t rows = (uint64_t)d.b * d.T;
   CUtensorMap tx, tdy, tdx, tb, tcm, ts;
