@@ -91,8 +91,9 @@ cudaError_t tc_replay_states(const Dims& d, const void* x, const float* dt_raw, 
 size_t tc_scan_states_bytes(const Dims& d);
 cudaError_t tc_scan(const Dims& d, bool reverse, const void* u, const void* k, const float* dt_raw, const float* A,
                     const float* init, float* fin, __nv_bfloat16* states, int* status, cudaStream_t st);
-size_t tc_backward2_ws(const Dims& d);
-cudaError_t tc_backward2(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
+// Chunk-parallel backward (ssd_tc_bwdc.cu): both scans, then every (chunk, head) at once.
+size_t tc_backward_ws(const Dims& d);
+cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
 bool tc_backward_supported(const Dims& d);
 
 // TMA tensor maps over bf16 tensors with 128-byte swizzle (tma_host.cu).

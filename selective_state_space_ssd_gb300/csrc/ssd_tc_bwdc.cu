@@ -1,0 +1,858 @@
+// Chunk-parallel backward of the Mamba-2 scan on tcgen05 tensor cores (bf16
+// io, chunk L = 64, head dim P = 64, state N = 128).
+//
+// The recompute backward of the burn-mamba page "combined_backward.rs" in
+// three stages:
+//   1. the forward state scan replays S_c (the state entering chunk c) from
+//      the saved inputs (ssd_tc_scan.cu, forward mode);
+//   2. the reverse scan gives dS_{c+1} (the gradient of the state leaving
+//      chunk c) for every chunk, and ds0 (ssd_tc_scan.cu, reverse mode);
+//   3. this kernel: with S_c and dS_{c+1} known, every (chunk, head) is
+//      independent, and computes the K5 (BLUE + ORANGE), K4, K3 and K2
+//      backwards of the page:
+//
+//   set 1:  dW~ = dy x^T,  Y = C S_c^T,  ddv = B dS_{c+1}^T
+//   E:      W = CB o decay,  dCB = dW~ o dt'_s o decay,
+//           d_diff = dCB o CB  (ORANGE; row sums - column sums; mask before exp)
+//   set 2:  dv_or = W^T dy,
+//           dB^T += dS_{c+1} dvd^T + C^T dCB,  dC^T += S_c dch^T + B^T dCB^T
+//   O:      dv = dv_or + exp(cum_end - cum_s) ddv,  dx = dt' dv,
+//           sum_p dv x (-> ddt), sum_p ddv v (K3 d cum terms)
+//   BK:     BLUE d cum_t = exp(cum_t) sum_p dy Y;  K4: exp(cum_end) <dS_{c+1}, S_c>
+//   SC:     K1 scalars; d cum assembly, suffix sums -> ddt_raw, dA part
+// with dch = exp(cum) dy, dvd = exp(cum_end - cum) dt' x and decay[t][s] =
+// exp(cum_t - cum_s) for s <= t.
+//
+// The (chunk, group, head) list is cut into one contiguous range per CTA (a
+// persistent grid of one CTA per SM), so that every SM gets the same number
+// of heads.  Heads of one chunk share B, C and CB, and their dB^T and dC^T
+// add up in two TMEM accumulators; a CTA writes one fp32 partial per chunk
+// it touched, and a small kernel adds the (at most a few) partials of each
+// chunk in a fixed order.  Per-head accumulators are double-buffered in TMEM
+// and smem, so the roles below work on two heads at once.
+//
+// Warp roles (608 threads):
+//   warps 0-3   O: dv -> dx (TMA store), K3 sums; at a chunk's end the dB^T,
+//               dC^T accumulators out to the partial buffer.
+//   warps 4-7   E: W, dCB tiles and the ORANGE sums.
+//   warps 8-11  BK: BLUE and K4.
+//   warps 12-15 P: the dch and dvd tiles.
+//   warp 16     SC: K1 scalars two heads ahead, and the per-head assembly.
+//   warp 17     TMA producer (x, dy, S_c, dS_{c+1} per head; B, C per chunk).
+//   warp 18     MMA issuer (polls both MMA sets) and TMEM owner.
+// Every wait is bounded; on a timeout the kernel records a code in the
+// workspace status word and stops.
+#include "ssd_device.cuh"
+#include "ssd_internal.h"
+#include "tc_common.cuh"
+
+namespace ssd {
+namespace {
+using namespace tc;
+
+constexpr int kL = 64, kP = 64, kN = 128;
+constexpr int kThreads = 640;
+constexpr int kWarpE0 = 4, kWarpK0 = 8, kWarpP0 = 12, kWarpScal = 16, kWarpAsm = 17, kWarpTma = 18,
+              kWarpMma = 19;
+constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
+constexpr uint32_t kTileNP = kN * kP * 2;  // 16 KB
+constexpr uint32_t kStageBytes = 2 * kTileLP + 2 * kTileNP;  // 48 KB
+constexpr uint32_t kTmemCols = 512;
+
+struct alignas(1024) BwdcSmem {
+  struct Stage {
+    uint8_t x[kTileLP];   // [s][p]
+    uint8_t dy[kTileLP];  // [t][p]
+    uint8_t dS[kTileNP];  // dS_{c+1} bf16 [n][p]
+    uint8_t S[kTileNP];   // S_c bf16 [n][p], right after dS: [dS | S] is one MN-major operand
+  } st[2];
+  uint8_t BC[4][kTileLP];   // B atom 0, C atom 0, B atom 1, C atom 1 ([t][64 n] each): [B; C] is one
+                            // K-major operand of 128 rows
+  uint8_t dch[2][kTileLP];  // exp(cum) dy [t][p]; after set 2 the dx staging tile [s][p]
+  uint8_t dvd[2][kTileLP];  // exp(cum_end - cum) dt' x [s][p]
+  uint8_t W[2][kTileLP];    // [t][s]; (the 8 KB after W[j] feed the unused upper rows of dv_or)
+  uint8_t dcbs[kTileLP];    // sum over the chunk run of dCB [t][s], bf16
+  float dcbacc[kL][kL + 4];  // the same sum in fp32 while the run goes on
+  // K1 scalars, ring of four heads.  G_s = exp(cum_e(s) - cum_s), Gd_s = G_s dt'_s and
+  // E_t[j] = exp(cum_t - cum_e(j)), where e(j) is the last position of 16-block j: exp(cum_t - cum_s)
+  // for s in an earlier block than t is E_t[blk(s)] G_s (both factors <= 1).
+  float cum[4][kL], ecum[4][kL], dec[4][kL], dtp[4][kL], z[4][kL], G[4][kL], Gd[4][kL];
+  float E[4][kL][4];
+  float aend[4], Ah[4];
+  // per-head partial sums for the d cum assembly
+  float drow[2][kL], dcolp[2][4][kL], dcb[2][kL], dde[2][kL], dvx[2][kL], k4p[2][4];
+  uint64_t full[2], empty[2], pre_done[2], s1_done[2], e_done[2], s2_done[2], bk_done[2], o_done[2], fin_done[2];
+  uint64_t sc_ready[4], sc_free[4];
+  uint64_t chunk_full, chunk_empty, acc_full, acc_free, drain;
+  uint32_t tmem_slot;
+};
+
+struct BwdcParams {
+  const float* dt_raw;
+  const float* A;
+  const float* CB;  // [b, nc, G, L, L] fp32
+  float* ddt_raw;
+  float* dA_part;  // [b, H, nc]
+  float* dB_part;  // [chunks][nseg][L][N]
+  float* dC_part;
+  int* status;
+  int T, H, G, hpg, nc;
+  int nseg;   // partial slots per chunk
+  int total;  // number of (chunk, group, head) items: b * nc * G * hpg (< 2^31)
+};
+
+// Walks this CTA's items in order without divisions: head jh of group g of
+// chunk c of batch b, chunk id k = (b * nc + c) * G + g, item f = k * hpg + jh.
+struct HeadCursor {
+  int f, k, b, c, g, jh;
+  __device__ __forceinline__ void seek(const BwdcParams& p, int f0) {
+    f = f0;
+    k = f0 / p.hpg;
+    jh = f0 - k * p.hpg;
+    g = k % p.G;
+    const int bc = k / p.G;
+    c = bc % p.nc;
+    b = bc / p.nc;
+  }
+  __device__ __forceinline__ void next(const BwdcParams& p) {
+    ++f;
+    if (++jh == p.hpg) {
+      jh = 0;
+      ++k;
+      if (++g == p.G) {
+        g = 0;
+        if (++c == p.nc) {
+          c = 0;
+          ++b;
+        }
+      }
+    }
+  }
+  __device__ __forceinline__ int h(const BwdcParams& p) const { return g * p.hpg + jh; }
+  // first / last item of this CTA's run on chunk k
+  __device__ __forceinline__ bool first(int q0) const { return f == q0 || jh == 0; }
+  __device__ __forceinline__ bool last(const BwdcParams& p, int q1) const { return f == q1 - 1 || jh == p.hpg - 1; }
+};
+
+// CTA i owns items [i * total / grid, (i + 1) * total / grid); the CTA that owns item f:
+__host__ __device__ __forceinline__ long long cta_of(long long f, long long total, long long grid) {
+  return ((f + 1) * grid - 1) / total;
+}
+
+__device__ __forceinline__ void load_row8(const uint8_t* tile, int r, int j, float* out) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(tile + sw128_chunk(r, j));
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = unpack_bf16(w[e]);
+    out[2 * e] = f.x;
+    out[2 * e + 1] = f.y;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_bwdc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+              const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_B,
+              const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_S,
+              const __grid_constant__ CUtensorMap tm_dS, BwdcParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  BwdcSmem& sm = *reinterpret_cast<BwdcSmem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = prm.T, H = prm.H, nc = prm.nc;
+  const int total = prm.total;
+  const int q0 = (int)((long long)blockIdx.x * total / gridDim.x);
+  const int q1 = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
+  const int nh = q1 - q0;
+  int* status = prm.status;
+
+  if (tid == 0) {
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&sm.full[j], 1);
+      mbar_init(&sm.empty[j], 4);  // MMA commit + P, BK, O warps
+      mbar_init(&sm.pre_done[j], 1);
+      mbar_init(&sm.s1_done[j], 1);
+      mbar_init(&sm.e_done[j], 1);
+      mbar_init(&sm.s2_done[j], 1);
+      mbar_init(&sm.bk_done[j], 1);
+      mbar_init(&sm.o_done[j], 1);
+      mbar_init(&sm.fin_done[j], 1);
+    }
+    for (int k = 0; k < 4; ++k) {
+      mbar_init(&sm.sc_ready[k], 1);
+      mbar_init(&sm.sc_free[k], 5);  // P, E, BK, O, AS
+    }
+    mbar_init(&sm.chunk_full, 1);
+    mbar_init(&sm.chunk_empty, 1);
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_free, 1);
+    mbar_init(&sm.drain, 1);
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) tmem_alloc(&sm.tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t ACC_B = tmem, ACC_C = tmem + 64u;                  // dB^T, dC^T (M = 128, lane n)
+  auto TW = [&](int j) { return tmem + 128u + 192u * j; };         // dW~ (M = 64), then dv_or (M = 128, lane s)
+  auto YD = [&](int j) { return tmem + 128u + 192u * j + 64u; };   // [B; C] [dS | S]^T (M = 128, 128 columns):
+                                                                   // ddv in lanes 0-63 / cols 0-63, Y in lanes
+                                                                   // 64-127 / cols 64-127
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_x);
+      prefetch_tmap(&tm_dy);
+      prefetch_tmap(&tm_S);
+      prefetch_tmap(&tm_dS);
+      prefetch_tmap(&tm_B);
+      prefetch_tmap(&tm_C);
+      int seg = -1;
+      HeadCursor hr, hp;  // this head, and the one two ahead for the L2 prefetch
+      hr.seek(prm, q0);
+      hp.seek(prm, q0 + 2);
+      for (int q = 0; q < nh; ++q, hr.next(prm), hp.next(prm)) {
+        const int j = q & 1;
+        const int row = hr.b * T + hr.c * kL;
+        if (hr.first(q0)) {
+          ++seg;
+          if (seg >= 1 && !mbar_wait(&sm.chunk_empty, (seg - 1) & 1, status, 101)) break;
+          mbar_expect_tx(&sm.chunk_full, 4 * kTileLP);
+          for (int a = 0; a < 2; ++a) {
+            tma_load_3d(sm.BC[2 * a], &tm_B, a * 64, hr.g, row, &sm.chunk_full);
+            tma_load_3d(sm.BC[2 * a + 1], &tm_C, a * 64, hr.g, row, &sm.chunk_full);
+          }
+        }
+        if (q + 2 < nh) {  // warm L2 with the tiles of head q + 2 while the ring is still busy
+          const int prow = hp.b * T + hp.c * kL;
+          const int psrow = (int)((((size_t)hp.b * H + hp.h(prm)) * nc + hp.c) * kN);
+          tma_prefetch_2d(&tm_x, hp.h(prm) * kP, prow);
+          tma_prefetch_2d(&tm_dy, hp.h(prm) * kP, prow);
+          tma_prefetch_2d(&tm_S, 0, psrow);
+          tma_prefetch_2d(&tm_dS, 0, psrow);
+        }
+        if (q >= 2 && !mbar_wait(&sm.empty[j], ((q >> 1) - 1) & 1, status, 102)) break;
+        BwdcSmem::Stage& sg = sm.st[j];
+        mbar_expect_tx(&sm.full[j], kStageBytes);
+        tma_load_2d(sg.x, &tm_x, hr.h(prm) * kP, row, &sm.full[j]);
+        tma_load_2d(sg.dy, &tm_dy, hr.h(prm) * kP, row, &sm.full[j]);
+        const int srow = (int)((((size_t)hr.b * H + hr.h(prm)) * nc + hr.c) * kN);
+        tma_load_2d(sg.dS, &tm_dS, 0, srow, &sm.full[j]);
+        tma_load_2d(sg.S, &tm_S, 0, srow, &sm.full[j]);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int n1 = 0, n2 = 0, seg1 = -1, seg2 = -1;
+      HeadCursor c1, c2;  // the heads of sets 1 and 2 still to issue
+      c1.seek(prm, q0);
+      c2.seek(prm, q0);
+      uint32_t idle = 0;
+      while (n2 < nh) {
+        bool moved = false;
+        if (n1 < nh && n1 <= n2 + 2) {
+          // set 1 of head n1: its stage, its TMEM buffer (read out by O and BK two heads ago), the chunk's B, C
+          const int j = n1 & 1;
+          const bool first = c1.first(q0);
+          bool rdy = mbar_probe(&sm.full[j], (n1 >> 1) & 1);
+          if (rdy && n1 >= 2)
+            rdy = mbar_probe(&sm.o_done[j], ((n1 >> 1) - 1) & 1) && mbar_probe(&sm.bk_done[j], ((n1 >> 1) - 1) & 1);
+          if (rdy && first) rdy = mbar_probe(&sm.chunk_full, (seg1 + 1) & 1);
+          if (rdy) {
+            if (first) ++seg1;
+            tc_fence_after();
+            const BwdcSmem::Stage& sg = sm.st[j];
+#pragma unroll 1
+            for (int kk = 0; kk < kP; kk += 16)  // dW~[t][s] = sum_p dy[t][p] x[s][p]
+              mma_bf16(TW(j), kdesc(sg.dy, kL, kk), kdesc(sg.x, kL, kk), idesc_bf16(64, 64, false, false), kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < kN; kk += 16)  // [B; C][s or t][n] x [dS | S][n][p]: ddv and Y
+              mma_bf16(YD(j), kdesc(sm.BC[0], 2 * kL, kk), mdesc(sg.dS, kN, kk), idesc_bf16(128, 128, false, true),
+                       kk > 0);
+            mma_commit(&sm.s1_done[j]);
+            ++n1;
+            c1.next(prm);
+            moved = true;
+          }
+        }
+        if (!moved && n2 < n1) {
+          // set 2 of head n2: its dch, dvd (P) and W (E) tiles; a new chunk run also needs the accumulators
+          // read out; the last head of a run adds the run's summed dCB terms
+          const int j = n2 & 1;
+          const bool first = c2.first(q0), last = c2.last(prm, q1);
+          bool rdy = mbar_probe(&sm.pre_done[j], (n2 >> 1) & 1) && mbar_probe(&sm.e_done[j], (n2 >> 1) & 1);
+          if (rdy && first && seg2 >= 0) rdy = mbar_probe(&sm.acc_free, seg2 & 1);
+          if (rdy) {
+            if (first) ++seg2;
+            tc_fence_after();
+            const BwdcSmem::Stage& sg = sm.st[j];
+#pragma unroll 1
+            for (int kk = 0; kk < kL; kk += 16)  // dv_or[s][p] = sum_t W[t][s] dy[t][p]  (rows s in lanes 0-63)
+              mma_bf16(TW(j), mdesc(sm.W[j], kL, kk), mdesc(sg.dy, kL, kk), idesc_bf16(128, 64, true, true), kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < kP; kk += 16)  // dB^T[n][s] += sum_p dS[n][p] dvd[s][p]
+              mma_bf16(ACC_B, kdesc(sg.dS, kN, kk), kdesc(sm.dvd[j], kL, kk), idesc_bf16(128, 64, false, false),
+                       !(first && kk == 0));
+#pragma unroll 1
+            for (int kk = 0; kk < kP; kk += 16)  // dC^T[n][t] += sum_p S[n][p] dch[t][p]
+              mma_bf16(ACC_C, kdesc(sg.S, kN, kk), kdesc(sm.dch[j], kL, kk), idesc_bf16(128, 64, false, false),
+                       !(first && kk == 0));
+            mma_commit(&sm.s2_done[j]);
+            mma_commit(&sm.empty[j]);
+            if (last) {
+              // dB^T[n][s] += sum_t C[t][n] dCBsum[t][s],  dC^T[n][t] += sum_s B[s][n] dCBsum[t][s]
+              const uint32_t b0 = smem_u32(sm.BC[0]), c0 = smem_u32(sm.BC[1]);
+#pragma unroll 1
+              for (int kk = 0; kk < kL; kk += 16) {
+                mma_bf16(ACC_B, sdesc_sw128(c0 + kk * 128, 2 * kTileLP, 1024), mdesc(sm.dcbs, kL, kk),
+                         idesc_bf16(128, 64, true, true), true);
+                mma_bf16(ACC_C, sdesc_sw128(b0 + kk * 128, 2 * kTileLP, 1024), kdesc(sm.dcbs, kL, kk),
+                         idesc_bf16(128, 64, true, false), true);
+              }
+              mma_commit(&sm.acc_full);
+              mma_commit(&sm.chunk_empty);
+            }
+            ++n2;
+            c2.next(prm);
+            moved = true;
+          }
+        }
+        if (moved) {
+          idle = 0;
+        } else if (__nanosleep(32), ++idle > (1u << 25)) {
+          atomicCAS(status, 0, 103);
+          break;
+        }
+      }
+      mma_commit(&sm.drain);  // nothing may still be writing TMEM when it is freed
+      mbar_wait(&sm.drain, 0, status, 104);
+    }
+  } else if (warp == kWarpScal) {
+    // ------------------------------------------------------------ SC: K1 scalars, up to four heads ahead
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    HeadCursor hr;
+    hr.seek(prm, q0);
+    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+      const int k = q & 3;
+      if (q >= 4 && !mbar_wait(&sm.sc_free[k], ((q >> 2) - 1) & 1, status, 105)) break;
+      const int h = hr.h(prm);
+      const float A_h = prm.A[h];
+      const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
+      const float z0 = prm.dt_raw[rr * H + h], z1 = prm.dt_raw[(rr + 1) * H + h];
+      const float d0 = softplus_f(z0), d1 = softplus_f(z1);
+      const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
+      float inc = a1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      const float c0 = inc - a1 + a0, c1 = inc;
+      const float cend = __shfl_sync(0xffffffffu, inc, 31);
+      sm.cum[k][t0] = c0;
+      sm.cum[k][t1] = c1;
+      sm.dtp[k][t0] = d0;
+      sm.dtp[k][t1] = d1;
+      sm.z[k][t0] = z0;
+      sm.z[k][t1] = z1;
+      sm.ecum[k][t0] = expf(c0);
+      sm.ecum[k][t1] = expf(c1);
+      sm.dec[k][t0] = expf(cend - c0);
+      sm.dec[k][t1] = expf(cend - c1);
+      if (lane == 0) {
+        sm.aend[k] = expf(cend);
+        sm.Ah[k] = A_h;
+      }
+      const float e0 = __shfl_sync(0xffffffffu, c1, 7), e1 = __shfl_sync(0xffffffffu, c1, 15);
+      const float e2 = __shfl_sync(0xffffffffu, c1, 23), e3 = __shfl_sync(0xffffffffu, c1, 31);
+      const int blk = t0 >> 4;
+      const float my_end = blk == 0 ? e0 : (blk == 1 ? e1 : (blk == 2 ? e2 : e3));
+      const float g0 = expf(my_end - c0), g1 = expf(my_end - c1);  // decay to the end of the 16-block
+      sm.G[k][t0] = g0;
+      sm.G[k][t1] = g1;
+      sm.Gd[k][t0] = g0 * d0;
+      sm.Gd[k][t1] = g1 * d1;
+      const float ends[4] = {e0, e1, e2, e3};
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        sm.E[k][t0][qq] = (qq < blk) ? expf(c0 - ends[qq]) : 0.f;
+        sm.E[k][t1][qq] = (qq < blk) ? expf(c1 - ends[qq]) : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.sc_ready[k]);
+    }
+  } else if (warp == kWarpAsm) {
+    // ------------------------------------------------------------ AS: d cum assembly per head
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    HeadCursor hr;
+    hr.seek(prm, q0);
+    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      const int h = hr.h(prm);
+      bool ok = mbar_wait(&sm.e_done[j], ph, status, 106);
+      ok = ok && mbar_wait(&sm.bk_done[j], ph, status, 107);
+      ok = ok && mbar_wait(&sm.o_done[j], ph, status, 108);
+      if (!ok) break;
+      const float A_h = sm.Ah[k];
+      // d cum per position: ORANGE row - column sums, BLUE, K3; K3's and K4's chunk-end terms at t = 63
+      const float dec0 = sm.dec[k][t0], dec1 = sm.dec[k][t1];
+      const float k3_0 = sm.dde[j][t0] * dec0, k3_1 = sm.dde[j][t1] * dec1;
+      float dc0 = sm.drow[j][t0] - (sm.dcolp[j][0][t0] + sm.dcolp[j][1][t0] + sm.dcolp[j][2][t0] + sm.dcolp[j][3][t0]) +
+                  sm.dcb[j][t0] - k3_0;
+      float dc1 = sm.drow[j][t1] - (sm.dcolp[j][0][t1] + sm.dcolp[j][1][t1] + sm.dcolp[j][2][t1] + sm.dcolp[j][3][t1]) +
+                  sm.dcb[j][t1] - k3_1;
+      float k3sum = k3_0 + k3_1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) k3sum += __shfl_xor_sync(0xffffffffu, k3sum, o);
+      const float k4 = sm.aend[k] * (sm.k4p[j][0] + sm.k4p[j][1] + sm.k4p[j][2] + sm.k4p[j][3]);
+      if (lane == 31) dc1 += k3sum + k4;
+      // suffix sums (K1 backward): dda[t] = sum_{u >= t} d cum[u]
+      const float pair = dc0 + dc1;
+      float suf = pair;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += u;
+      }
+      const float dda0 = suf, dda1 = suf - dc0;
+      const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
+      prm.ddt_raw[rr * H + h] = (sm.dvx[j][t0] + A_h * dda0) * sigmoid_f(sm.z[k][t0]);
+      prm.ddt_raw[(rr + 1) * H + h] = (sm.dvx[j][t1] + A_h * dda1) * sigmoid_f(sm.z[k][t1]);
+      float dAp = dda0 * sm.dtp[k][t0] + dda1 * sm.dtp[k][t1];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
+      if (lane == 0) prm.dA_part[((size_t)hr.b * H + h) * nc + hr.c] = dAp;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.fin_done[j]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+    }
+  } else if (warp >= kWarpP0) {
+    // ------------------------------------------------------------ P: dch and dvd tiles
+    const int pt = tid - 32 * kWarpP0;  // 0..127
+    for (int q = 0; q < nh; ++q) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      bool ok = mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 110);
+      ok = ok && mbar_wait(&sm.full[j], ph, status, 111);
+      if (ok && q >= 2) ok = mbar_wait(&sm.s2_done[j], ph ^ 1, status, 112);  // set 2 of q-2 read dch, dvd
+      if (ok && q >= 2) ok = mbar_wait(&sm.o_done[j], ph ^ 1, status, 109);   // and O of q-2 sent dx from dch
+      if (named_bar_or(4, 128, !ok)) break;
+      const BwdcSmem::Stage& sg = sm.st[j];
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        const int ch = pt + 128 * i;
+        const int t = ch >> 3, jj = ch & 7;
+        const uint32_t off = sw128_chunk(t, jj);
+        const uint4 rx = *reinterpret_cast<const uint4*>(sg.x + off);
+        const uint4 ry = *reinterpret_cast<const uint4*>(sg.dy + off);
+        const float fx = sm.dec[k][t] * sm.dtp[k][t], fy = sm.ecum[k][t];
+        const uint32_t ix[4] = {rx.x, rx.y, rx.z, rx.w}, iy[4] = {ry.x, ry.y, ry.z, ry.w};
+        uint32_t ox[4], oy[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 vx = unpack_bf16(ix[e]), vy = unpack_bf16(iy[e]);
+          ox[e] = pack_bf16(fx * vx.x, fx * vx.y);
+          oy[e] = pack_bf16(fy * vy.x, fy * vy.y);
+        }
+        *reinterpret_cast<uint4*>(sm.dvd[j] + off) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+        *reinterpret_cast<uint4*>(sm.dch[j] + off) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+      }
+      fence_proxy_async();
+      named_bar(4, 128);
+      if (pt == 0) {
+        mbar_arrive(&sm.pre_done[j]);
+        mbar_arrive(&sm.empty[j]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+    }
+  } else if (warp >= kWarpK0) {
+    // ------------------------------------------------------------ BK: BLUE and K4
+    const int n = tid - 32 * kWarpK0;  // 0..127: S / dS row for K4
+    const int q4 = warp & 3;
+    for (int q = 0; q < nh; ++q) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      bool ok = mbar_wait(&sm.s1_done[j], ph, status, 113);
+      ok = ok && mbar_wait(&sm.full[j], ph, status, 114);
+      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 115);
+      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 116);
+      if (named_bar_or(3, 128, !ok)) break;
+      tc_fence_after();
+      const BwdcSmem::Stage& sg = sm.st[j];
+      {  // K4: <dS_{c+1}, S_c>
+        float part = 0.f;
+#pragma unroll 1
+        for (int jj = 0; jj < 8; ++jj) {
+          float sv[8], dv[8];
+          load_row8(sg.S, n, jj, sv);
+          load_row8(sg.dS, n, jj, dv);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) part += dv[u] * sv[u];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) sm.k4p[j][q4] = part;
+      }
+      if (q4 >= 2) {  // BLUE d cum: exp(cum_t) sum_p dy[t][p] Y[t][p]; Y row t sits in lane 64 + t
+        const int t = 32 * (q4 - 2) + lane;
+        float acc = 0.f;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          float yv[32];
+          tmem_ld32(taddr(YD(j), 32 * q4, 64 + 32 * hf), yv);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float gv[8];
+            load_row8(sg.dy, t, 4 * hf + jj, gv);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc += gv[u] * yv[8 * jj + u];
+          }
+        }
+        sm.dcb[j][t] = acc * sm.ecum[k][t];
+      }
+      tc_fence_before();
+      named_bar(3, 128);
+      if (n == 0) {
+        mbar_arrive(&sm.bk_done[j]);
+        mbar_arrive(&sm.empty[j]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+    }
+  } else if (warp >= kWarpE0) {
+    // ------------------------------------------------------------ E: W, the dCB sum and the ORANGE sums
+    const int q4 = warp & 3;
+    const int hl = lane >> 4, t = 16 * q4 + (lane & 15);
+    // this lane covers columns s = 16 jj + 8 hl + e (jj, e < 4, 8) of row t: every lane meets all four
+    // 16-column blocks, so the branch on the block below is uniform across the warp
+    int seg = -1;
+    HeadCursor hc;
+    hc.seek(prm, q0);
+    for (int q = 0; q < nh; ++q, hc.next(prm)) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      const bool first = hc.first(q0), last = hc.last(prm, q1);
+      if (first) ++seg;
+      const float* cbrow = prm.CB + ((size_t)hc.k * kL + t) * kL + 8 * hl;
+      bool ok = mbar_wait(&sm.s1_done[j], ph, status, 117);
+      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 118);
+      if (ok && q >= 2) ok = mbar_wait(&sm.s2_done[j], ph ^ 1, status, 119);   // W[j] read by set 2 of q-2
+      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 120);  // partial slot of q-2
+      // the bf16 dCB sum of the previous run must have been read by its MMAs
+      if (ok && last && seg >= 1) ok = mbar_wait(&sm.chunk_empty, (seg - 1) & 1, status, 126);
+      if (named_bar_or(2, 128, !ok)) break;
+      tc_fence_after();
+      const float ct = sm.cum[k][t];
+      float rowsum = 0.f;
+#pragma unroll 1
+      for (int jj = 0; jj < 4; ++jj) {
+        const int s0 = 16 * jj + 8 * hl;
+        uint32_t r8[8];  // lane l: row t, columns s0 .. s0 + 7 (lanes 16-31 read their rows' upper 8)
+        tmem_ld_pair8(taddr(TW(j), 32 * q4, 16 * jj), r8);
+        const float4 ca = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj));
+        const float4 cb4 = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj + 4));
+        const float cb[8] = {ca.x, ca.y, ca.z, ca.w, cb4.x, cb4.y, cb4.z, cb4.w};
+        tmem_wait_ld();
+        float w[8], dcb[8];
+        if (jj < q4) {  // block before the row's block: exp(cum_t - cum_s) = E_t[jj] G_s
+          const float f = sm.E[k][t][jj];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            w[e] = cb[e] * (f * sm.G[k][s0 + e]);
+            dcb[e] = __uint_as_float(r8[e]) * (f * sm.Gd[k][s0 + e]);
+          }
+        } else if (jj == q4) {  // the diagonal block, masked before the exponential
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = s0 + e;
+            const float ex = (s <= t) ? expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
+            w[e] = cb[e] * ex;
+            dcb[e] = __uint_as_float(r8[e]) * sm.dtp[k][s] * ex;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            w[e] = 0.f;
+            dcb[e] = 0.f;
+          }
+        }
+        store_row_bf16(sm.W[j], t, hl + 2 * jj, w, 1);
+        // the run's dCB sum, fp32; its last head also writes the bf16 copy for the MMA
+        float4* acc = reinterpret_cast<float4*>(&sm.dcbacc[t][s0]);
+        float4 lo = make_float4(dcb[0], dcb[1], dcb[2], dcb[3]), hi = make_float4(dcb[4], dcb[5], dcb[6], dcb[7]);
+        if (!first) {
+          const float4 a0 = acc[0], a1 = acc[1];
+          lo = make_float4(lo.x + a0.x, lo.y + a0.y, lo.z + a0.z, lo.w + a0.w);
+          hi = make_float4(hi.x + a1.x, hi.y + a1.y, hi.z + a1.z, hi.w + a1.w);
+        }
+        if (last) {
+          const float sum8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          store_row_bf16(sm.dcbs, t, hl + 2 * jj, sum8, 1);
+        } else {
+          acc[0] = lo;
+          acc[1] = hi;
+        }
+        float dd[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          dd[e] = dcb[e] * cb[e];  // d_diff = dW o decay o dt' o CB
+          rowsum += dd[e];
+        }
+        // column sums of these 8 columns over the 16 rows of this half: transposing butterfly
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const bool up = lane & 8;
+          const float send = up ? dd[kk] : dd[kk + 4], keep = up ? dd[kk + 4] : dd[kk];
+          dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const bool up = lane & 4;
+          const float send = up ? dd[kk] : dd[kk + 2], keep = up ? dd[kk + 2] : dd[kk];
+          dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        {
+          const bool up = lane & 2;
+          const float send = up ? dd[0] : dd[1], keep = up ? dd[1] : dd[0];
+          dd[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        dd[0] += __shfl_xor_sync(0xffffffffu, dd[0], 1);
+        // lanes l and l ^ 1 now both hold column s0 + 4 b3 + 2 b2 + b1 (b_i: bits of the lane)
+        if (!(lane & 1)) sm.dcolp[j][q4][s0 + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1)] = dd[0];
+      }
+      rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
+      if (lane < 16) sm.drow[j][t] = rowsum;
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(2, 128);
+      if (tid == 32 * kWarpE0) {
+        mbar_arrive(&sm.e_done[j]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ O warps 0-3
+    const int ot = tid;  // 0..127
+    const int q4 = warp;
+    int seg = -1;
+    HeadCursor hr;
+    hr.seek(prm, q0);
+    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      if (hr.first(q0)) ++seg;
+      bool ok = mbar_wait(&sm.s2_done[j], ph, status, 121);
+      ok = ok && mbar_wait(&sm.full[j], ph, status, 122);
+      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 123);
+      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 124);
+      if (named_bar_or(1, 128, !ok)) break;
+      tc_fence_after();
+      const BwdcSmem::Stage& sg = sm.st[j];
+      if (q4 < 2) {  // dv = dv_or + exp(cum_end - cum_s) ddv; rows s = lanes 0-63 of TW and YD
+        const int s = 32 * q4 + lane;
+        const float e = sm.dec[k][s], d = sm.dtp[k][s];
+        float sx = 0.f, sd = 0.f;
+#pragma unroll 1
+        for (int qq = 0; qq < 4; ++qq) {  // 16 columns at a time
+          uint32_t ro[16], rd[16];
+          tmem_ld16_nowait(taddr(TW(j), 32 * q4, 16 * qq), ro);
+          tmem_ld16_nowait(taddr(YD(j), 32 * q4, 16 * qq), rd);
+          tmem_wait_ld();
+          float dxv[16];
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            float xv[8];
+            load_row8(sg.x, s, 2 * qq + jj, xv);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int p = 8 * jj + u;
+              const float ddv = __uint_as_float(rd[p]);
+              const float dv = __uint_as_float(ro[p]) + e * ddv;
+              sx += dv * xv[u];
+              sd += ddv * xv[u];
+              dxv[p] = d * dv;
+            }
+          }
+          store_row_bf16(sm.dch[j], s, 2 * qq, dxv, 2);  // dch[j] is free once set 2 has run
+        }
+        sm.dvx[j][s] = sx;
+        sm.dde[j][s] = sd * d;  // sum_p ddv[s][p] v[s][p]
+      }
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(1, 128);
+      if (ot == 0) {
+        tma_store_2d(&tm_dx, sm.dch[j], hr.h(prm) * kP, hr.b * T + hr.c * kL);
+        tma_store_commit();
+        tma_store_wait_read0();  // P may refill dch[j] once o_done says so
+        mbar_arrive(&sm.o_done[j]);
+        mbar_arrive(&sm.empty[j]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+      if (hr.last(prm, q1)) {
+        // the chunk run ends: dB^T and dC^T (lane n, column s or t) to this CTA's partial slot of chunk k
+        ok = mbar_wait(&sm.acc_full, seg & 1, status, 125);
+        if (named_bar_or(1, 128, !ok)) break;
+        tc_fence_after();
+        const long long slot =
+            (long long)hr.k * prm.nseg + ((long long)blockIdx.x - cta_of((long long)hr.k * prm.hpg, total, gridDim.x));
+        float* pb = prm.dB_part + (size_t)slot * kL * kN;
+        float* pc = prm.dC_part + (size_t)slot * kL * kN;
+        const int n = 32 * q4 + lane;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t vb[32], vc[32];
+          tmem_ld32_nowait(taddr(ACC_B, 32 * q4, 32 * hf), vb);
+          tmem_ld32_nowait(taddr(ACC_C, 32 * q4, 32 * hf), vc);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            pb[(32 * hf + e) * kN + n] = __uint_as_float(vb[e]);
+            pc[(32 * hf + e) * kN + n] = __uint_as_float(vc[e]);
+          }
+        }
+        tc_fence_before();
+        named_bar(1, 128);
+        if (ot == 0) mbar_arrive(&sm.acc_free);
+      }
+    }
+    if (ot == 0) tma_store_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// dB / dC of chunk k = sum of its partial slots, in CTA order.
+__global__ void k_bwdc_dbdc_sum(const float* dB_part, const float* dC_part, __nv_bfloat16* dB, __nv_bfloat16* dC,
+                                long long nchunks, int nseg, long long total, long long grid, int hpg, int T, int G,
+                                int nc) {
+  const long long count = nchunks * kL * kN;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < count;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long k = e / (kL * kN);
+    const int tn = (int)(e - k * kL * kN);
+    const long long first = cta_of(k * hpg, total, grid), last = cta_of((k + 1) * hpg - 1, total, grid);
+    float sb = 0.f, sc = 0.f;
+    for (long long s = 0; s <= last - first; ++s) {
+      sb += dB_part[(k * nseg + s) * kL * kN + tn];
+      sc += dC_part[(k * nseg + s) * kL * kN + tn];
+    }
+    const int g = (int)(k % G);
+    const long long bc = k / G;
+    const int c = (int)(bc % nc), b = (int)(bc / nc);
+    const int t = tn / kN, n = tn % kN;
+    const size_t o = (((size_t)b * T + c * kL + t) * G + g) * kN + n;
+    dB[o] = __float2bfloat16_rn(sb);
+    dC[o] = __float2bfloat16_rn(sc);
+  }
+}
+
+__global__ void k_bwdc_dA_sum(const float* part, float* dA, int b, int H, int nc) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= H) return;
+  float acc = 0.f;
+  for (int bb = 0; bb < b; ++bb)
+    for (int c = 0; c < nc; ++c) acc += part[((size_t)bb * H + h) * nc + c];
+  dA[h] = acc;
+}
+
+struct BwdcLayout {
+  long long total, nchunks;
+  int grid, nseg;
+};
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+BwdcLayout layout(const Dims& d, int sms) {
+  BwdcLayout l;
+  l.nchunks = (long long)d.b * d.nc * d.G;
+  l.total = l.nchunks * d.hpg;
+  l.grid = (int)(l.total < sms ? l.total : sms);
+  if (l.grid < 1) l.grid = 1;
+  // most CTAs one chunk's heads can span: ceil(hpg / min items per CTA) + 1
+  const long long per = l.total / l.grid;
+  l.nseg = (int)((d.hpg + per - 1) / per + 1);
+  return l;
+}
+
+struct BwdcWs {
+  __nv_bfloat16* states;   // S_c   [b,H,nc][N][P]
+  __nv_bfloat16* dstates;  // dS_{c+1}
+  float* CB;               // [b,nc,G,L,L]
+  float* dB_part;
+  float* dC_part;
+  float* dA_part;
+};
+
+BwdcWs carve(const Dims& d, const BwdcLayout& l, Carver& cv) {
+  BwdcWs w;
+  w.states = cv.take<__nv_bfloat16>((size_t)d.b * d.H * d.nc * kN * kP);
+  w.dstates = cv.take<__nv_bfloat16>((size_t)d.b * d.H * d.nc * kN * kP);
+  w.CB = cv.take<float>((size_t)l.nchunks * kL * kL);
+  w.dB_part = cv.take<float>((size_t)l.nchunks * l.nseg * kL * kN);
+  w.dC_part = cv.take<float>((size_t)l.nchunks * l.nseg * kL * kN);
+  w.dA_part = cv.take<float>((size_t)d.b * d.H * d.nc);
+  return w;
+}
+
+// The workspace is sized for the largest grid (the device's SM count may not
+// be known when it is sized): slots for a grid of 1024 CTAs cover any smaller grid.
+constexpr int kMaxGrid = 1024;
+
+}  // namespace
+
+size_t tc_backward_ws(const Dims& d) {
+  Carver cv(nullptr);
+  carve(d, layout(d, kMaxGrid), cv);
+  return cv.off;
+}
+
+cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st) {
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorNoDevice;
+  const BwdcLayout l = layout(d, sms < kMaxGrid ? sms : kMaxGrid);
+  const BwdcLayout lmax = layout(d, kMaxGrid);
+  Carver cv(ws);
+  BwdcWs w = carve(d, lmax, cv);
+  int* status = static_cast<int*>(ws);
+  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, st);
+  if (e == cudaSuccess) e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, nullptr, w.states, status, st);
+  if (e == cudaSuccess) e = tc_scan(d, true, a.dy, a.C, a.dt_raw, a.A, a.ds_final, a.ds0, w.dstates, status, st);
+  if (e != cudaSuccess) return e;
+  const uint64_t rows = (uint64_t)d.b * d.T;
+  const uint64_t srows = (uint64_t)d.b * d.H * d.nc * kN;
+  CUtensorMap tx, tdy, tdx, tb, tcm, ts, tds;
+  e = make_tmap_2d_bf16(&tx, a.x, (uint64_t)d.H * kP, rows, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdy, a.dy, (uint64_t)d.H * kP, rows, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdx, a.dx, (uint64_t)d.H * kP, rows, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tb, a.B, d.N, d.G, rows, 64, 1, 64);
+  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tcm, a.C, d.N, d.G, rows, 64, 1, 64);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, w.states, kP, srows, 64, kN);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tds, w.dstates, kP, srows, 64, kN);
+  if (e != cudaSuccess) return e;
+  // partial slots use the layout of the launched grid (nseg of the largest grid bounds it)
+  BwdcParams prm{a.dt_raw, a.A, w.CB, a.ddt_raw, w.dA_part, w.dB_part, w.dC_part, status,
+                 d.T,      d.H, d.G,  d.hpg,     d.nc,      lmax.nseg, (int)l.total};
+  const int smem = (int)sizeof(BwdcSmem) + 1024;
+  e = cudaFuncSetAttribute(k_tc_bwdc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  SSD_LAUNCH("k_tc_bwd_chunk", st, k_tc_bwdc<<<l.grid, kThreads, smem, st>>>(tx, tdy, tdx, tb, tcm, ts, tds, prm));
+  const long long cnt = l.nchunks * kL * kN;
+  const int blocks = (int)((cnt + 255) / 256 < 4096 ? (cnt + 255) / 256 : 4096);
+  SSD_LAUNCH("k_tc_dbdc_sum", st,
+             k_bwdc_dbdc_sum<<<blocks, 256, 0, st>>>(w.dB_part, w.dC_part, static_cast<__nv_bfloat16*>(a.dB),
+                                                     static_cast<__nv_bfloat16*>(a.dC), l.nchunks, lmax.nseg, l.total,
+                                                     l.grid, d.hpg, d.T, d.G, d.nc));
+  SSD_LAUNCH("k_tc_dA_sum", st, k_bwdc_dA_sum<<<(d.H + 127) / 128, 128, 0, st>>>(w.dA_part, a.dA, d.b, d.H, d.nc));
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

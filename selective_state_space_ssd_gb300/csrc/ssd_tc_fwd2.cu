@@ -440,7 +440,10 @@ __global__ void __launch_bounds__(256) k_cb(const __nv_bfloat16* B, const __nv_b
 bool tc_forward_supported(const Dims& d) {
   return d.variant == kMamba2 && d.bf16 && d.L == kL && d.P == kP && d.N == kN;
 }
-bool tc_backward_supported(const Dims& d) { return tc_forward_supported(d); }
+// The chunk-parallel backward indexes its (chunk, head) items with 32-bit integers.
+bool tc_backward_supported(const Dims& d) {
+  return tc_forward_supported(d) && (long long)d.b * d.nc * d.H < (1ll << 31);
+}
 
 size_t tc_fwd2_ws(const Dims& d) {
   Carver cv(nullptr);
