@@ -52,27 +52,29 @@ using namespace tc;
 
 constexpr int kL = 64, kP = 64, kN = 128;
 constexpr int kThreads = 640;
-constexpr int kWarpE0 = 4, kWarpK0 = 8, kWarpP0 = 12, kWarpScal = 16, kWarpAsm = 17, kWarpTma = 18,
-              kWarpMma = 19;
+constexpr int kWarpE0 = 4, kWarpEB0 = 10, kWarpP0 = 12, kWarpScal = 16, kWarpAsm = 17, kWarpMma = 18,
+              kWarpTma = 19;
 constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
 constexpr uint32_t kTileNP = kN * kP * 2;  // 16 KB
-constexpr uint32_t kStageBytes = 2 * kTileLP + 2 * kTileNP;  // 48 KB
 constexpr uint32_t kTmemCols = 512;
 
 struct alignas(1024) BwdcSmem {
-  struct Stage {
+  // per-head TMA tiles in two rings: x, dy (three slots, free after dv_or) and dS, S (two slots, free
+  // once the YD and state MMAs and K4 have read them)
+  struct XY {
     uint8_t x[kTileLP];   // [s][p]
     uint8_t dy[kTileLP];  // [t][p]
+  } xy[3];
+  struct SD {
     uint8_t dS[kTileNP];  // dS_{c+1} bf16 [n][p]
     uint8_t S[kTileNP];   // S_c bf16 [n][p], right after dS: [dS | S] is one MN-major operand
-  } st[2];
+  } sd[2];
   uint8_t BC[4][kTileLP];   // B atom 0, C atom 0, B atom 1, C atom 1 ([t][64 n] each): [B; C] is one
                             // K-major operand of 128 rows
   uint8_t dch[2][kTileLP];  // exp(cum) dy [t][p]; after set 2 the dx staging tile [s][p]
   uint8_t dvd[2][kTileLP];  // exp(cum_end - cum) dt' x [s][p]
   uint8_t W[2][kTileLP];    // [t][s]; (the 8 KB after W[j] feed the unused upper rows of dv_or)
-  uint8_t dcbs[kTileLP];    // sum over the chunk run of dCB [t][s], bf16
-  float dcbacc[kL][kL + 4];  // the same sum in fp32 while the run goes on
+  uint8_t dcbs[kTileLP];    // sum over the chunk run of dCB [t][s], bf16 (the fp32 sum lives in E's registers)
   // K1 scalars, ring of four heads.  G_s = exp(cum_e(s) - cum_s), Gd_s = G_s dt'_s and
   // E_t[j] = exp(cum_t - cum_e(j)), where e(j) is the last position of 16-block j: exp(cum_t - cum_s)
   // for s in an earlier block than t is E_t[blk(s)] G_s (both factors <= 1).
@@ -80,8 +82,9 @@ struct alignas(1024) BwdcSmem {
   float E[4][kL][4];
   float aend[4], Ah[4];
   // per-head partial sums for the d cum assembly
-  float drow[2][kL], dcolp[2][4][kL], dcb[2][kL], dde[2][kL], dvx[2][kL], k4p[2][4];
-  uint64_t full[2], empty[2], pre_done[2], s1_done[2], e_done[2], s2_done[2], bk_done[2], o_done[2], fin_done[2];
+  float drow[2][2][kL], dcolp[2][4][kL], dcb[2][kL], dde[2][2][kL], dvx[2][2][kL], k4p[2][2];
+  uint64_t xy_full[3], xy_empty[3], sd_full[2], sd_empty[2];
+  uint64_t pre_done[2], s1a_done[2], s1_done[2], e_done[2], s2_done[2], bk_done[2], o_done[2], fin_done[2];
   uint64_t sc_ready[4], sc_free[4];
   uint64_t chunk_full, chunk_empty, acc_full, acc_free, drain;
   uint32_t tmem_slot;
@@ -90,7 +93,8 @@ struct alignas(1024) BwdcSmem {
 struct BwdcParams {
   const float* dt_raw;
   const float* A;
-  const float* CB;  // [b, nc, G, L, L] fp32
+  const float* CB;               // [b, nc, G, L, L] fp32
+  const __nv_bfloat16* x;        // [b, T, H, P]: O reads its rows from L2, so the stage need not wait for O
   float* ddt_raw;
   float* dA_part;  // [b, H, nc]
   float* dB_part;  // [chunks][nseg][L][N]
@@ -150,6 +154,84 @@ __device__ __forceinline__ void load_row8(const uint8_t* tile, int r, int j, flo
   }
 }
 
+// W, the run's dCB sum and the ORANGE sums for the 16-column blocks jlo and
+// jlo + 1, where at or left of the diagonal block of rows t = 16 q4 + (lane & 15)
+// (the rest is zero; see the kernel's set-up).  Lane l < 16 takes columns
+// 16 jj .. 16 jj + 7 of its row and lane l + 16 the other 8, so every warp
+// meets each block whole and the branch on the block is warp-uniform.  cbv
+// holds CB[t][s0 .. s0 + 7] of both blocks (s0 = 16 jj + 8 (lane >> 4)) and
+// dacc the run's fp32 dCB sum of the same elements.
+// Returns the lane's part of its row sum of d_diff.
+__device__ __forceinline__ float e_blocks(BwdcSmem& sm, uint32_t tw, const float (&cbv)[16], float (&dacc)[16], int j,
+                                          int k, int q4, int jlo, bool first, bool last) {
+  const int lane = threadIdx.x & 31, hl = lane >> 4, t = 16 * q4 + (lane & 15);
+  const float ct = sm.cum[k][t];
+  float rowsum = 0.f;
+  uint32_t rr[2][8];  // dW~[t][s0 .. s0 + 7] of both blocks (lanes 16-31 read their rows' upper 8 columns)
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+    if (jlo + b <= q4) tmem_ld_pair8(taddr(tw, 32 * q4, 16 * (jlo + b)), rr[b]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const int jj = jlo + b;
+    if (jj > q4) break;
+    const int s0 = 16 * jj + 8 * hl;
+    const uint32_t* r8 = rr[b];
+    const float* cb = cbv + 8 * b;
+    float w[8], dcb[8];
+    if (jj < q4) {  // block before the row's block: exp(cum_t - cum_s) = E_t[jj] G_s
+      const float f = sm.E[k][t][jj];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        w[e] = cb[e] * (f * sm.G[k][s0 + e]);
+        dcb[e] = __uint_as_float(r8[e]) * (f * sm.Gd[k][s0 + e]);
+      }
+    } else {  // the diagonal block, masked before the exponential
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int s = s0 + e;
+        const float ex = (s <= t) ? expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
+        w[e] = cb[e] * ex;
+        dcb[e] = __uint_as_float(r8[e]) * sm.dtp[k][s] * ex;
+      }
+    }
+    store_row_bf16(sm.W[j], t, hl + 2 * jj, w, 1);
+    // the run's dCB sum, fp32; its last head also writes the bf16 copy for the MMA
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dacc[8 * b + e] = first ? dcb[e] : dacc[8 * b + e] + dcb[e];
+    if (last) store_row_bf16(sm.dcbs, t, hl + 2 * jj, dacc + 8 * b, 1);
+    float dd[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      dd[e] = dcb[e] * cb[e];  // d_diff = dW o decay o dt' o CB
+      rowsum += dd[e];
+    }
+    // column sums of these 8 columns over the 16 rows of this half: transposing butterfly
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const bool up = lane & 8;
+      const float send = up ? dd[kk] : dd[kk + 4], keep = up ? dd[kk + 4] : dd[kk];
+      dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const bool up = lane & 4;
+      const float send = up ? dd[kk] : dd[kk + 2], keep = up ? dd[kk + 2] : dd[kk];
+      dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+      const bool up = lane & 2;
+      const float send = up ? dd[0] : dd[1], keep = up ? dd[1] : dd[0];
+      dd[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    dd[0] += __shfl_xor_sync(0xffffffffu, dd[0], 1);
+    // lanes l and l ^ 1 now both hold column s0 + 4 b3 + 2 b2 + b1 (b_i: bits of the lane)
+    if (!(lane & 1)) sm.dcolp[j][q4][s0 + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1)] = dd[0];
+  }
+  return rowsum + __shfl_xor_sync(0xffffffffu, rowsum, 16);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_bwdc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
               const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_B,
@@ -167,19 +249,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int j = 0; j < 2; ++j) {
-      mbar_init(&sm.full[j], 1);
-      mbar_init(&sm.empty[j], 4);  // MMA commit + P, BK, O warps
+      mbar_init(&sm.sd_full[j], 1);
+      mbar_init(&sm.sd_empty[j], 2);  // MMA commit (after set 1) + BK warps
       mbar_init(&sm.pre_done[j], 1);
+      mbar_init(&sm.s1a_done[j], 1);
       mbar_init(&sm.s1_done[j], 1);
-      mbar_init(&sm.e_done[j], 1);
+      mbar_init(&sm.e_done[j], 2);  // E warps (column blocks 0-1) and EB warps (blocks 2-3)
       mbar_init(&sm.s2_done[j], 1);
       mbar_init(&sm.bk_done[j], 1);
       mbar_init(&sm.o_done[j], 1);
       mbar_init(&sm.fin_done[j], 1);
     }
+    for (int x = 0; x < 3; ++x) {
+      mbar_init(&sm.xy_full[x], 1);
+      mbar_init(&sm.xy_empty[x], 3);  // MMA commit (after D) + P, BK warps
+    }
     for (int k = 0; k < 4; ++k) {
       mbar_init(&sm.sc_ready[k], 1);
-      mbar_init(&sm.sc_free[k], 5);  // P, E, BK, O, AS
+      mbar_init(&sm.sc_free[k], 6);  // P, E, EB, BK, O, AS
     }
     mbar_init(&sm.chunk_full, 1);
     mbar_init(&sm.chunk_empty, 1);
@@ -189,6 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init_fence();
   }
   if (warp == kWarpMma) tmem_alloc(&sm.tmem_slot, kTmemCols);
+  // W, the dCB sum, the column sums and the second row-sum part are zero above the diagonal blocks
+  // for every head: written once here, never touched by the per-head work
+  for (int i = tid; i < (int)(3 * kTileLP / 16); i += kThreads)
+    reinterpret_cast<uint4*>(sm.W[0])[i] = make_uint4(0, 0, 0, 0);  // W[0], W[1], dcbs are contiguous
+  for (int i = tid; i < 2 * 4 * kL; i += kThreads) (&sm.dcolp[0][0][0])[i] = 0.f;
+  for (int i = tid; i < 2 * kL; i += kThreads) sm.drow[i / kL][1][i % kL] = 0.f;
+  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -224,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sm.BC[2 * a + 1], &tm_C, a * 64, hr.g, row, &sm.chunk_full);
           }
         }
-        if (q + 2 < nh) {  // warm L2 with the tiles of head q + 2 while the ring is still busy
+        if (q + 2 < nh) {  // warm L2 with the tiles of head q + 2 while the rings are still busy
           const int prow = hp.b * T + hp.c * kL;
           const int psrow = (int)((((size_t)hp.b * H + hp.h(prm)) * nc + hp.c) * kN);
           tma_prefetch_2d(&tm_x, hp.h(prm) * kP, prow);
@@ -232,96 +326,97 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_prefetch_2d(&tm_S, 0, psrow);
           tma_prefetch_2d(&tm_dS, 0, psrow);
         }
-        if (q >= 2 && !mbar_wait(&sm.empty[j], ((q >> 1) - 1) & 1, status, 102)) break;
-        BwdcSmem::Stage& sg = sm.st[j];
-        mbar_expect_tx(&sm.full[j], kStageBytes);
-        tma_load_2d(sg.x, &tm_x, hr.h(prm) * kP, row, &sm.full[j]);
-        tma_load_2d(sg.dy, &tm_dy, hr.h(prm) * kP, row, &sm.full[j]);
+        const int x3 = q % 3, xr = q / 3;
+        if (q >= 3 && !mbar_wait(&sm.xy_empty[x3], (xr - 1) & 1, status, 102)) break;
+        mbar_expect_tx(&sm.xy_full[x3], 2 * kTileLP);
+        tma_load_2d(sm.xy[x3].x, &tm_x, hr.h(prm) * kP, row, &sm.xy_full[x3]);
+        tma_load_2d(sm.xy[x3].dy, &tm_dy, hr.h(prm) * kP, row, &sm.xy_full[x3]);
+        if (q >= 2 && !mbar_wait(&sm.sd_empty[j], ((q >> 1) - 1) & 1, status, 99)) break;
         const int srow = (int)((((size_t)hr.b * H + hr.h(prm)) * nc + hr.c) * kN);
-        tma_load_2d(sg.dS, &tm_dS, 0, srow, &sm.full[j]);
-        tma_load_2d(sg.S, &tm_S, 0, srow, &sm.full[j]);
+        mbar_expect_tx(&sm.sd_full[j], 2 * kTileNP);
+        tma_load_2d(sm.sd[j].dS, &tm_dS, 0, srow, &sm.sd_full[j]);
+        tma_load_2d(sm.sd[j].S, &tm_S, 0, srow, &sm.sd_full[j]);
       }
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer.  Per head:
+    //   set 1  dW~ = dy x^T (E waits for this part alone), [B; C] [dS | S]^T (ddv and Y),
+    //          dB^T += dS dvd^T and dC^T += S dch^T; then the dS / S slot is free
+    //   set 2  dv_or = W^T dy (after E), and at a chunk run's end the run's summed dCB terms; then the
+    //          x / dy slot is free
+    // Set 2 goes first whenever it can: it is short and E, O and the x / dy ring wait on it.
     if (lane == 0) {
-      int n1 = 0, n2 = 0, seg1 = -1, seg2 = -1;
-      HeadCursor c1, c2;  // the heads of sets 1 and 2 still to issue
+      int n1 = 0, n2 = 0, seg1 = -1;
+      HeadCursor c1, c2;
       c1.seek(prm, q0);
       c2.seek(prm, q0);
+      const uint32_t bc_b = smem_u32(sm.BC[0]), bc_c = smem_u32(sm.BC[1]);
       uint32_t idle = 0;
       while (n2 < nh) {
         bool moved = false;
-        if (n1 < nh && n1 <= n2 + 2) {
-          // set 1 of head n1: its stage, its TMEM buffer (read out by O and BK two heads ago), the chunk's B, C
+        if (n2 < n1 && mbar_probe(&sm.e_done[n2 & 1], (n2 >> 1) & 1)) {
+          const int j = n2 & 1;
+          tc_fence_after();
+#pragma unroll 1
+          for (int kk = 0; kk < kL; kk += 16)  // dv_or[s][p] = sum_t W[t][s] dy[t][p]  (rows s in lanes 0-63)
+            mma_bf16(TW(j), mdesc(sm.W[j], kL, kk), mdesc(sm.xy[n2 % 3].dy, kL, kk), idesc_bf16(128, 64, true, true),
+                     kk > 0);
+          mma_commit(&sm.s2_done[j]);
+          mma_commit(&sm.xy_empty[n2 % 3]);
+          if (c2.last(prm, q1)) {
+            // dB^T[n][s] += sum_t C[t][n] dCBsum[t][s],  dC^T[n][t] += sum_s B[s][n] dCBsum[t][s]
+#pragma unroll 1
+            for (int kk = 0; kk < kL; kk += 16) {
+              mma_bf16(ACC_B, sdesc_sw128(bc_c + kk * 128, 2 * kTileLP, 1024), mdesc(sm.dcbs, kL, kk),
+                       idesc_bf16(128, 64, true, true), true);
+              mma_bf16(ACC_C, sdesc_sw128(bc_b + kk * 128, 2 * kTileLP, 1024), kdesc(sm.dcbs, kL, kk),
+                       idesc_bf16(128, 64, true, false), true);
+            }
+            mma_commit(&sm.acc_full);
+            mma_commit(&sm.chunk_empty);
+          }
+          ++n2;
+          c2.next(prm);
+          moved = true;
+        }
+        if (!moved && n1 < nh && n1 <= n2 + 1) {
           const int j = n1 & 1;
           const bool first = c1.first(q0);
-          bool rdy = mbar_probe(&sm.full[j], (n1 >> 1) & 1);
-          if (rdy && n1 >= 2)
+          bool rdy = mbar_probe(&sm.xy_full[n1 % 3], (n1 / 3) & 1) && mbar_probe(&sm.sd_full[j], (n1 >> 1) & 1) &&
+                     mbar_probe(&sm.pre_done[j], (n1 >> 1) & 1);
+          if (rdy && n1 >= 2)  // TW and YD read out by O and BK two heads ago
             rdy = mbar_probe(&sm.o_done[j], ((n1 >> 1) - 1) & 1) && mbar_probe(&sm.bk_done[j], ((n1 >> 1) - 1) & 1);
-          if (rdy && first) rdy = mbar_probe(&sm.chunk_full, (seg1 + 1) & 1);
+          if (rdy && first) rdy = mbar_probe(&sm.chunk_full, (seg1 + 1) & 1) && (seg1 < 0 || mbar_probe(&sm.acc_free, seg1 & 1));
           if (rdy) {
             if (first) ++seg1;
             tc_fence_after();
-            const BwdcSmem::Stage& sg = sm.st[j];
+            const BwdcSmem::XY& gx = sm.xy[n1 % 3];
+            const BwdcSmem::SD& gs = sm.sd[j];
 #pragma unroll 1
             for (int kk = 0; kk < kP; kk += 16)  // dW~[t][s] = sum_p dy[t][p] x[s][p]
-              mma_bf16(TW(j), kdesc(sg.dy, kL, kk), kdesc(sg.x, kL, kk), idesc_bf16(64, 64, false, false), kk > 0);
+              mma_bf16(TW(j), kdesc(gx.dy, kL, kk), kdesc(gx.x, kL, kk), idesc_bf16(64, 64, false, false), kk > 0);
+            mma_commit(&sm.s1a_done[j]);
 #pragma unroll 1
             for (int kk = 0; kk < kN; kk += 16)  // [B; C][s or t][n] x [dS | S][n][p]: ddv and Y
-              mma_bf16(YD(j), kdesc(sm.BC[0], 2 * kL, kk), mdesc(sg.dS, kN, kk), idesc_bf16(128, 128, false, true),
+              mma_bf16(YD(j), kdesc(sm.BC[0], 2 * kL, kk), mdesc(gs.dS, kN, kk), idesc_bf16(128, 128, false, true),
                        kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < kP; kk += 16) {  // dB^T[n][s] += sum_p dS[n][p] dvd[s][p];  dC^T[n][t] += S dch^T
+              mma_bf16(ACC_B, kdesc(gs.dS, kN, kk), kdesc(sm.dvd[j], kL, kk), idesc_bf16(128, 64, false, false),
+                       !(first && kk == 0));
+              mma_bf16(ACC_C, kdesc(gs.S, kN, kk), kdesc(sm.dch[j], kL, kk), idesc_bf16(128, 64, false, false),
+                       !(first && kk == 0));
+            }
             mma_commit(&sm.s1_done[j]);
+            mma_commit(&sm.sd_empty[j]);
             ++n1;
             c1.next(prm);
             moved = true;
           }
         }
-        if (!moved && n2 < n1) {
-          // set 2 of head n2: its dch, dvd (P) and W (E) tiles; a new chunk run also needs the accumulators
-          // read out; the last head of a run adds the run's summed dCB terms
-          const int j = n2 & 1;
-          const bool first = c2.first(q0), last = c2.last(prm, q1);
-          bool rdy = mbar_probe(&sm.pre_done[j], (n2 >> 1) & 1) && mbar_probe(&sm.e_done[j], (n2 >> 1) & 1);
-          if (rdy && first && seg2 >= 0) rdy = mbar_probe(&sm.acc_free, seg2 & 1);
-          if (rdy) {
-            if (first) ++seg2;
-            tc_fence_after();
-            const BwdcSmem::Stage& sg = sm.st[j];
-#pragma unroll 1
-            for (int kk = 0; kk < kL; kk += 16)  // dv_or[s][p] = sum_t W[t][s] dy[t][p]  (rows s in lanes 0-63)
-              mma_bf16(TW(j), mdesc(sm.W[j], kL, kk), mdesc(sg.dy, kL, kk), idesc_bf16(128, 64, true, true), kk > 0);
-#pragma unroll 1
-            for (int kk = 0; kk < kP; kk += 16)  // dB^T[n][s] += sum_p dS[n][p] dvd[s][p]
-              mma_bf16(ACC_B, kdesc(sg.dS, kN, kk), kdesc(sm.dvd[j], kL, kk), idesc_bf16(128, 64, false, false),
-                       !(first && kk == 0));
-#pragma unroll 1
-            for (int kk = 0; kk < kP; kk += 16)  // dC^T[n][t] += sum_p S[n][p] dch[t][p]
-              mma_bf16(ACC_C, kdesc(sg.S, kN, kk), kdesc(sm.dch[j], kL, kk), idesc_bf16(128, 64, false, false),
-                       !(first && kk == 0));
-            mma_commit(&sm.s2_done[j]);
-            mma_commit(&sm.empty[j]);
-            if (last) {
-              // dB^T[n][s] += sum_t C[t][n] dCBsum[t][s],  dC^T[n][t] += sum_s B[s][n] dCBsum[t][s]
-              const uint32_t b0 = smem_u32(sm.BC[0]), c0 = smem_u32(sm.BC[1]);
-#pragma unroll 1
-              for (int kk = 0; kk < kL; kk += 16) {
-                mma_bf16(ACC_B, sdesc_sw128(c0 + kk * 128, 2 * kTileLP, 1024), mdesc(sm.dcbs, kL, kk),
-                         idesc_bf16(128, 64, true, true), true);
-                mma_bf16(ACC_C, sdesc_sw128(b0 + kk * 128, 2 * kTileLP, 1024), kdesc(sm.dcbs, kL, kk),
-                         idesc_bf16(128, 64, true, false), true);
-              }
-              mma_commit(&sm.acc_full);
-              mma_commit(&sm.chunk_empty);
-            }
-            ++n2;
-            c2.next(prm);
-            moved = true;
-          }
-        }
         if (moved) {
           idle = 0;
-        } else if (__nanosleep(32), ++idle > (1u << 25)) {
+        } else if (++idle > (1u << 26)) {
           atomicCAS(status, 0, 103);
           break;
         }
@@ -340,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = hr.h(prm);
       const float A_h = prm.A[h];
       const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
-      const float z0 = prm.dt_raw[rr * H + h], z1 = prm.dt_raw[(rr + 1) * H + h];
+      // streaming loads: these strided reads must not push CB (read by E, EB) out of L1
+      const float z0 = __ldcs(prm.dt_raw + rr * H + h), z1 = __ldcs(prm.dt_raw + (rr + 1) * H + h);
       const float d0 = softplus_f(z0), d1 = softplus_f(z1);
       const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
       float inc = a1;
@@ -398,15 +494,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float A_h = sm.Ah[k];
       // d cum per position: ORANGE row - column sums, BLUE, K3; K3's and K4's chunk-end terms at t = 63
       const float dec0 = sm.dec[k][t0], dec1 = sm.dec[k][t1];
-      const float k3_0 = sm.dde[j][t0] * dec0, k3_1 = sm.dde[j][t1] * dec1;
-      float dc0 = sm.drow[j][t0] - (sm.dcolp[j][0][t0] + sm.dcolp[j][1][t0] + sm.dcolp[j][2][t0] + sm.dcolp[j][3][t0]) +
+      const float k3_0 = (sm.dde[j][0][t0] + sm.dde[j][1][t0]) * dec0, k3_1 = (sm.dde[j][0][t1] + sm.dde[j][1][t1]) * dec1;
+      float dc0 = sm.drow[j][0][t0] + sm.drow[j][1][t0] - (sm.dcolp[j][0][t0] + sm.dcolp[j][1][t0] + sm.dcolp[j][2][t0] + sm.dcolp[j][3][t0]) +
                   sm.dcb[j][t0] - k3_0;
-      float dc1 = sm.drow[j][t1] - (sm.dcolp[j][0][t1] + sm.dcolp[j][1][t1] + sm.dcolp[j][2][t1] + sm.dcolp[j][3][t1]) +
+      float dc1 = sm.drow[j][0][t1] + sm.drow[j][1][t1] - (sm.dcolp[j][0][t1] + sm.dcolp[j][1][t1] + sm.dcolp[j][2][t1] + sm.dcolp[j][3][t1]) +
                   sm.dcb[j][t1] - k3_1;
       float k3sum = k3_0 + k3_1;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) k3sum += __shfl_xor_sync(0xffffffffu, k3sum, o);
-      const float k4 = sm.aend[k] * (sm.k4p[j][0] + sm.k4p[j][1] + sm.k4p[j][2] + sm.k4p[j][3]);
+      const float k4 = sm.aend[k] * (sm.k4p[j][0] + sm.k4p[j][1]);
       if (lane == 31) dc1 += k3sum + k4;
       // suffix sums (K1 backward): dda[t] = sum_{u >= t} d cum[u]
       const float pair = dc0 + dc1;
@@ -418,8 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float dda0 = suf, dda1 = suf - dc0;
       const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
-      prm.ddt_raw[rr * H + h] = (sm.dvx[j][t0] + A_h * dda0) * sigmoid_f(sm.z[k][t0]);
-      prm.ddt_raw[(rr + 1) * H + h] = (sm.dvx[j][t1] + A_h * dda1) * sigmoid_f(sm.z[k][t1]);
+      __stcs(prm.ddt_raw + rr * H + h, (sm.dvx[j][0][t0] + sm.dvx[j][1][t0] + A_h * dda0) * sigmoid_f(sm.z[k][t0]));
+      __stcs(prm.ddt_raw + (rr + 1) * H + h,
+             (sm.dvx[j][0][t1] + sm.dvx[j][1][t1] + A_h * dda1) * sigmoid_f(sm.z[k][t1]));
       float dAp = dda0 * sm.dtp[k][t0] + dda1 * sm.dtp[k][t1];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
@@ -431,16 +528,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= kWarpP0) {
-    // ------------------------------------------------------------ P: dch and dvd tiles
+    // ------------------------------------------------------------ P: dch and dvd tiles; the accumulator
+    //                                                              read-out at the end of a chunk run
     const int pt = tid - 32 * kWarpP0;  // 0..127
-    for (int q = 0; q < nh; ++q) {
+    const int q4 = warp & 3;
+    int seg = -1;
+    HeadCursor hr;
+    hr.seek(prm, q0);
+    for (int q = 0; q < nh; ++q, hr.next(prm)) {
       const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      if (hr.first(q0)) ++seg;
       bool ok = mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 110);
-      ok = ok && mbar_wait(&sm.full[j], ph, status, 111);
-      if (ok && q >= 2) ok = mbar_wait(&sm.s2_done[j], ph ^ 1, status, 112);  // set 2 of q-2 read dch, dvd
-      if (ok && q >= 2) ok = mbar_wait(&sm.o_done[j], ph ^ 1, status, 109);   // and O of q-2 sent dx from dch
+      ok = ok && mbar_wait(&sm.xy_full[q % 3], (q / 3) & 1, status, 111);
+      if (ok && q >= 2) ok = mbar_wait(&sm.s1_done[j], ph ^ 1, status, 112);  // set 1 of q-2 read dch, dvd
+      // and O of q-2 has sent dx out of dch (set 1 of this head waits for that O anyway)
+      if (ok && q >= 2) ok = mbar_wait(&sm.o_done[j], ph ^ 1, status, 109);
       if (named_bar_or(4, 128, !ok)) break;
-      const BwdcSmem::Stage& sg = sm.st[j];
+      const BwdcSmem::XY& sg = sm.xy[q % 3];
 #pragma unroll 1
       for (int i = 0; i < 4; ++i) {
         const int ch = pt + 128 * i;
@@ -464,234 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar(4, 128);
       if (pt == 0) {
         mbar_arrive(&sm.pre_done[j]);
-        mbar_arrive(&sm.empty[j]);
-        mbar_arrive(&sm.sc_free[k]);
-      }
-    }
-  } else if (warp >= kWarpK0) {
-    // ------------------------------------------------------------ BK: BLUE and K4
-    const int n = tid - 32 * kWarpK0;  // 0..127: S / dS row for K4
-    const int q4 = warp & 3;
-    for (int q = 0; q < nh; ++q) {
-      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
-      bool ok = mbar_wait(&sm.s1_done[j], ph, status, 113);
-      ok = ok && mbar_wait(&sm.full[j], ph, status, 114);
-      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 115);
-      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 116);
-      if (named_bar_or(3, 128, !ok)) break;
-      tc_fence_after();
-      const BwdcSmem::Stage& sg = sm.st[j];
-      {  // K4: <dS_{c+1}, S_c>
-        float part = 0.f;
-#pragma unroll 1
-        for (int jj = 0; jj < 8; ++jj) {
-          float sv[8], dv[8];
-          load_row8(sg.S, n, jj, sv);
-          load_row8(sg.dS, n, jj, dv);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) part += dv[u] * sv[u];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (lane == 0) sm.k4p[j][q4] = part;
-      }
-      if (q4 >= 2) {  // BLUE d cum: exp(cum_t) sum_p dy[t][p] Y[t][p]; Y row t sits in lane 64 + t
-        const int t = 32 * (q4 - 2) + lane;
-        float acc = 0.f;
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          float yv[32];
-          tmem_ld32(taddr(YD(j), 32 * q4, 64 + 32 * hf), yv);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            float gv[8];
-            load_row8(sg.dy, t, 4 * hf + jj, gv);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) acc += gv[u] * yv[8 * jj + u];
-          }
-        }
-        sm.dcb[j][t] = acc * sm.ecum[k][t];
-      }
-      tc_fence_before();
-      named_bar(3, 128);
-      if (n == 0) {
-        mbar_arrive(&sm.bk_done[j]);
-        mbar_arrive(&sm.empty[j]);
-        mbar_arrive(&sm.sc_free[k]);
-      }
-    }
-  } else if (warp >= kWarpE0) {
-    // ------------------------------------------------------------ E: W, the dCB sum and the ORANGE sums
-    const int q4 = warp & 3;
-    const int hl = lane >> 4, t = 16 * q4 + (lane & 15);
-    // this lane covers columns s = 16 jj + 8 hl + e (jj, e < 4, 8) of row t: every lane meets all four
-    // 16-column blocks, so the branch on the block below is uniform across the warp
-    int seg = -1;
-    HeadCursor hc;
-    hc.seek(prm, q0);
-    for (int q = 0; q < nh; ++q, hc.next(prm)) {
-      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
-      const bool first = hc.first(q0), last = hc.last(prm, q1);
-      if (first) ++seg;
-      const float* cbrow = prm.CB + ((size_t)hc.k * kL + t) * kL + 8 * hl;
-      bool ok = mbar_wait(&sm.s1_done[j], ph, status, 117);
-      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 118);
-      if (ok && q >= 2) ok = mbar_wait(&sm.s2_done[j], ph ^ 1, status, 119);   // W[j] read by set 2 of q-2
-      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 120);  // partial slot of q-2
-      // the bf16 dCB sum of the previous run must have been read by its MMAs
-      if (ok && last && seg >= 1) ok = mbar_wait(&sm.chunk_empty, (seg - 1) & 1, status, 126);
-      if (named_bar_or(2, 128, !ok)) break;
-      tc_fence_after();
-      const float ct = sm.cum[k][t];
-      float rowsum = 0.f;
-#pragma unroll 1
-      for (int jj = 0; jj < 4; ++jj) {
-        const int s0 = 16 * jj + 8 * hl;
-        uint32_t r8[8];  // lane l: row t, columns s0 .. s0 + 7 (lanes 16-31 read their rows' upper 8)
-        tmem_ld_pair8(taddr(TW(j), 32 * q4, 16 * jj), r8);
-        const float4 ca = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj));
-        const float4 cb4 = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj + 4));
-        const float cb[8] = {ca.x, ca.y, ca.z, ca.w, cb4.x, cb4.y, cb4.z, cb4.w};
-        tmem_wait_ld();
-        float w[8], dcb[8];
-        if (jj < q4) {  // block before the row's block: exp(cum_t - cum_s) = E_t[jj] G_s
-          const float f = sm.E[k][t][jj];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            w[e] = cb[e] * (f * sm.G[k][s0 + e]);
-            dcb[e] = __uint_as_float(r8[e]) * (f * sm.Gd[k][s0 + e]);
-          }
-        } else if (jj == q4) {  // the diagonal block, masked before the exponential
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = s0 + e;
-            const float ex = (s <= t) ? expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
-            w[e] = cb[e] * ex;
-            dcb[e] = __uint_as_float(r8[e]) * sm.dtp[k][s] * ex;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            w[e] = 0.f;
-            dcb[e] = 0.f;
-          }
-        }
-        store_row_bf16(sm.W[j], t, hl + 2 * jj, w, 1);
-        // the run's dCB sum, fp32; its last head also writes the bf16 copy for the MMA
-        float4* acc = reinterpret_cast<float4*>(&sm.dcbacc[t][s0]);
-        float4 lo = make_float4(dcb[0], dcb[1], dcb[2], dcb[3]), hi = make_float4(dcb[4], dcb[5], dcb[6], dcb[7]);
-        if (!first) {
-          const float4 a0 = acc[0], a1 = acc[1];
-          lo = make_float4(lo.x + a0.x, lo.y + a0.y, lo.z + a0.z, lo.w + a0.w);
-          hi = make_float4(hi.x + a1.x, hi.y + a1.y, hi.z + a1.z, hi.w + a1.w);
-        }
-        if (last) {
-          const float sum8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          store_row_bf16(sm.dcbs, t, hl + 2 * jj, sum8, 1);
-        } else {
-          acc[0] = lo;
-          acc[1] = hi;
-        }
-        float dd[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          dd[e] = dcb[e] * cb[e];  // d_diff = dW o decay o dt' o CB
-          rowsum += dd[e];
-        }
-        // column sums of these 8 columns over the 16 rows of this half: transposing butterfly
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const bool up = lane & 8;
-          const float send = up ? dd[kk] : dd[kk + 4], keep = up ? dd[kk + 4] : dd[kk];
-          dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const bool up = lane & 4;
-          const float send = up ? dd[kk] : dd[kk + 2], keep = up ? dd[kk + 2] : dd[kk];
-          dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        {
-          const bool up = lane & 2;
-          const float send = up ? dd[0] : dd[1], keep = up ? dd[1] : dd[0];
-          dd[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-        dd[0] += __shfl_xor_sync(0xffffffffu, dd[0], 1);
-        // lanes l and l ^ 1 now both hold column s0 + 4 b3 + 2 b2 + b1 (b_i: bits of the lane)
-        if (!(lane & 1)) sm.dcolp[j][q4][s0 + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1)] = dd[0];
-      }
-      rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
-      if (lane < 16) sm.drow[j][t] = rowsum;
-      tc_fence_before();
-      fence_proxy_async();
-      named_bar(2, 128);
-      if (tid == 32 * kWarpE0) {
-        mbar_arrive(&sm.e_done[j]);
-        mbar_arrive(&sm.sc_free[k]);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ O warps 0-3
-    const int ot = tid;  // 0..127
-    const int q4 = warp;
-    int seg = -1;
-    HeadCursor hr;
-    hr.seek(prm, q0);
-    for (int q = 0; q < nh; ++q, hr.next(prm)) {
-      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
-      if (hr.first(q0)) ++seg;
-      bool ok = mbar_wait(&sm.s2_done[j], ph, status, 121);
-      ok = ok && mbar_wait(&sm.full[j], ph, status, 122);
-      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 123);
-      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 124);
-      if (named_bar_or(1, 128, !ok)) break;
-      tc_fence_after();
-      const BwdcSmem::Stage& sg = sm.st[j];
-      if (q4 < 2) {  // dv = dv_or + exp(cum_end - cum_s) ddv; rows s = lanes 0-63 of TW and YD
-        const int s = 32 * q4 + lane;
-        const float e = sm.dec[k][s], d = sm.dtp[k][s];
-        float sx = 0.f, sd = 0.f;
-#pragma unroll 1
-        for (int qq = 0; qq < 4; ++qq) {  // 16 columns at a time
-          uint32_t ro[16], rd[16];
-          tmem_ld16_nowait(taddr(TW(j), 32 * q4, 16 * qq), ro);
-          tmem_ld16_nowait(taddr(YD(j), 32 * q4, 16 * qq), rd);
-          tmem_wait_ld();
-          float dxv[16];
-#pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            float xv[8];
-            load_row8(sg.x, s, 2 * qq + jj, xv);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int p = 8 * jj + u;
-              const float ddv = __uint_as_float(rd[p]);
-              const float dv = __uint_as_float(ro[p]) + e * ddv;
-              sx += dv * xv[u];
-              sd += ddv * xv[u];
-              dxv[p] = d * dv;
-            }
-          }
-          store_row_bf16(sm.dch[j], s, 2 * qq, dxv, 2);  // dch[j] is free once set 2 has run
-        }
-        sm.dvx[j][s] = sx;
-        sm.dde[j][s] = sd * d;  // sum_p ddv[s][p] v[s][p]
-      }
-      tc_fence_before();
-      fence_proxy_async();
-      named_bar(1, 128);
-      if (ot == 0) {
-        tma_store_2d(&tm_dx, sm.dch[j], hr.h(prm) * kP, hr.b * T + hr.c * kL);
-        tma_store_commit();
-        tma_store_wait_read0();  // P may refill dch[j] once o_done says so
-        mbar_arrive(&sm.o_done[j]);
-        mbar_arrive(&sm.empty[j]);
+        mbar_arrive(&sm.xy_empty[q % 3]);
         mbar_arrive(&sm.sc_free[k]);
       }
       if (hr.last(prm, q1)) {
         // the chunk run ends: dB^T and dC^T (lane n, column s or t) to this CTA's partial slot of chunk k
         ok = mbar_wait(&sm.acc_full, seg & 1, status, 125);
-        if (named_bar_or(1, 128, !ok)) break;
+        if (named_bar_or(4, 128, !ok)) break;
         tc_fence_after();
         const long long slot =
             (long long)hr.k * prm.nseg + ((long long)blockIdx.x - cta_of((long long)hr.k * prm.hpg, total, gridDim.x));
@@ -706,16 +589,192 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            pb[(32 * hf + e) * kN + n] = __uint_as_float(vb[e]);
-            pc[(32 * hf + e) * kN + n] = __uint_as_float(vc[e]);
+            __stcs(pb + (32 * hf + e) * kN + n, __uint_as_float(vb[e]));
+            __stcs(pc + (32 * hf + e) * kN + n, __uint_as_float(vc[e]));
           }
         }
         tc_fence_before();
-        named_bar(1, 128);
-        if (ot == 0) mbar_arrive(&sm.acc_free);
+        named_bar(4, 128);
+        if (pt == 0) mbar_arrive(&sm.acc_free);
       }
     }
-    if (ot == 0) tma_store_wait0();
+  } else if (warp >= kWarpEB0 || (warp >= kWarpE0 && warp < kWarpE0 + 4)) {
+    // ------------------------------------------------------------ E (warps 4-7): column blocks 0-1;
+    //   EB (warps 10-11): column blocks 2-3 of the lower 32 rows.  W, the dCB sum and the ORANGE sums.
+    const bool eb = warp >= kWarpEB0;
+    const int q4 = warp & 3;
+    const int bar = eb ? 5 : 2, nthr = eb ? 64 : 128, part = eb ? 1 : 0;
+    const int t = 16 * q4 + (lane & 15), s8 = 8 * (lane >> 4);
+    int seg = -1;
+    float cbv[16];   // CB[t][16 jj + s8 .. + 7] of this role's two blocks, loaded once per chunk run
+    float dacc[16];  // the run's dCB sum over the same elements
+    HeadCursor hc;
+    hc.seek(prm, q0);
+    for (int q = 0; q < nh; ++q, hc.next(prm)) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      const bool first = hc.first(q0), last = hc.last(prm, q1);
+      if (first) {
+        ++seg;
+        const float* cbrow = prm.CB + ((size_t)hc.k * kL + t) * kL + s8;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int jj = 2 * part + b;
+          const float4 u = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj));
+          const float4 v = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj + 4));
+          cbv[8 * b + 0] = u.x;
+          cbv[8 * b + 1] = u.y;
+          cbv[8 * b + 2] = u.z;
+          cbv[8 * b + 3] = u.w;
+          cbv[8 * b + 4] = v.x;
+          cbv[8 * b + 5] = v.y;
+          cbv[8 * b + 6] = v.z;
+          cbv[8 * b + 7] = v.w;
+        }
+      }
+      bool ok = mbar_wait(&sm.s1a_done[j], ph, status, 117);
+      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 118);
+      if (ok && q >= 2) ok = mbar_wait(&sm.s2_done[j], ph ^ 1, status, 119);   // W[j] read by set 2 of q-2
+      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 120);  // partial slot of q-2
+      // the bf16 dCB sum of the previous run must have been read by its MMAs
+      if (ok && last && seg >= 1) ok = mbar_wait(&sm.chunk_empty, (seg - 1) & 1, status, 126);
+      if (named_bar_or(bar, nthr, !ok)) break;
+      tc_fence_after();
+      const float rs = e_blocks(sm, TW(j), cbv, dacc, j, k, q4, 2 * part, first, last);
+      if (lane < 16) sm.drow[j][part][16 * q4 + lane] = rs;
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(bar, nthr);
+      if (lane == 0 && (warp == kWarpE0 || warp == kWarpEB0)) {
+        mbar_arrive(&sm.e_done[j]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+    }
+  } else if (warp >= 2 && warp < 4) {
+    // ------------------------------------------------------------ BK (warps 2-3): BLUE and K4
+    const int i = tid - 64;  // 0..63: Y row t (lane 64 + t), and S / dS rows i, i + 64
+    for (int q = 0; q < nh; ++q) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      bool ok = mbar_wait(&sm.s1_done[j], ph, status, 113);
+      ok = ok && mbar_wait(&sm.sd_full[j], ph, status, 114);
+      ok = ok && mbar_wait(&sm.xy_full[q % 3], (q / 3) & 1, status, 98);
+      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 115);
+      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 116);
+      if (named_bar_or(3, 64, !ok)) break;
+      tc_fence_after();
+      const BwdcSmem::SD& sg = sm.sd[j];
+      const BwdcSmem::XY& sx = sm.xy[q % 3];
+      {  // K4: <dS_{c+1}, S_c>
+        float part = 0.f;
+#pragma unroll 1
+        for (int jj = 0; jj < 16; ++jj) {
+          const int r = i + 64 * (jj >> 3);
+          float sv[8], dv[8];
+          load_row8(sg.S, r, jj & 7, sv);
+          load_row8(sg.dS, r, jj & 7, dv);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) part += dv[u] * sv[u];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) sm.k4p[j][warp - 2] = part;
+      }
+      {  // BLUE d cum: exp(cum_t) sum_p dy[t][p] Y[t][p]
+        float acc = 0.f;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          float yv[32];
+          tmem_ld32(taddr(YD(j), 32 * warp, 64 + 32 * hf), yv);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float gv[8];
+            load_row8(sx.dy, i, 4 * hf + jj, gv);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc += gv[u] * yv[8 * jj + u];
+          }
+        }
+        sm.dcb[j][i] = acc * sm.ecum[k][i];
+      }
+      tc_fence_before();
+      named_bar(3, 64);
+      if (i == 0) {
+        mbar_arrive(&sm.bk_done[j]);
+        mbar_arrive(&sm.sd_empty[j]);
+        mbar_arrive(&sm.xy_empty[q % 3]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ O (warps 0, 1, 8, 9): dv -> dx.  Rows s of
+    //   dv_or (TW) and ddv (YD) sit in lanes 0-63; warps 0-1 take columns 0-31, warps 8-9 columns 32-63.
+    const int ch = warp >= 8 ? 1 : 0;
+    const int s = 32 * (warp & 3) + lane;
+    const bool lead = warp == 0 && lane == 0;
+    HeadCursor hr;
+    hr.seek(prm, q0);
+    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+      const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
+      // x[s][32 ch .. 32 ch + 31] of this head, from L2 (the TMA brought it in), fetched before the waits
+      uint4 xr[4];
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            prm.x + ((size_t)hr.b * T + hr.c * kL + s) * ((size_t)H * kP) + (size_t)hr.h(prm) * kP + 32 * ch);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) xr[u] = __ldg(src + u);
+      }
+      bool ok = mbar_wait(&sm.s2_done[j], ph, status, 121);
+      ok = ok && mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 123);
+      if (ok && q >= 2) ok = mbar_wait(&sm.fin_done[j], ph ^ 1, status, 124);
+      if (named_bar_or(1, 128, !ok)) break;
+      tc_fence_after();
+      const float e = sm.dec[k][s], d = sm.dtp[k][s];
+      float sx = 0.f, sd = 0.f;
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {  // 16 columns at a time
+        const int c0 = 32 * ch + 16 * qq;
+        uint32_t ro[16], rd[16];
+        tmem_ld16_nowait(taddr(TW(j), 32 * (warp & 3), c0), ro);
+        tmem_ld16_nowait(taddr(YD(j), 32 * (warp & 3), c0), rd);
+        tmem_wait_ld();
+        float dxv[16];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          float xv[8];
+          {
+            const uint4 w4 = xr[2 * qq + jj];
+            const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float2 f = unpack_bf16(w[e2]);
+              xv[2 * e2] = f.x;
+              xv[2 * e2 + 1] = f.y;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int p = 8 * jj + u;
+            const float ddv = __uint_as_float(rd[p]);
+            const float dv = __uint_as_float(ro[p]) + e * ddv;
+            sx += dv * xv[u];
+            sd += ddv * xv[u];
+            dxv[p] = d * dv;
+          }
+        }
+        store_row_bf16(sm.dch[j], s, c0 / 8, dxv, 2);  // dch[j] is free once set 2 has run
+      }
+      sm.dvx[j][ch][s] = sx;
+      sm.dde[j][ch][s] = sd * d;  // sum_p ddv[s][p] v[s][p], this column half
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(1, 128);
+      if (lead) {
+        tma_store_2d(&tm_dx, sm.dch[j], hr.h(prm) * kP, hr.b * T + hr.c * kL);
+        tma_store_commit();
+        tma_store_wait_read0();  // P may refill dch[j] once o_done says so
+        mbar_arrive(&sm.o_done[j]);
+        mbar_arrive(&sm.sc_free[k]);
+      }
+    }
+    if (lead) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -839,7 +898,8 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&tds, w.dstates, kP, srows, 64, kN);
   if (e != cudaSuccess) return e;
   // partial slots use the layout of the launched grid (nseg of the largest grid bounds it)
-  BwdcParams prm{a.dt_raw, a.A, w.CB, a.ddt_raw, w.dA_part, w.dB_part, w.dC_part, status,
+  BwdcParams prm{a.dt_raw, a.A, w.CB, static_cast<const __nv_bfloat16*>(a.x), a.ddt_raw, w.dA_part, w.dB_part,
+                 w.dC_part, status,
                  d.T,      d.H, d.G,  d.hpg,     d.nc,      lmax.nseg, (int)l.total};
   const int smem = (int)sizeof(BwdcSmem) + 1024;
   e = cudaFuncSetAttribute(k_tc_bwdc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
