@@ -89,6 +89,10 @@ def kernel_bytes(name, cfg):
     dtb = t["dt_raw"]
     m2 = cfg["variant"] == "mamba2"
     part = b * T * H * N * 4 if m2 else 0
+    G = cfg.get("ngroups", 1)
+    sbf = b * H * nc * P * N * 2                 # bf16 chunk states
+    cbb = b * nc * G * L * L * 4                 # fp32 C B^T per (chunk, group)
+    cpart = b * nc * G * L * N * 4               # fp32 dB (or dC) partial, one slot per chunk
     dvws = b * T * H * P * 4 if m2 else 0
     table = {
         "k_chunk_state": t["x"] + dtb + t["B"] + states + small,
@@ -100,9 +104,15 @@ def kernel_bytes(name, cfg):
                         + (2 * part if m2 else t["B"] + t["C"]) + small),
         "k_group_sum": part + t["B"],
         "k_dA_sum": small + t["A"],
-        # tensor-core kernels: the leaf inputs and outputs of the call they serve
-        "k_tc_fwd": t["x"] + dtb + t["A"] + t["B"] + t["C"] + t["s0"] + t["x"] + t["s0"],
-        "k_tc_bwd": 3 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 3 * t["s0"] + dtb,
+        "k_tc_dA_sum": small + t["A"],
+        # tensor-core kernels (bf16 tiles; chunk states S_c and dS_{c+1} kept as bf16 [N][P] tiles)
+        "k_cb": t["B"] + t["C"] + cbb,
+        "k_tc_fwd2": t["x"] + dtb + t["A"] + t["B"] + t["C"] + cbb + t["s0"] + t["x"] + t["s0"],
+        "k_tc_states": t["x"] + dtb + t["A"] + t["B"] + t["s0"] + sbf,
+        "k_tc_dstates": t["x"] + dtb + t["A"] + t["C"] + t["s0"] + sbf + t["s0"],
+        "k_tc_bwd_chunk": (2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + cbb + 2 * sbf      # dy, x, ..., S_c, dS
+                           + t["x"] + dtb + small + 2 * cpart),                              # dx, ddt_raw, dA, dB/dC parts
+        "k_tc_dbdc_sum": 2 * cpart + t["B"] + t["C"],
         "k_m1_forward": 2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 2 * t["s0"],
         "k_m1_backward": 2 * t["x"] + 2 * dtb + t["A"] + t["B"] + t["C"] + 3 * t["s0"] + t["x"]
                          + 2 * b * T * H * N * 4 + b * H * N * 4 + b * H * (T // L) * N * 4,

@@ -69,7 +69,7 @@ ssd_status make_dims(const ssd_problem* pr, Dims* d) {
 
 size_t ws_bytes(const Dims& d, bool backward) {
   if (d.variant == kMamba1) return backward ? m1_backward_ws(d) : m1_forward_ws(d);
-  if (!backward && tc_forward_supported(d)) return tc_fwd2_ws(d);
+  if (!backward && tc_forward_supported(d)) return tc_forward_ws(d);
   if (backward && tc_backward_supported(d)) return tc_backward_ws(d);
   return backward ? simt_backward_ws(d) : simt_forward_ws(d);
 }
@@ -201,7 +201,7 @@ ssd_status ssd_forward(const ssd_problem* prob, const void* x, const float* dt_r
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
   cudaError_t e = d.variant == kMamba1        ? m1_forward(d, a, ws, st)
-                  : tc_forward_supported(d) ? tc_forward2(d, a, ws, st)
+                  : tc_forward_supported(d) ? tc_forward(d, a, ws, st)
                                             : simt_forward(d, a, ws, st);
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

@@ -45,6 +45,7 @@
 #include "ssd_device.cuh"
 #include "ssd_internal.h"
 #include "tc_common.cuh"
+#include "tc_items.cuh"
 
 namespace ssd {
 namespace {
@@ -104,44 +105,6 @@ struct BwdcParams {
   int nseg;   // partial slots per chunk
   int total;  // number of (chunk, group, head) items: b * nc * G * hpg (< 2^31)
 };
-
-// Walks this CTA's items in order without divisions: head jh of group g of
-// chunk c of batch b, chunk id k = (b * nc + c) * G + g, item f = k * hpg + jh.
-struct HeadCursor {
-  int f, k, b, c, g, jh;
-  __device__ __forceinline__ void seek(const BwdcParams& p, int f0) {
-    f = f0;
-    k = f0 / p.hpg;
-    jh = f0 - k * p.hpg;
-    g = k % p.G;
-    const int bc = k / p.G;
-    c = bc % p.nc;
-    b = bc / p.nc;
-  }
-  __device__ __forceinline__ void next(const BwdcParams& p) {
-    ++f;
-    if (++jh == p.hpg) {
-      jh = 0;
-      ++k;
-      if (++g == p.G) {
-        g = 0;
-        if (++c == p.nc) {
-          c = 0;
-          ++b;
-        }
-      }
-    }
-  }
-  __device__ __forceinline__ int h(const BwdcParams& p) const { return g * p.hpg + jh; }
-  // first / last item of this CTA's run on chunk k
-  __device__ __forceinline__ bool first(int q0) const { return f == q0 || jh == 0; }
-  __device__ __forceinline__ bool last(const BwdcParams& p, int q1) const { return f == q1 - 1 || jh == p.hpg - 1; }
-};
-
-// CTA i owns items [i * total / grid, (i + 1) * total / grid); the CTA that owns item f:
-__host__ __device__ __forceinline__ long long cta_of(long long f, long long total, long long grid) {
-  return ((f + 1) * grid - 1) / total;
-}
 
 __device__ __forceinline__ void load_row8(const uint8_t* tile, int r, int j, float* out) {
   const uint4 raw = *reinterpret_cast<const uint4*>(tile + sw128_chunk(r, j));
@@ -246,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q1 = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
   const int nh = q1 - q0;
   int* status = prm.status;
+  const ItemGeom geo{prm.hpg, prm.G, nc};
 
   if (tid == 0) {
     for (int j = 0; j < 2; ++j) {
@@ -303,10 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_B);
       prefetch_tmap(&tm_C);
       int seg = -1;
-      HeadCursor hr, hp;  // this head, and the one two ahead for the L2 prefetch
-      hr.seek(prm, q0);
-      hp.seek(prm, q0 + 2);
-      for (int q = 0; q < nh; ++q, hr.next(prm), hp.next(prm)) {
+      ItemCursor hr, hp;  // this head, and the one two ahead for the L2 prefetch
+      hr.seek(geo, q0);
+      hp.seek(geo, q0 + 2);
+      for (int q = 0; q < nh; ++q, hr.next(geo), hp.next(geo)) {
         const int j = q & 1;
         const int row = hr.b * T + hr.c * kL;
         if (hr.first(q0)) {
@@ -320,19 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (q + 2 < nh) {  // warm L2 with the tiles of head q + 2 while the rings are still busy
           const int prow = hp.b * T + hp.c * kL;
-          const int psrow = (int)((((size_t)hp.b * H + hp.h(prm)) * nc + hp.c) * kN);
-          tma_prefetch_2d(&tm_x, hp.h(prm) * kP, prow);
-          tma_prefetch_2d(&tm_dy, hp.h(prm) * kP, prow);
+          const int psrow = (int)((((size_t)hp.b * H + hp.h(geo)) * nc + hp.c) * kN);
+          tma_prefetch_2d(&tm_x, hp.h(geo) * kP, prow);
+          tma_prefetch_2d(&tm_dy, hp.h(geo) * kP, prow);
           tma_prefetch_2d(&tm_S, 0, psrow);
           tma_prefetch_2d(&tm_dS, 0, psrow);
         }
         const int x3 = q % 3, xr = q / 3;
         if (q >= 3 && !mbar_wait(&sm.xy_empty[x3], (xr - 1) & 1, status, 102)) break;
         mbar_expect_tx(&sm.xy_full[x3], 2 * kTileLP);
-        tma_load_2d(sm.xy[x3].x, &tm_x, hr.h(prm) * kP, row, &sm.xy_full[x3]);
-        tma_load_2d(sm.xy[x3].dy, &tm_dy, hr.h(prm) * kP, row, &sm.xy_full[x3]);
+        tma_load_2d(sm.xy[x3].x, &tm_x, hr.h(geo) * kP, row, &sm.xy_full[x3]);
+        tma_load_2d(sm.xy[x3].dy, &tm_dy, hr.h(geo) * kP, row, &sm.xy_full[x3]);
         if (q >= 2 && !mbar_wait(&sm.sd_empty[j], ((q >> 1) - 1) & 1, status, 99)) break;
-        const int srow = (int)((((size_t)hr.b * H + hr.h(prm)) * nc + hr.c) * kN);
+        const int srow = (int)((((size_t)hr.b * H + hr.h(geo)) * nc + hr.c) * kN);
         mbar_expect_tx(&sm.sd_full[j], 2 * kTileNP);
         tma_load_2d(sm.sd[j].dS, &tm_dS, 0, srow, &sm.sd_full[j]);
         tma_load_2d(sm.sd[j].S, &tm_S, 0, srow, &sm.sd_full[j]);
@@ -347,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Set 2 goes first whenever it can: it is short and E, O and the x / dy ring wait on it.
     if (lane == 0) {
       int n1 = 0, n2 = 0, seg1 = -1;
-      HeadCursor c1, c2;
-      c1.seek(prm, q0);
-      c2.seek(prm, q0);
+      ItemCursor c1, c2;
+      c1.seek(geo, q0);
+      c2.seek(geo, q0);
       const uint32_t bc_b = smem_u32(sm.BC[0]), bc_c = smem_u32(sm.BC[1]);
       uint32_t idle = 0;
       while (n2 < nh) {
@@ -363,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kk > 0);
           mma_commit(&sm.s2_done[j]);
           mma_commit(&sm.xy_empty[n2 % 3]);
-          if (c2.last(prm, q1)) {
+          if (c2.last(geo, q1)) {
             // dB^T[n][s] += sum_t C[t][n] dCBsum[t][s],  dC^T[n][t] += sum_s B[s][n] dCBsum[t][s]
 #pragma unroll 1
             for (int kk = 0; kk < kL; kk += 16) {
@@ -376,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&sm.chunk_empty);
           }
           ++n2;
-          c2.next(prm);
+          c2.next(geo);
           moved = true;
         }
         if (!moved && n1 < nh && n1 <= n2 + 1) {
@@ -410,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&sm.s1_done[j]);
             mma_commit(&sm.sd_empty[j]);
             ++n1;
-            c1.next(prm);
+            c1.next(geo);
             moved = true;
           }
         }
@@ -427,12 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpScal) {
     // ------------------------------------------------------------ SC: K1 scalars, up to four heads ahead
     const int t0 = 2 * lane, t1 = t0 + 1;
-    HeadCursor hr;
-    hr.seek(prm, q0);
-    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+    ItemCursor hr;
+    hr.seek(geo, q0);
+    for (int q = 0; q < nh; ++q, hr.next(geo)) {
       const int k = q & 3;
       if (q >= 4 && !mbar_wait(&sm.sc_free[k], ((q >> 2) - 1) & 1, status, 105)) break;
-      const int h = hr.h(prm);
+      const int h = hr.h(geo);
       const float A_h = prm.A[h];
       const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
       // streaming loads: these strided reads must not push CB (read by E, EB) out of L1
@@ -482,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpAsm) {
     // ------------------------------------------------------------ AS: d cum assembly per head
     const int t0 = 2 * lane, t1 = t0 + 1;
-    HeadCursor hr;
-    hr.seek(prm, q0);
-    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+    ItemCursor hr;
+    hr.seek(geo, q0);
+    for (int q = 0; q < nh; ++q, hr.next(geo)) {
       const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
-      const int h = hr.h(prm);
+      const int h = hr.h(geo);
       bool ok = mbar_wait(&sm.e_done[j], ph, status, 106);
       ok = ok && mbar_wait(&sm.bk_done[j], ph, status, 107);
       ok = ok && mbar_wait(&sm.o_done[j], ph, status, 108);
@@ -533,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pt = tid - 32 * kWarpP0;  // 0..127
     const int q4 = warp & 3;
     int seg = -1;
-    HeadCursor hr;
-    hr.seek(prm, q0);
-    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+    ItemCursor hr;
+    hr.seek(geo, q0);
+    for (int q = 0; q < nh; ++q, hr.next(geo)) {
       const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
       if (hr.first(q0)) ++seg;
       bool ok = mbar_wait(&sm.sc_ready[k], (q >> 2) & 1, status, 110);
@@ -571,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sm.xy_empty[q % 3]);
         mbar_arrive(&sm.sc_free[k]);
       }
-      if (hr.last(prm, q1)) {
+      if (hr.last(geo, q1)) {
         // the chunk run ends: dB^T and dC^T (lane n, column s or t) to this CTA's partial slot of chunk k
         ok = mbar_wait(&sm.acc_full, seg & 1, status, 125);
         if (named_bar_or(4, 128, !ok)) break;
@@ -608,11 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int seg = -1;
     float cbv[16];   // CB[t][16 jj + s8 .. + 7] of this role's two blocks, loaded once per chunk run
     float dacc[16];  // the run's dCB sum over the same elements
-    HeadCursor hc;
-    hc.seek(prm, q0);
-    for (int q = 0; q < nh; ++q, hc.next(prm)) {
+    ItemCursor hc;
+    hc.seek(geo, q0);
+    for (int q = 0; q < nh; ++q, hc.next(geo)) {
       const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
-      const bool first = hc.first(q0), last = hc.last(prm, q1);
+      const bool first = hc.first(q0), last = hc.last(geo, q1);
       if (first) {
         ++seg;
         const float* cbrow = prm.CB + ((size_t)hc.k * kL + t) * kL + s8;
@@ -709,15 +673,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ch = warp >= 8 ? 1 : 0;
     const int s = 32 * (warp & 3) + lane;
     const bool lead = warp == 0 && lane == 0;
-    HeadCursor hr;
-    hr.seek(prm, q0);
-    for (int q = 0; q < nh; ++q, hr.next(prm)) {
+    ItemCursor hr;
+    hr.seek(geo, q0);
+    for (int q = 0; q < nh; ++q, hr.next(geo)) {
       const int j = q & 1, ph = (q >> 1) & 1, k = q & 3;
       // x[s][32 ch .. 32 ch + 31] of this head, from L2 (the TMA brought it in), fetched before the waits
       uint4 xr[4];
       {
         const uint4* src = reinterpret_cast<const uint4*>(
-            prm.x + ((size_t)hr.b * T + hr.c * kL + s) * ((size_t)H * kP) + (size_t)hr.h(prm) * kP + 32 * ch);
+            prm.x + ((size_t)hr.b * T + hr.c * kL + s) * ((size_t)H * kP) + (size_t)hr.h(geo) * kP + 32 * ch);
 #pragma unroll
         for (int u = 0; u < 4; ++u) xr[u] = __ldg(src + u);
       }
@@ -767,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async();
       named_bar(1, 128);
       if (lead) {
-        tma_store_2d(&tm_dx, sm.dch[j], hr.h(prm) * kP, hr.b * T + hr.c * kL);
+        tma_store_2d(&tm_dx, sm.dch[j], hr.h(geo) * kP, hr.b * T + hr.c * kL);
         tma_store_commit();
         tma_store_wait_read0();  // P may refill dch[j] once o_done says so
         mbar_arrive(&sm.o_done[j]);

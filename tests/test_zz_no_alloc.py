@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 CASES = {
     # CUDA-core path: its scratch holds the chunk states
     "mamba2_tiny_fp32": CONFIGS["mamba2_tiny_fp32"],
-    # tensor-core path: its scratch is the status word only
+    # tensor-core path: its scratch holds the bf16 chunk states and C B^T
     "mamba2_bf16_tc": scaled(CONFIGS["mamba2_130m_bf16"], batch=2, seqlen=256, nheads=4),
     # MIMO on CUDA cores: chunk states of 3 heads in the scratch
     "mimo_bf16": scaled(CONFIGS["mimo_r4_bf16"], batch=1, seqlen=256, nheads=3, ngroups=3),
