@@ -109,6 +109,7 @@ def kernel_bytes(name, cfg):
         "k_cb": t["B"] + t["C"] + cbb,
         "k_tc_fwd2": t["x"] + dtb + t["A"] + t["B"] + t["C"] + cbb + t["s0"] + t["x"] + t["s0"],
         "k_tc_states": t["x"] + dtb + t["A"] + t["B"] + t["s0"] + sbf,
+        "k_tc_fwd_chunk": t["x"] + dtb + t["A"] + t["C"] + cbb + sbf + t["x"],
         "k_tc_dstates": t["x"] + dtb + t["A"] + t["C"] + t["s0"] + sbf + t["s0"],
         "k_tc_bwd_chunk": (2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + cbb + 2 * sbf      # dy, x, ..., S_c, dS
                            + t["x"] + dtb + small + 2 * cpart),                              # dx, ddt_raw, dA, dB/dC parts
@@ -385,10 +386,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (small cases for ncu captures; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = CONFIGS[args.workload]
+    if args.batch is not None:
+        cfg = scaled(cfg, batch=args.batch)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
