@@ -28,6 +28,10 @@ SMALL = {
     "m2_bf16_tiles": scaled(M2_BF16, batch=2, seqlen=256, nheads=4, ngroups=2),
     "m2_bf16_ragged": scaled(M2_BF16, batch=1, seqlen=192, nheads=3, headdim=24, dstate=40, ngroups=1),
     "m2_bf16_single_chunk": scaled(M2_BF16, batch=1, seqlen=64, nheads=2),
+    # tensor-core kernels' item ranges: one head per group (every head is a run of its own), and more
+    # (chunk, head) items than SMs with five heads per group (short runs, chunks split over CTAs)
+    "m2_bf16_head_per_group": scaled(M2_BF16, batch=2, seqlen=256, nheads=4, ngroups=4),
+    "m2_bf16_split_runs": scaled(M2_BF16, batch=4, seqlen=512, nheads=10, ngroups=2),
     "m1_small": scaled(M1, batch=2, seqlen=256, nheads=40),
     "m1_ragged": scaled(M1, batch=1, seqlen=96, nheads=37, dstate=5, chunk=32),
     "mimo_bf16_tiles": scaled(MIMO, batch=1, seqlen=256, nheads=3, ngroups=3),
