@@ -80,7 +80,7 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_
 // Tensor-core path (Mamba-2, bf16 io, L = 64, P = 64, N = 128).
 bool tc_forward_supported(const Dims& d);
 // K2 pre-pass (ssd_tc_prep.cu): CB[b, c, g] = C B^T of every chunk and group, fp32.
-cudaError_t tc_cb_prepass(const Dims& d, const void* B, const void* C, float* CB, cudaStream_t st);
+cudaError_t tc_cb_prepass(const Dims& d, const void* B, const void* C, float* CB, int* status, cudaStream_t st);
 // Chunk-parallel forward (ssd_tc_fwdc.cu): the state scan, then every (chunk, head) output at once.
 size_t tc_forward_ws(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);

@@ -154,7 +154,7 @@ __device__ __forceinline__ float e_blocks(BwdcSmem& sm, uint32_t tw, const float
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int s = s0 + e;
-        const float ex = (s <= t) ? expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
+        const float ex = (s <= t) ? __expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
         w[e] = cb[e] * ex;
         dcb[e] = __uint_as_float(r8[e]) * sm.dtp[k][s] * ex;
       }
@@ -380,9 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (moved) {
           idle = 0;
-        } else if (++idle > (1u << 26)) {
-          atomicCAS(status, 0, 103);
-          break;
+        } else {
+          // nothing ready: back off briefly instead of spinning (the spin took issue slots from
+          // the warps this one waits for); about a second in all before giving up
+          if (++idle > (1u << 25)) {
+            atomicCAS(status, 0, 103);
+            break;
+          }
+          __nanosleep(32);
         }
       }
       mma_commit(&sm.drain);  // nothing may still be writing TMEM when it is freed
@@ -749,37 +754,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // dB / dC of chunk k = sum of its partial slots, in CTA order.
-__global__ void k_bwdc_dbdc_sum(const float* dB_part, const float* dC_part, __nv_bfloat16* dB, __nv_bfloat16* dC,
-                                long long nchunks, int nseg, long long total, long long grid, int hpg, int T, int G,
-                                int nc) {
-  const long long count = nchunks * kL * kN;
-  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < count;
-       e += (long long)gridDim.x * blockDim.x) {
-    const long long k = e / (kL * kN);
-    const int tn = (int)(e - k * kL * kN);
-    const long long first = cta_of(k * hpg, total, grid), last = cta_of((k + 1) * hpg - 1, total, grid);
-    float sb = 0.f, sc = 0.f;
-    for (long long s = 0; s <= last - first; ++s) {
-      sb += dB_part[(k * nseg + s) * kL * kN + tn];
-      sc += dC_part[(k * nseg + s) * kL * kN + tn];
+// The fixed-order sums after the chunk kernel, in one launch:
+//   blocks [0, 4 nchunks): a quarter of chunk k's dB, dC (2048 elements, 8 per
+//     thread as two float4), the chunk's partial slots added in slot order;
+//   the blocks after them: dA[h] = sum over (batch, chunk) of the per-head
+//     parts, one warp per head (lane-strided sums, then a fixed shuffle tree).
+__global__ void __launch_bounds__(256) k_bwdc_sums(const float* __restrict__ dB_part, const float* __restrict__ dC_part,
+                                                   __nv_bfloat16* dB, __nv_bfloat16* dC, const float* __restrict__ dA_part,
+                                                   float* dA, long long nchunks, int nseg, long long total, long long grid,
+                                                   int hpg, int T, int G, int nc, int b, int H) {
+  const long long nb = 4 * nchunks;
+  const int lane = threadIdx.x & 31;
+  if ((long long)blockIdx.x >= nb) {
+    const int h = (int)(((long long)blockIdx.x - nb) * 8) + (threadIdx.x >> 5);
+    if (h >= H) return;
+    const int n = b * nc;
+    float acc = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      const int bb = i / nc, c = i - bb * nc;
+      acc += dA_part[((size_t)bb * H + h) * nc + c];
     }
-    const int g = (int)(k % G);
-    const long long bc = k / G;
-    const int c = (int)(bc % nc), b = (int)(bc / nc);
-    const int t = tn / kN, n = tn % kN;
-    const size_t o = (((size_t)b * T + c * kL + t) * G + g) * kN + n;
-    dB[o] = __float2bfloat16_rn(sb);
-    dC[o] = __float2bfloat16_rn(sc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) dA[h] = acc;
+    return;
   }
-}
-
-__global__ void k_bwdc_dA_sum(const float* part, float* dA, int b, int H, int nc) {
-  const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  if (h >= H) return;
-  float acc = 0.f;
-  for (int bb = 0; bb < b; ++bb)
-    for (int c = 0; c < nc; ++c) acc += part[((size_t)bb * H + h) * nc + c];
-  dA[h] = acc;
+  const long long k = blockIdx.x >> 2;
+  const int ns = (int)(cta_of((k + 1) * hpg - 1, total, grid) - cta_of(k * hpg, total, grid)) + 1;
+  const int g = (int)(k % G);
+  const long long bc = k / G;
+  const int c = (int)(bc % nc), bb = (int)(bc / nc);
+  const float4* pb = reinterpret_cast<const float4*>(dB_part + (size_t)k * nseg * kL * kN);
+  const float4* pc = reinterpret_cast<const float4*>(dC_part + (size_t)k * nseg * kL * kN);
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int e4 = (int)(blockIdx.x & 3) * 512 + u * 256 + threadIdx.x;  // float4 index in the chunk's [L][N]
+    float4 sb = pb[e4], sc = pc[e4];
+    for (int s = 1; s < ns; ++s) {
+      const float4 vb = pb[(size_t)s * (kL * kN / 4) + e4], vc = pc[(size_t)s * (kL * kN / 4) + e4];
+      sb.x += vb.x, sb.y += vb.y, sb.z += vb.z, sb.w += vb.w;
+      sc.x += vc.x, sc.y += vc.y, sc.z += vc.z, sc.w += vc.w;
+    }
+    const int t = (4 * e4) / kN, n = (4 * e4) % kN;
+    const size_t o = (((size_t)bb * T + c * kL + t) * G + g) * kN + n;
+    *reinterpret_cast<uint2*>(dB + o) = make_uint2(pack_bf16(sb.x, sb.y), pack_bf16(sb.z, sb.w));
+    *reinterpret_cast<uint2*>(dC + o) = make_uint2(pack_bf16(sc.x, sc.y), pack_bf16(sc.z, sc.w));
+  }
 }
 
 struct BwdcLayout {
@@ -846,7 +866,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   Carver cv(ws);
   BwdcWs w = carve(d, lmax, cv);
   int* status = static_cast<int*>(ws);
-  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, st);
+  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, status, st);
   if (e == cudaSuccess) e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, nullptr, w.states, status, st);
   if (e == cudaSuccess) e = tc_scan(d, true, a.dy, a.C, a.dt_raw, a.A, a.ds_final, a.ds0, w.dstates, status, st);
   if (e != cudaSuccess) return e;
@@ -869,13 +889,12 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   e = cudaFuncSetAttribute(k_tc_bwdc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   SSD_LAUNCH("k_tc_bwd_chunk", st, k_tc_bwdc<<<l.grid, kThreads, smem, st>>>(tx, tdy, tdx, tb, tcm, ts, tds, prm));
-  const long long cnt = l.nchunks * kL * kN;
-  const int blocks = (int)((cnt + 255) / 256 < 4096 ? (cnt + 255) / 256 : 4096);
-  SSD_LAUNCH("k_tc_dbdc_sum", st,
-             k_bwdc_dbdc_sum<<<blocks, 256, 0, st>>>(w.dB_part, w.dC_part, static_cast<__nv_bfloat16*>(a.dB),
-                                                     static_cast<__nv_bfloat16*>(a.dC), l.nchunks, lmax.nseg, l.total,
-                                                     l.grid, d.hpg, d.T, d.G, d.nc));
-  SSD_LAUNCH("k_tc_dA_sum", st, k_bwdc_dA_sum<<<(d.H + 127) / 128, 128, 0, st>>>(w.dA_part, a.dA, d.b, d.H, d.nc));
+  const long long sum_blocks = 4 * l.nchunks + (d.H + 7) / 8;
+  if (sum_blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  SSD_LAUNCH("k_tc_bwd_sums", st,
+             k_bwdc_sums<<<(unsigned)sum_blocks, 256, 0, st>>>(
+                 w.dB_part, w.dC_part, static_cast<__nv_bfloat16*>(a.dB), static_cast<__nv_bfloat16*>(a.dC), w.dA_part,
+                 a.dA, l.nchunks, lmax.nseg, l.total, l.grid, d.hpg, d.T, d.G, d.nc, d.b, d.H));
   return cudaGetLastError();
 }
 

@@ -372,7 +372,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t s
   Carver cv(ws);
   FwdcWs w = carve(d, cv);
   int* status = static_cast<int*>(ws);
-  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, st);
+  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, status, st);
   if (e == cudaSuccess) e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, a.s_final, w.states, status, st);
   if (e != cudaSuccess) return e;
   const uint64_t rows = (uint64_t)d.b * d.T;

@@ -12,12 +12,15 @@
 //     dch[t][p] = exp(cum_t) dy[t][p];
 // it writes dS_{c+1} for every chunk c (bf16 tiles) and dS_0 = ds0.
 //
-// One CTA owns one (batch, head); three CTAs share an SM.  The fp32 state
-// lives in 64 TMEM columns (thread n of the state warps owns row n): per chunk
-// the state warps read it, send its bf16 copy out through TMA, scale it by
-// exp(cum_end) in place, and the MMA then accumulates the chunk's K^T U into
-// the same columns, so the recurrence costs one MMA group and one TMEM round
-// trip per chunk.
+// One CTA owns one (batch, head); three CTAs share an SM.  The fp32 state S
+// lives in 64 TMEM columns (thread n of the state warps owns row n) and the
+// chunk's contribution P = K^T U in 64 more: the MMA writes P for chunk c while
+// the state warps still finish chunk c - 1, and the state warps then form
+// S <- exp(cum_end) S + P a quarter of the row at a time; the bf16 copy of the
+// new state (the next chunk's input state) goes out through shared memory, one
+// TMA store of 32 rows per state warp.
+// The recurrence's critical path per chunk is one P read-out and a few FMAs;
+// the MMA is off it.
 //
 // Warp roles (288 threads): warps 0-3 state, warps 4-5 scale the U tile in
 // place (x -> dvd or dy -> dch), warp 6 K1 scalars (softplus, in-chunk cumsum,
@@ -38,16 +41,17 @@ constexpr int kWarpScale0 = 4, kWarpScal = 6, kWarpTma = 7, kWarpMma = 8;
 constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
 constexpr uint32_t kTileLN = kL * kN * 2;  // 16 KB
 constexpr uint32_t kTileNP = kN * kP * 2;  // 16 KB
-constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kTmemCols = 128;
+constexpr int kScal = 4;  // K1 scalars run up to four chunks ahead  // S in columns 0-63, P in 64-127
 
 struct alignas(1024) ScanSmem {
   uint8_t u[2][kTileLP];  // x or dy [t][p], scaled in place to dvd or dch
   uint8_t k[2][kTileLN];  // B or C [t][n], two 64-column atoms
-  uint8_t out[kTileNP];   // bf16 state tile [n][p] on its way out
-  float scale[2][kL];     // per-row factor of U: exp(cum_end - cum) dt' or exp(cum)
-  float aend[2];          // exp(cum_end)
-  uint64_t full[2], empty[2], sc_ready[2], sc_free[2], pre_done[2];
-  uint64_t d_ready, mma_done, drain;
+  uint8_t out[kTileNP];   // bf16 state tile [n][p] on its way out; state warp w owns rows 32 w .. 32 w + 31
+  float scale[kScal][kL];  // per-row factor of U: exp(cum_end - cum) dt' or exp(cum); ring of kScal chunks
+  float aend[kScal];       // exp(cum_end)
+  uint64_t full[2], empty[2], pre_done[2], sc_ready[kScal], sc_free[kScal];
+  uint64_t p_ready, p_free, drain;
   uint32_t tmem_slot;
 };
 
@@ -79,12 +83,14 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);  // MMA commit (it waited for the scale warps)
-      mbar_init(&sm.sc_ready[s], 1);
-      mbar_init(&sm.sc_free[s], 2);  // scale warps + state warps
       mbar_init(&sm.pre_done[s], 1);
     }
-    mbar_init(&sm.d_ready, 1);
-    mbar_init(&sm.mma_done, 1);
+    for (int s = 0; s < kScal; ++s) {
+      mbar_init(&sm.sc_ready[s], 1);
+      mbar_init(&sm.sc_free[s], 5);  // scale warps + the four state warps
+    }
+    mbar_init(&sm.p_ready, 1);
+    mbar_init(&sm.p_free, 4);  // the four state warps have read P
     mbar_init(&sm.drain, 1);
     mbar_init_fence();
   }
@@ -111,18 +117,19 @@ __global__ void __launch_bounds__(kThreads, 3)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      const uint32_t tP = tmem + 64u;
       bool ok = true;
       for (int r = 0; r < nc && ok; ++r) {
         const int s = r & 1;
         ok = mbar_wait(&sm.pre_done[s], (r >> 1) & 1, status, 82);
-        ok = ok && mbar_wait(&sm.d_ready, r & 1, status, 83);
+        ok = ok && (r == 0 || mbar_wait(&sm.p_free, (r - 1) & 1, status, 83));
         if (!ok) break;
         tc_fence_after();
-        // D[n][p] += sum_t K[t][n] U[t][p]: A = K^T (MN-major), B = U (MN-major)
+        // P[n][p] = sum_t K[t][n] U[t][p]: A = K^T (MN-major), B = U (MN-major)
 #pragma unroll
         for (int kk = 0; kk < kL; kk += 16)
-          mma_bf16(tmem, mdesc(sm.k[s], kL, kk), mdesc(sm.u[s], kL, kk), idesc_bf16(128, 64, true, true), true);
-        mma_commit(&sm.mma_done);
+          mma_bf16(tP, mdesc(sm.k[s], kL, kk), mdesc(sm.u[s], kL, kk), idesc_bf16(128, 64, true, true), kk > 0);
+        mma_commit(&sm.p_ready);
         mma_commit(&sm.empty[s]);
       }
       // nothing may still be writing TMEM when it is freed
@@ -130,14 +137,20 @@ __global__ void __launch_bounds__(kThreads, 3)
       mbar_wait(&sm.drain, 0, status, 84);
     }
   } else if (warp == kWarpScal) {
-    // ------------------------------------------------------------ K1 scalars
+    // ------------------------------------------------------------ K1 scalars.  The dt_raw reads (64
+    //   strided floats per chunk) are issued two chunks ahead of their use.
     const float A_h = prm.A[h];
     const int t0 = 2 * lane, t1 = t0 + 1;
-    for (int r = 0; r < nc; ++r) {
-      const int s = r & 1, c = chunk_of(r);
-      if (r >= 2 && !mbar_wait(&sm.sc_free[s], ((r >> 1) - 1) & 1, status, 85)) break;
-      const size_t rr = (size_t)row0 + c * kL + t0;
-      const float z0 = prm.dt_raw[rr * H + h], z1 = prm.dt_raw[(rr + 1) * H + h];
+    auto fetch = [&](int r, float& z0, float& z1) {
+      if (r < nc) {
+        const size_t rr = (size_t)row0 + chunk_of(r) * kL + t0;
+        z0 = prm.dt_raw[rr * H + h];
+        z1 = prm.dt_raw[(rr + 1) * H + h];
+      }
+    };
+    auto step = [&](int r, float z0, float z1) -> bool {
+      const int s = r % kScal;
+      if (r >= kScal && !mbar_wait(&sm.sc_free[s], (r / kScal - 1) & 1, status, 85)) return false;
       const float d0 = softplus_f(z0), d1 = softplus_f(z1);
       const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
       float inc = a1;
@@ -158,13 +171,26 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (lane == 0) sm.aend[s] = expf(cend);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sc_ready[s]);
+      return true;
+    };
+    float za0 = 0.f, za1 = 0.f, zb0 = 0.f, zb1 = 0.f;
+    fetch(0, za0, za1);
+    fetch(1, zb0, zb1);
+    for (int r = 0; r < nc; r += 2) {
+      if (!step(r, za0, za1)) break;
+      fetch(r + 2, za0, za1);
+      if (r + 1 < nc) {
+        if (!step(r + 1, zb0, zb1)) break;
+        fetch(r + 3, zb0, zb1);
+      }
     }
   } else if (warp >= kWarpScale0) {
     // ------------------------------------------------------------ scale warps: U *= scale (per row)
     const int pt = tid - 32 * kWarpScale0;  // 0..63
     for (int r = 0; r < nc; ++r) {
       const int s = r & 1;
-      bool ok = mbar_wait(&sm.sc_ready[s], (r >> 1) & 1, status, 86);
+      const int k = r % kScal;
+      bool ok = mbar_wait(&sm.sc_ready[k], (r / kScal) & 1, status, 86);
       ok = ok && mbar_wait(&sm.full[s], (r >> 1) & 1, status, 87);
       if (named_bar_or(2, 64, !ok)) break;
 #pragma unroll
@@ -172,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int q = pt + 64 * i, t = q >> 3, j = q & 7;
         uint4* p = reinterpret_cast<uint4*>(sm.u[s] + sw128_chunk(t, j));
         const uint4 w = *p;
-        const float f = sm.scale[s][t];
+        const float f = sm.scale[k][t];
         const float2 v0 = unpack_bf16(w.x), v1 = unpack_bf16(w.y), v2 = unpack_bf16(w.z), v3 = unpack_bf16(w.w);
         *p = make_uint4(pack_bf16(f * v0.x, f * v0.y), pack_bf16(f * v1.x, f * v1.y), pack_bf16(f * v2.x, f * v2.y),
                         pack_bf16(f * v3.x, f * v3.y));
@@ -181,63 +207,76 @@ __global__ void __launch_bounds__(kThreads, 3)
       named_bar(2, 64);
       if (pt == 0) {
         mbar_arrive(&sm.pre_done[s]);
-        mbar_arrive(&sm.sc_free[s]);
+        mbar_arrive(&sm.sc_free[k]);
       }
     }
   } else {
     // ------------------------------------------------------------ state warps 0-3 (thread n owns row n)
     const int n = tid;
-    const uint32_t trow = taddr(tmem, 32 * warp, 0);
+    const uint32_t srow = taddr(tmem, 32 * warp, 0), prow = taddr(tmem, 32 * warp, 64);
     const size_t fbase = unit * kP * kN;
-    bool alive = true;  // the same in every state thread (set after a vote)
-    for (int r = 0; r < nc; ++r) {
-      const int s = r & 1, c = chunk_of(r);
-      bool ok = r == 0 || mbar_wait(&sm.mma_done, (r - 1) & 1, status, 88);
-      ok = ok && mbar_wait(&sm.sc_ready[s], (r >> 1) & 1, status, 89);
-      if (n == 0 && r > 0) tma_store_wait_read0();  // the previous out tile has been read
-      if (named_bar_or(1, 128, !ok)) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      const float a = sm.aend[s];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v[32];
-        if (r == 0) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            v[e] = prm.init ? prm.init[fbase + (size_t)(32 * hf + e) * kN + n] : 0.f;
-        } else {
-          tmem_ld32(trow + 32 * hf, v);
-        }
-        store_row_bf16(sm.out, n, 4 * hf, v, 4);  // the state at the chunk boundary
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] *= a;
-        tmem_st32(trow + 32 * hf, v);
-      }
-      tmem_wait_st();
+    uint8_t* slice = sm.out + 4096 * warp;  // this warp's 32 rows of the out tile
+    // this warp's rows of the out tile to the input state of chunk c (rows of 64 bf16, [b,H,nc][N][P])
+    auto send = [&](int c) {
       fence_proxy_async();
-      tc_fence_before();
-      named_bar(1, 128);
-      if (n == 0) {
-        tma_store_2d(&tm_out, sm.out, 0, (int)((unit * nc + c) * kN));
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&tm_out, slice, 0, (int)((unit * nc + c) * kN) + 32 * warp);
         tma_store_commit();
-        mbar_arrive(&sm.d_ready);
-        mbar_arrive(&sm.sc_free[s]);
       }
+    };
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {  // S = init: into TMEM, and out as the first chunk's input state
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = prm.init ? prm.init[fbase + (size_t)(16 * q + e) * kN + n] : 0.f;
+      tmem_st16(srow + 16 * q, v);
+      store_row_bf16(sm.out, n, 2 * q, v, 2);
     }
-    if (alive && prm.fin && !named_bar_or(1, 128, !mbar_wait(&sm.mma_done, (nc - 1) & 1, status, 90))) {
+    send(chunk_of(0));
+    tmem_wait_st();
+    for (int r = 0; r < nc; ++r) {
+      const int s = r & 1;
+      const int k = r % kScal;
+      bool ok = mbar_wait(&sm.sc_ready[k], (r / kScal) & 1, status, 89);
+      ok = ok && mbar_wait(&sm.p_ready, r & 1, status, 88);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v[32];
-        tmem_ld32(trow + 32 * hf, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) prm.fin[fbase + (size_t)(32 * hf + e) * kN + n] = v[e];
+      const float a = sm.aend[k];
+      const bool more = r + 1 < nc;
+      if (more) {  // the previous store has read the slice
+        if (lane == 0) tma_store_wait_read0();
+        __syncwarp();
       }
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t sv[16], pv[16];
+        tmem_ld16_nowait(srow + 16 * q, sv);
+        tmem_ld16_nowait(prow + 16 * q, pv);
+        tmem_wait_ld();
+        if (q == 3) {  // P and exp(cum_end) fully read by this warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sm.p_free);
+            mbar_arrive(&sm.sc_free[k]);
+          }
+        }
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = fmaf(a, __uint_as_float(sv[e]), __uint_as_float(pv[e]));
+        tmem_st16(srow + 16 * q, v);
+        if (more) {
+          store_row_bf16(sm.out, n, 2 * q, v, 2);
+        } else if (prm.fin) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) prm.fin[fbase + (size_t)(16 * q + e) * kN + n] = v[e];
+        }
+      }
+      if (more) send(chunk_of(r + 1));
+      tmem_wait_st();
     }
-    if (n == 0) tma_store_wait0();
+    if (lane == 0) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -257,7 +296,7 @@ cudaError_t tc_scan(const Dims& d, bool reverse, const void* u, const void* k, c
   const uint64_t rows = (uint64_t)d.b * d.T;
   cudaError_t e = make_tmap_2d_bf16(&tu, u, (uint64_t)d.H * kP, rows, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d_bf16(&tk, k, d.N, d.G, rows, 64, 1, 64);
-  if (e == cudaSuccess) e = make_tmap_2d_bf16(&to, states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, kN);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&to, states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, 32);
   if (e != cudaSuccess) return e;
   ScanParams prm{dt_raw, A, init, fin, status, d.T, d.H, d.hpg, d.nc};
   const int smem = (int)sizeof(ScanSmem) + 1024;
