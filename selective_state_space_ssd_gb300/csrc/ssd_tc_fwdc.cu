@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = u.a.h(geo) + i;
         const float A_h = prm.A[h];
         const size_t rr = (size_t)u.a.b * T + u.a.c * kL + t0;
-        const float d0 = softplus_f(__ldcs(prm.dt_raw + rr * H + h)), d1 = softplus_f(__ldcs(prm.dt_raw + (rr + 1) * H + h));
+        const float d0 = softplus_fast(__ldcs(prm.dt_raw + rr * H + h)), d1 = softplus_fast(__ldcs(prm.dt_raw + (rr + 1) * H + h));
         const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
         float inc = a1;
 #pragma unroll
@@ -211,19 +211,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.cum[r][i][t1] = c1;
         sm.dtp[r][i][t0] = d0;
         sm.dtp[r][i][t1] = d1;
-        sm.ecum[r][i][t0] = expf(c0);
-        sm.ecum[r][i][t1] = expf(c1);
+        sm.ecum[r][i][t0] = __expf(c0);
+        sm.ecum[r][i][t1] = __expf(c1);
         const float e0 = __shfl_sync(0xffffffffu, c1, 7), e1 = __shfl_sync(0xffffffffu, c1, 15);
         const float e2 = __shfl_sync(0xffffffffu, c1, 23), e3 = __shfl_sync(0xffffffffu, c1, 31);
         const int blk = t0 >> 4;
         const float my_end = blk == 0 ? e0 : (blk == 1 ? e1 : (blk == 2 ? e2 : e3));
-        sm.Gd[r][i][t0] = expf(my_end - c0) * d0;  // decay to the end of the 16-block, times dt'
-        sm.Gd[r][i][t1] = expf(my_end - c1) * d1;
+        sm.Gd[r][i][t0] = __expf(my_end - c0) * d0;  // decay to the end of the 16-block, times dt'
+        sm.Gd[r][i][t1] = __expf(my_end - c1) * d1;
         const float ends[4] = {e0, e1, e2, e3};
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          sm.E[r][i][t0][jj] = (jj < blk) ? expf(c0 - ends[jj]) : 0.f;
-          sm.E[r][i][t1][jj] = (jj < blk) ? expf(c1 - ends[jj]) : 0.f;
+          sm.E[r][i][t0][jj] = (jj < blk) ? __expf(c0 - ends[jj]) : 0.f;
+          sm.E[r][i][t1][jj] = (jj < blk) ? __expf(c1 - ends[jj]) : 0.f;
         }
       }
       __syncwarp();
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int s = s0 + e;
-              w[e] = (s <= t) ? cbv[8 * jj + e] * expf(fminf(ct - sm.cum[r][i][s], 0.f)) * sm.dtp[r][i][s] : 0.f;
+              w[e] = (s <= t) ? cbv[8 * jj + e] * __expf(fminf(ct - sm.cum[r][i][s], 0.f)) * sm.dtp[r][i][s] : 0.f;
             }
           }
           store_row_bf16(sm.W[r][i], t, hl + 2 * jj, w, 1);

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     auto step = [&](int r, float z0, float z1) -> bool {
       const int s = r % kScal;
       if (r >= kScal && !mbar_wait(&sm.sc_free[s], (r / kScal - 1) & 1, status, 85)) return false;
-      const float d0 = softplus_f(z0), d1 = softplus_f(z1);
+      const float d0 = softplus_fast(z0), d1 = softplus_fast(z1);
       const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
       float inc = a1;
 #pragma unroll
@@ -162,13 +162,13 @@ __global__ void __launch_bounds__(kThreads, 3)
       const float c0 = inc - a1 + a0, c1 = inc;
       const float cend = __shfl_sync(0xffffffffu, inc, 31);
       if (kRev) {
-        sm.scale[s][t0] = expf(c0);
-        sm.scale[s][t1] = expf(c1);
+        sm.scale[s][t0] = __expf(c0);
+        sm.scale[s][t1] = __expf(c1);
       } else {
-        sm.scale[s][t0] = expf(cend - c0) * d0;
-        sm.scale[s][t1] = expf(cend - c1) * d1;
+        sm.scale[s][t0] = __expf(cend - c0) * d0;
+        sm.scale[s][t1] = __expf(cend - c1) * d1;
       }
-      if (lane == 0) sm.aend[s] = expf(cend);
+      if (lane == 0) sm.aend[s] = __expf(cend);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sc_ready[s]);
       return true;
