@@ -76,11 +76,8 @@ struct alignas(1024) BwdcSmem {
   uint8_t dvd[2][kTileLP];  // exp(cum_end - cum) dt' x [s][p]
   uint8_t W[2][kTileLP];    // [t][s]; (the 8 KB after W[j] feed the unused upper rows of dv_or)
   uint8_t dcbs[kTileLP];    // sum over the chunk run of dCB [t][s], bf16 (the fp32 sum lives in E's registers)
-  // K1 scalars, ring of four heads.  G_s = exp(cum_e(s) - cum_s), Gd_s = G_s dt'_s and
-  // E_t[j] = exp(cum_t - cum_e(j)), where e(j) is the last position of 16-block j: exp(cum_t - cum_s)
-  // for s in an earlier block than t is E_t[blk(s)] G_s (both factors <= 1).
-  float cum[4][kL], ecum[4][kL], dec[4][kL], dtp[4][kL], z[4][kL], G[4][kL], Gd[4][kL];
-  float E[4][kL][4];
+  // K1 scalars, ring of four heads
+  float cum[4][kL], ecum[4][kL], dec[4][kL], dtp[4][kL], z[4][kL];
   float aend[4], Ah[4];
   // per-head partial sums for the d cum assembly
   float drow[2][2][kL], dcolp[2][4][kL], dcb[2][kL], dde[2][2][kL], dvx[2][2][kL], k4p[2][2];
@@ -142,22 +139,15 @@ __device__ __forceinline__ float e_blocks(BwdcSmem& sm, uint32_t tw, const float
     const int s0 = 16 * jj + 8 * hl;
     const uint32_t* r8 = rr[b];
     const float* cb = cbv + 8 * b;
+    // exp(cum_t - cum_s), masked before the exponential (cum_t - cum_s <= 0 for s <= t, so no block
+    // needs a split of the decay); one code path for every block keeps E's code small
     float w[8], dcb[8];
-    if (jj < q4) {  // block before the row's block: exp(cum_t - cum_s) = E_t[jj] G_s
-      const float f = sm.E[k][t][jj];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        w[e] = cb[e] * (f * sm.G[k][s0 + e]);
-        dcb[e] = __uint_as_float(r8[e]) * (f * sm.Gd[k][s0 + e]);
-      }
-    } else {  // the diagonal block, masked before the exponential
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int s = s0 + e;
-        const float ex = (s <= t) ? __expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
-        w[e] = cb[e] * ex;
-        dcb[e] = __uint_as_float(r8[e]) * sm.dtp[k][s] * ex;
-      }
+    for (int e = 0; e < 8; ++e) {
+      const int s = s0 + e;
+      const float ex = (s <= t) ? __expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
+      w[e] = cb[e] * ex;
+      dcb[e] = __uint_as_float(r8[e]) * sm.dtp[k][s] * ex;
     }
     store_row_bf16(sm.W[j], t, hl + 2 * jj, w, 1);
     // the run's dCB sum, fp32; its last head also writes the bf16 copy for the MMA
@@ -429,21 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         sm.aend[k] = __expf(cend);
         sm.Ah[k] = A_h;
-      }
-      const float e0 = __shfl_sync(0xffffffffu, c1, 7), e1 = __shfl_sync(0xffffffffu, c1, 15);
-      const float e2 = __shfl_sync(0xffffffffu, c1, 23), e3 = __shfl_sync(0xffffffffu, c1, 31);
-      const int blk = t0 >> 4;
-      const float my_end = blk == 0 ? e0 : (blk == 1 ? e1 : (blk == 2 ? e2 : e3));
-      const float g0 = __expf(my_end - c0), g1 = __expf(my_end - c1);  // decay to the end of the 16-block
-      sm.G[k][t0] = g0;
-      sm.G[k][t1] = g1;
-      sm.Gd[k][t0] = g0 * d0;
-      sm.Gd[k][t1] = g1 * d1;
-      const float ends[4] = {e0, e1, e2, e3};
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        sm.E[k][t0][qq] = (qq < blk) ? __expf(c0 - ends[qq]) : 0.f;
-        sm.E[k][t1][qq] = (qq < blk) ? __expf(c1 - ends[qq]) : 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sc_ready[k]);
