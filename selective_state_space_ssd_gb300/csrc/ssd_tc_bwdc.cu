@@ -127,18 +127,22 @@ __device__ __forceinline__ float e_blocks(BwdcSmem& sm, uint32_t tw, const float
   const int lane = threadIdx.x & 31, hl = lane >> 4, t = 16 * q4 + (lane & 15);
   const float ct = sm.cum[k][t];
   float rowsum = 0.f;
-  uint32_t rr[2][8];  // dW~[t][s0 .. s0 + 7] of both blocks (lanes 16-31 read their rows' upper 8 columns)
-#pragma unroll
-  for (int b = 0; b < 2; ++b)
-    if (jlo + b <= q4) tmem_ld_pair8(taddr(tw, 32 * q4, 16 * (jlo + b)), rr[b]);
-  tmem_wait_ld();
-#pragma unroll
+  // one loop body for both blocks (rolled: the kernel is bound by instruction fetch); the block's CB and
+  // dCB-sum registers are picked with selects, so the arrays stay in registers
+#pragma unroll 1
   for (int b = 0; b < 2; ++b) {
     const int jj = jlo + b;
     if (jj > q4) break;
     const int s0 = 16 * jj + 8 * hl;
-    const uint32_t* r8 = rr[b];
-    const float* cb = cbv + 8 * b;
+    uint32_t r8[8];  // dW~[t][s0 .. s0 + 7] (lanes 16-31 read their rows' upper 8 columns)
+    tmem_ld_pair8(taddr(tw, 32 * q4, 16 * jj), r8);
+    float cb[8], da[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      cb[e] = b ? cbv[8 + e] : cbv[e];
+      da[e] = b ? dacc[8 + e] : dacc[e];
+    }
+    tmem_wait_ld();
     // exp(cum_t - cum_s), masked before the exponential (cum_t - cum_s <= 0 for s <= t, so no block
     // needs a split of the decay); one code path for every block keeps E's code small
     float w[8], dcb[8];
@@ -152,8 +156,14 @@ __device__ __forceinline__ float e_blocks(BwdcSmem& sm, uint32_t tw, const float
     store_row_bf16(sm.W[j], t, hl + 2 * jj, w, 1);
     // the run's dCB sum, fp32; its last head also writes the bf16 copy for the MMA
 #pragma unroll
-    for (int e = 0; e < 8; ++e) dacc[8 * b + e] = first ? dcb[e] : dacc[8 * b + e] + dcb[e];
-    if (last) store_row_bf16(sm.dcbs, t, hl + 2 * jj, dacc + 8 * b, 1);
+    for (int e = 0; e < 8; ++e) {
+      da[e] = first ? dcb[e] : da[e] + dcb[e];
+      if (b)
+        dacc[8 + e] = da[e];
+      else
+        dacc[e] = da[e];
+    }
+    if (last) store_row_bf16(sm.dcbs, t, hl + 2 * jj, da, 1);
     float dd[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -672,38 +682,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float e = sm.dec[k][s], d = sm.dtp[k][s];
       float sx = 0.f, sd = 0.f;
+#pragma unroll 1
+      for (int qq = 0; qq < 4; ++qq) {  // 8 columns at a time (rolled: the kernel is bound by instruction fetch)
+        const int c0 = 32 * ch + 8 * qq;
+        uint32_t ro[8], rd[8];
+        tmem_ld8_nowait(taddr(TW(j), 32 * (warp & 3), c0), ro);
+        tmem_ld8_nowait(taddr(YD(j), 32 * (warp & 3), c0), rd);
+        const uint4 w4 = qq == 0 ? xr[0] : qq == 1 ? xr[1] : qq == 2 ? xr[2] : xr[3];
+        float xv[8];
+        {
+          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {  // 16 columns at a time
-        const int c0 = 32 * ch + 16 * qq;
-        uint32_t ro[16], rd[16];
-        tmem_ld16_nowait(taddr(TW(j), 32 * (warp & 3), c0), ro);
-        tmem_ld16_nowait(taddr(YD(j), 32 * (warp & 3), c0), rd);
-        tmem_wait_ld();
-        float dxv[16];
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          float xv[8];
-          {
-            const uint4 w4 = xr[2 * qq + jj];
-            const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float2 f = unpack_bf16(w[e2]);
-              xv[2 * e2] = f.x;
-              xv[2 * e2 + 1] = f.y;
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int p = 8 * jj + u;
-            const float ddv = __uint_as_float(rd[p]);
-            const float dv = __uint_as_float(ro[p]) + e * ddv;
-            sx += dv * xv[u];
-            sd += ddv * xv[u];
-            dxv[p] = d * dv;
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float2 f = unpack_bf16(w[e2]);
+            xv[2 * e2] = f.x;
+            xv[2 * e2 + 1] = f.y;
           }
         }
-        store_row_bf16(sm.dch[j], s, c0 / 8, dxv, 2);  // dch[j] is free once set 2 has run
+        tmem_wait_ld();
+        float dxv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float ddv = __uint_as_float(rd[u]);
+          const float dv = __uint_as_float(ro[u]) + e * ddv;
+          sx += dv * xv[u];
+          sd += ddv * xv[u];
+          dxv[u] = d * dv;
+        }
+        store_row_bf16(sm.dch[j], s, c0 / 8, dxv, 1);  // dch[j] is free once set 2 has run
       }
       sm.dvx[j][ch][s] = sx;
       sm.dde[j][ch][s] = sd * d;  // sum_p ddv[s][p] v[s][p], this column half
