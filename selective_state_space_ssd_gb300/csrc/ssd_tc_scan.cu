@@ -41,16 +41,21 @@ constexpr int kWarpScale0 = 4, kWarpScal = 6, kWarpTma = 7, kWarpMma = 8;
 constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
 constexpr uint32_t kTileLN = kL * kN * 2;  // 16 KB
 constexpr uint32_t kTileNP = kN * kP * 2;  // 16 KB
-constexpr uint32_t kTmemCols = 128;
-constexpr int kScal = 4;  // K1 scalars run up to four chunks ahead  // S in columns 0-63, P in 64-127
+constexpr uint32_t kTmemCols = 128;  // S in columns 0-63, P in 64-127
+constexpr int kScal = 4;             // K1 scalars run up to four chunks ahead
+constexpr int kStK = 2;              // B / C tiles (mostly L2 hits: every head of a group reads them)
 
+// kStU: depth of the x / dy ring, the HBM stream whose latency the ring hides (three stages when three
+// CTAs still fit an SM, else two).
+template <int kStU>
 struct alignas(1024) ScanSmem {
-  uint8_t u[2][kTileLP];  // x or dy [t][p], scaled in place to dvd or dch
-  uint8_t k[2][kTileLN];  // B or C [t][n], two 64-column atoms
-  uint8_t out[kTileNP];   // bf16 state tile [n][p] on its way out; state warp w owns rows 32 w .. 32 w + 31
-  float scale[kScal][kL];  // per-row factor of U: exp(cum_end - cum) dt' or exp(cum); ring of kScal chunks
-  float aend[kScal];       // exp(cum_end)
-  uint64_t full[2], empty[2], pre_done[2], sc_ready[kScal], sc_free[kScal];
+  uint8_t u[kStU][kTileLP];  // x or dy [t][p], scaled in place to dvd or dch
+  uint8_t k[kStK][kTileLN];  // B or C [t][n], two 64-column atoms
+  uint8_t out[kTileNP];      // bf16 state tile [n][p] on its way out; state warp w owns rows 32 w .. 32 w + 31
+  float scale[kScal][kL];    // per-row factor of U: exp(cum_end - cum) dt' or exp(cum); ring of kScal chunks
+  float aend[kScal];         // exp(cum_end)
+  uint64_t full_u[kStU], empty_u[kStU], pre_done[kStU], full_k[kStK], empty_k[kStK];
+  uint64_t sc_ready[kScal], sc_free[kScal];
   uint64_t p_ready, p_free, drain;
   uint32_t tmem_slot;
 };
@@ -64,12 +69,12 @@ struct ScanParams {
   int T, H, hpg, nc;
 };
 
-template <bool kRev>
+template <bool kRev, int kStU>
 __global__ void __launch_bounds__(kThreads, 3)
     k_scan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_out, ScanParams prm) {
   extern __shared__ uint8_t smem_raw[];
-  ScanSmem& sm = *reinterpret_cast<ScanSmem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  ScanSmem<kStU>& sm = *reinterpret_cast<ScanSmem<kStU>*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, b = blockIdx.y;
   const int T = prm.T, H = prm.H, nc = prm.nc;
@@ -80,10 +85,14 @@ __global__ void __launch_bounds__(kThreads, 3)
   auto chunk_of = [&](int r) { return kRev ? nc - 1 - r : r; };
 
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);  // MMA commit (it waited for the scale warps)
+    for (int s = 0; s < kStU; ++s) {
+      mbar_init(&sm.full_u[s], 1);
+      mbar_init(&sm.empty_u[s], 1);  // MMA commit (it waited for the scale warps)
       mbar_init(&sm.pre_done[s], 1);
+    }
+    for (int s = 0; s < kStK; ++s) {
+      mbar_init(&sm.full_k[s], 1);
+      mbar_init(&sm.empty_k[s], 1);  // MMA commit
     }
     for (int s = 0; s < kScal; ++s) {
       mbar_init(&sm.sc_ready[s], 1);
@@ -105,13 +114,17 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (lane == 0) {
       prefetch_tmap(&tm_u);
       prefetch_tmap(&tm_k);
+      int su = 0, pu = 0;  // x / dy ring slot and its phase
       for (int r = 0; r < nc; ++r) {
-        const int s = r & 1, c = chunk_of(r);
-        if (r >= 2 && !mbar_wait(&sm.empty[s], ((r >> 1) - 1) & 1, status, 81)) break;
-        mbar_expect_tx(&sm.full[s], kTileLP + kTileLN);
-        tma_load_2d(sm.u[s], &tm_u, h * kP, row0 + c * kL, &sm.full[s]);
+        const int sk = r & 1, c = chunk_of(r);
+        if (r >= kStU && !mbar_wait(&sm.empty_u[su], pu ^ 1, status, 81)) break;
+        mbar_expect_tx(&sm.full_u[su], kTileLP);
+        tma_load_2d(sm.u[su], &tm_u, h * kP, row0 + c * kL, &sm.full_u[su]);
+        if (r >= kStK && !mbar_wait(&sm.empty_k[sk], ((r >> 1) - 1) & 1, status, 80)) break;
+        mbar_expect_tx(&sm.full_k[sk], kTileLN);
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(sm.k[s] + a * (kTileLN / 2), &tm_k, a * 64, g, row0 + c * kL, &sm.full[s]);
+          tma_load_3d(sm.k[sk] + a * (kTileLN / 2), &tm_k, a * 64, g, row0 + c * kL, &sm.full_k[sk]);
+        if (++su == kStU) su = 0, pu ^= 1;
       }
     }
   } else if (warp == kWarpMma) {
@@ -119,18 +132,22 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (lane == 0) {
       const uint32_t tP = tmem + 64u;
       bool ok = true;
+      int su = 0, pu = 0;
       for (int r = 0; r < nc && ok; ++r) {
-        const int s = r & 1;
-        ok = mbar_wait(&sm.pre_done[s], (r >> 1) & 1, status, 82);
+        const int sk = r & 1;
+        ok = mbar_wait(&sm.pre_done[su], pu, status, 82);
+        ok = ok && mbar_wait(&sm.full_k[sk], (r >> 1) & 1, status, 79);
         ok = ok && (r == 0 || mbar_wait(&sm.p_free, (r - 1) & 1, status, 83));
         if (!ok) break;
         tc_fence_after();
         // P[n][p] = sum_t K[t][n] U[t][p]: A = K^T (MN-major), B = U (MN-major)
 #pragma unroll
         for (int kk = 0; kk < kL; kk += 16)
-          mma_bf16(tP, mdesc(sm.k[s], kL, kk), mdesc(sm.u[s], kL, kk), idesc_bf16(128, 64, true, true), kk > 0);
+          mma_bf16(tP, mdesc(sm.k[sk], kL, kk), mdesc(sm.u[su], kL, kk), idesc_bf16(128, 64, true, true), kk > 0);
         mma_commit(&sm.p_ready);
-        mma_commit(&sm.empty[s]);
+        mma_commit(&sm.empty_u[su]);
+        mma_commit(&sm.empty_k[sk]);
+        if (++su == kStU) su = 0, pu ^= 1;
       }
       // nothing may still be writing TMEM when it is freed
       mma_commit(&sm.drain);
@@ -187,11 +204,11 @@ __global__ void __launch_bounds__(kThreads, 3)
   } else if (warp >= kWarpScale0) {
     // ------------------------------------------------------------ scale warps: U *= scale (per row)
     const int pt = tid - 32 * kWarpScale0;  // 0..63
+    int s = 0, ps = 0;  // x / dy ring slot and its phase
     for (int r = 0; r < nc; ++r) {
-      const int s = r & 1;
       const int k = r % kScal;
       bool ok = mbar_wait(&sm.sc_ready[k], (r / kScal) & 1, status, 86);
-      ok = ok && mbar_wait(&sm.full[s], (r >> 1) & 1, status, 87);
+      ok = ok && mbar_wait(&sm.full_u[s], ps, status, 87);
       if (named_bar_or(2, 64, !ok)) break;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -209,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         mbar_arrive(&sm.pre_done[s]);
         mbar_arrive(&sm.sc_free[k]);
       }
+      if (++s == kStU) s = 0, ps ^= 1;
     }
   } else {
     // ------------------------------------------------------------ state warps 0-3 (thread n owns row n)
@@ -288,6 +306,47 @@ __global__ void __launch_bounds__(kThreads, 3)
 
 }  // namespace
 
+namespace {
+
+// Three x / dy stages when three CTAs of them still fit an SM (all (batch, head) chains of the workloads
+// stay resident at once), else two.
+template <int kStU, bool kRev>
+cudaError_t launch_stages(const Dims& d, const CUtensorMap& tu, const CUtensorMap& tk, const CUtensorMap& to,
+                          const ScanParams& prm, cudaStream_t st, bool* fits) {
+  const int smem = (int)sizeof(ScanSmem<kStU>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_scan<kRev, kStU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_scan<kRev, kStU>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  if (fits) {  // shared memory of three CTAs (each with the per-block reservation) against the SM's
+    int dev = 0, per_sm = 0, reserved = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    *fits = 3ll * (smem + reserved) <= per_sm;
+    if (!*fits) return cudaSuccess;
+  }
+  if (kRev) {
+    SSD_LAUNCH("k_tc_dstates", st, k_scan<kRev, kStU><<<dim3(d.H, d.b), kThreads, smem, st>>>(tu, tk, to, prm));
+  } else {
+    SSD_LAUNCH("k_tc_states", st, k_scan<kRev, kStU><<<dim3(d.H, d.b), kThreads, smem, st>>>(tu, tk, to, prm));
+  }
+  return cudaGetLastError();
+}
+
+template <bool kRev>
+cudaError_t launch_scan(const Dims& d, const CUtensorMap& tu, const CUtensorMap& tk, const CUtensorMap& to,
+                        const ScanParams& prm, cudaStream_t st) {
+  bool fits = false;
+  cudaError_t e = launch_stages<3, kRev>(d, tu, tk, to, prm, st, &fits);
+  if (e != cudaSuccess || fits) return e;
+  return launch_stages<2, kRev>(d, tu, tk, to, prm, st, nullptr);
+}
+
+}  // namespace
+
 size_t tc_scan_states_bytes(const Dims& d) { return (size_t)d.b * d.H * d.nc * kN * kP * sizeof(__nv_bfloat16); }
 
 cudaError_t tc_scan(const Dims& d, bool reverse, const void* u, const void* k, const float* dt_raw, const float* A,
@@ -299,16 +358,12 @@ cudaError_t tc_scan(const Dims& d, bool reverse, const void* u, const void* k, c
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&to, states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, 32);
   if (e != cudaSuccess) return e;
   ScanParams prm{dt_raw, A, init, fin, status, d.T, d.H, d.hpg, d.nc};
-  const int smem = (int)sizeof(ScanSmem) + 1024;
   if (reverse) {
-    e = cudaFuncSetAttribute(k_scan<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    SSD_LAUNCH("k_tc_dstates", st, k_scan<true><<<dim3(d.H, d.b), kThreads, smem, st>>>(tu, tk, to, prm));
+    e = launch_scan<true>(d, tu, tk, to, prm, st);
   } else {
-    e = cudaFuncSetAttribute(k_scan<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    SSD_LAUNCH("k_tc_states", st, k_scan<false><<<dim3(d.H, d.b), kThreads, smem, st>>>(tu, tk, to, prm));
+    e = launch_scan<false>(d, tu, tk, to, prm, st);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
