@@ -31,15 +31,20 @@
 // chunk in a fixed order.  Per-head accumulators are double-buffered in TMEM
 // and smem, so the roles below work on two heads at once.
 //
-// Warp roles (608 threads):
-//   warps 0-3   O: dv -> dx (TMA store), K3 sums; at a chunk's end the dB^T,
-//               dC^T accumulators out to the partial buffer.
-//   warps 4-7   E: W, dCB tiles and the ORANGE sums.
-//   warps 8-11  BK: BLUE and K4.
-//   warps 12-15 P: the dch and dvd tiles.
-//   warp 16     SC: K1 scalars two heads ahead, and the per-head assembly.
-//   warp 17     TMA producer (x, dy, S_c, dS_{c+1} per head; B, C per chunk).
-//   warp 18     MMA issuer (polls both MMA sets) and TMEM owner.
+// Warp roles (640 threads):
+//   warps 0, 1, 8, 9   O: dv -> dx (TMA store), K3 sums (rows s in TMEM lanes 0-63).
+//   warps 2, 3         BK: BLUE (Y in lanes 64-127) and K4.
+//   warps 4-7          E: W, the dCB sum and the ORANGE sums, column blocks 0-1.
+//   warps 10, 11       EB: the same for column blocks 2-3 (rows 32-63).
+//   warps 12-15        P: the dch and dvd tiles; at a chunk run's end the dB^T,
+//                      dC^T accumulators out to the partial buffer.
+//   warp 16            SC: K1 scalars up to four heads ahead.
+//   warp 17            AS: the per-head d cum assembly -> ddt_raw, dA part.
+//   warp 18            MMA issuer (polls both MMA sets) and TMEM owner.
+//   warp 19            TMA producer (x, dy, S_c, dS_{c+1} per head; B, C per chunk).
+// The roles run different code at once, so the kernel is sensitive to its
+// instruction footprint: hot loops stay rolled and the scalar roles use the
+// approximate exp / log units.
 // Every wait is bounded; on a timeout the kernel records a code in the
 // workspace status word and stops.
 #include "ssd_device.cuh"
