@@ -13,7 +13,7 @@
 //
 //   set 1:  dW~ = dy x^T,  Y = C S_c^T,  ddv = B dS_{c+1}^T
 //   E:      W = CB o decay,  dCB = dW~ o dt'_s o decay,
-//           d_diff = dCB o CB  (ORANGE; row sums - column sums; mask before exp)
+//           d_diff = dCB o CB  (ORANGE row sums; mask before exp)
 //   set 2:  dv_or = W^T dy,
 //           dB^T += dS_{c+1} dvd^T + C^T dCB,  dC^T += S_c dch^T + B^T dCB^T
 //   O:      dv = dv_or + exp(cum_end - cum_s) ddv,  dx = dt' dv,
@@ -85,7 +85,7 @@ struct alignas(1024) BwdcSmem {
   float cum[4][kL], ecum[4][kL], dec[4][kL], dtp[4][kL], z[4][kL];
   float aend[4], Ah[4];
   // per-head partial sums for the d cum assembly
-  float drow[2][2][kL], dcolp[2][4][kL], dcb[2][kL], dde[2][2][kL], dvx[2][2][kL], k4p[2][2];
+  float drow[2][2][kL], dcb[2][kL], dde[2][2][kL], dvx[2][2][kL], k4p[2][2];
   uint64_t xy_full[3], xy_empty[3], sd_full[2], sd_empty[2];
   uint64_t pre_done[2], s1a_done[2], s1_done[2], e_done[2], s2_done[2], bk_done[2], o_done[2], fin_done[2];
   uint64_t sc_ready[4], sc_free[4];
@@ -119,14 +119,15 @@ __device__ __forceinline__ void load_row8(const uint8_t* tile, int r, int j, flo
   }
 }
 
-// W, the run's dCB sum and the ORANGE sums for the 16-column blocks jlo and
+// W, the run's dCB sum and the ORANGE row sums for the 16-column blocks jlo and
 // jlo + 1, where at or left of the diagonal block of rows t = 16 q4 + (lane & 15)
 // (the rest is zero; see the kernel's set-up).  Lane l < 16 takes columns
 // 16 jj .. 16 jj + 7 of its row and lane l + 16 the other 8, so every warp
 // meets each block whole and the branch on the block is warp-uniform.  cbv
 // holds CB[t][s0 .. s0 + 7] of both blocks (s0 = 16 jj + 8 (lane >> 4)) and
 // dacc the run's fp32 dCB sum of the same elements.
-// Returns the lane's part of its row sum of d_diff.
+// Returns the row sum of d_diff over these blocks (the ORANGE column sums need
+// no pass here: the assembly takes them from O's sums, see the AS role).
 __device__ __forceinline__ float e_blocks(BwdcSmem& sm, uint32_t tw, const float (&cbv)[16], float (&dacc)[16], int j,
                                           int k, int q4, int jlo, bool first, bool last) {
   const int lane = threadIdx.x & 31, hl = lane >> 4, t = 16 * q4 + (lane & 15);
@@ -169,33 +170,12 @@ __device__ __forceinline__ float e_blocks(BwdcSmem& sm, uint32_t tw, const float
         dacc[e] = da[e];
     }
     if (last) store_row_bf16(sm.dcbs, t, hl + 2 * jj, da, 1);
-    float dd[8];
+    // ORANGE row sum of d_diff = dW o dt' o W, with W rounded to bf16 as the dv_or MMA reads it: the column
+    // sums come from dv_or (the AS role), and the two must see the same W or their large terms stop
+    // cancelling in dA
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      dd[e] = dcb[e] * cb[e];  // d_diff = dW o decay o dt' o CB
-      rowsum += dd[e];
-    }
-    // column sums of these 8 columns over the 16 rows of this half: transposing butterfly
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const bool up = lane & 8;
-      const float send = up ? dd[kk] : dd[kk + 4], keep = up ? dd[kk + 4] : dd[kk];
-      dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const bool up = lane & 4;
-      const float send = up ? dd[kk] : dd[kk + 2], keep = up ? dd[kk + 2] : dd[kk];
-      dd[kk] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    {
-      const bool up = lane & 2;
-      const float send = up ? dd[0] : dd[1], keep = up ? dd[1] : dd[0];
-      dd[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    dd[0] += __shfl_xor_sync(0xffffffffu, dd[0], 1);
-    // lanes l and l ^ 1 now both hold column s0 + 4 b3 + 2 b2 + b1 (b_i: bits of the lane)
-    if (!(lane & 1)) sm.dcolp[j][q4][s0 + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1)] = dd[0];
+    for (int e = 0; e < 8; ++e)
+      rowsum += __uint_as_float(r8[e]) * sm.dtp[k][s0 + e] * __bfloat162float(__float2bfloat16_rn(w[e]));
   }
   return rowsum + __shfl_xor_sync(0xffffffffu, rowsum, 16);
 }
@@ -249,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for every head: written once here, never touched by the per-head work
   for (int i = tid; i < (int)(3 * kTileLP / 16); i += kThreads)
     reinterpret_cast<uint4*>(sm.W[0])[i] = make_uint4(0, 0, 0, 0);  // W[0], W[1], dcbs are contiguous
-  for (int i = tid; i < 2 * 4 * kL; i += kThreads) (&sm.dcolp[0][0][0])[i] = 0.f;
   for (int i = tid; i < 2 * kL; i += kThreads) sm.drow[i / kL][1][i % kL] = 0.f;
   fence_proxy_async();
   tc_fence_before();
@@ -451,13 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = ok && mbar_wait(&sm.o_done[j], ph, status, 108);
       if (!ok) break;
       const float A_h = sm.Ah[k];
-      // d cum per position: ORANGE row - column sums, BLUE, K3; K3's and K4's chunk-end terms at t = 63
+      // d cum per position: ORANGE row sums, BLUE, minus <dv, v>; K3's and K4's chunk-end terms at t = 63
       const float dec0 = sm.dec[k][t0], dec1 = sm.dec[k][t1];
       const float k3_0 = (sm.dde[j][0][t0] + sm.dde[j][1][t0]) * dec0, k3_1 = (sm.dde[j][0][t1] + sm.dde[j][1][t1]) * dec1;
-      float dc0 = sm.drow[j][0][t0] + sm.drow[j][1][t0] - (sm.dcolp[j][0][t0] + sm.dcolp[j][1][t0] + sm.dcolp[j][2][t0] + sm.dcolp[j][3][t0]) +
-                  sm.dcb[j][t0] - k3_0;
-      float dc1 = sm.drow[j][0][t1] + sm.drow[j][1][t1] - (sm.dcolp[j][0][t1] + sm.dcolp[j][1][t1] + sm.dcolp[j][2][t1] + sm.dcolp[j][3][t1]) +
-                  sm.dcb[j][t1] - k3_1;
+      // Every term in which cum_s enters through exp(-cum_s) v_s (ORANGE's column sums and K3's
+      // exp(cum_end - cum_s)) adds up to -<dv_s, v_s>, with dv the whole gradient of v = dt' x:
+      // -dt'_s sum_p dv[s][p] x[s][p] from O's sums
+      const float vx0 = sm.dvx[j][0][t0] + sm.dvx[j][1][t0], vx1 = sm.dvx[j][0][t1] + sm.dvx[j][1][t1];
+      float dc0 = sm.drow[j][0][t0] + sm.drow[j][1][t0] + sm.dcb[j][t0] - sm.dtp[k][t0] * vx0;
+      float dc1 = sm.drow[j][0][t1] + sm.drow[j][1][t1] + sm.dcb[j][t1] - sm.dtp[k][t1] * vx1;
       float k3sum = k3_0 + k3_1;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) k3sum += __shfl_xor_sync(0xffffffffu, k3sum, o);
@@ -473,9 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float dda0 = suf, dda1 = suf - dc0;
       const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
-      __stcs(prm.ddt_raw + rr * H + h, (sm.dvx[j][0][t0] + sm.dvx[j][1][t0] + A_h * dda0) * sigmoid_fast(sm.z[k][t0]));
+      __stcs(prm.ddt_raw + rr * H + h, (vx0 + A_h * dda0) * sigmoid_fast(sm.z[k][t0]));
       __stcs(prm.ddt_raw + (rr + 1) * H + h,
-             (sm.dvx[j][0][t1] + sm.dvx[j][1][t1] + A_h * dda1) * sigmoid_fast(sm.z[k][t1]));
+             (vx1 + A_h * dda1) * sigmoid_fast(sm.z[k][t1]));
       float dAp = dda0 * sm.dtp[k][t0] + dda1 * sm.dtp[k][t1];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
