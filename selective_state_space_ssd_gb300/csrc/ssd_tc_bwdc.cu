@@ -32,11 +32,11 @@
 //   warps 0-15  the pool: all CUDA-core work, in three phases per iteration i
 //               (warp w works on TMEM lane quadrant w % 4):
 //                 S1  O of head i-1 (quadrants 0-1: rows s of dv_or and ddv) beside
-//                     BK of head i-1 (quadrants 2-3: rows t of Y; K4 on the smem tiles);
+//                     BLUE of head i-1 (quadrants 2-3: rows t of Y);
 //                     at a chunk run's end every warp reads the dB^T, dC^T accumulators out
 //                 S2  P of head i+1: the dch and dvd tiles
 //                 S3  E of head i on ten warps (one 16 x 16 block of dW~ each) beside
-//                     the d cum assembly AS of head i-1 on one more
+//                     the d cum assembly AS of head i-1 on one more and K4 of head i on four
 //               The phases run in lockstep (named barriers), so the pool executes one
 //               phase's code at a time: a small instruction footprint and short per-head
 //               latency chains.
@@ -87,8 +87,8 @@ struct alignas(1024) BwdcSmem {
   float cum[4][kL], ecum[4][kL], dec[4][kL], dtp[4][kL], z[4][kL];
   float aend[4], Ah[4];
   // per-head partial sums for the d cum assembly (two heads): ORANGE row sums per column block, BLUE
-  // and the dv.x / ddv.x sums per 16-column group, K4 per BK warp
-  float drow[2][4][kL], blue[2][4][kL], dvx[2][4][kL], dde[2][4][kL], k4p[2][8];
+  // and the dv.x / ddv.x sums per 16-column group, K4 per K4 warp
+  float drow[2][4][kL], blue[2][4][kL], dvx[2][4][kL], dde[2][4][kL], k4p[2][4];
   uint64_t xy_full[3], xy_empty[3], sd_full[2], sd_empty[2];
   uint64_t pre_done[2], s1a_done[2], s1b_done[2], e_done[2], s2_done[2], tmem_free[2];
   uint64_t sc_ready[4], sc_free[4];
@@ -362,9 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int ip = i - 1, jp = ip & 1, kp = ip & 3;
         const bool run_end = has_prev && co.last(geo, q1);
+        // one thread waits for the phase's inputs; the named barrier passes them to the pool
         bool ok = true;
-        if (has_prev) ok = mbar_wait(&sm.s2_done[jp], (ip >> 1) & 1, status, 121);
-        if (ok && run_end) ok = mbar_wait(&sm.acc_full, (seg_o + 1) & 1, status, 122);
+        if (tid == 0 && has_prev) ok = mbar_wait(&sm.s2_done[jp], (ip >> 1) & 1, status, 121);
+        if (tid == 0 && ok && run_end) ok = mbar_wait(&sm.acc_full, (seg_o + 1) & 1, status, 122);
         if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
         tc_fence_after();
         if (has_prev) {
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm.dvx[jp][gi][s] = sx;
             sm.dde[jp][gi][s] = sd * d;  // sum_p ddv[s][p] v[s][p], this column group
           } else {
-            // BK: BLUE on rows t = 32 (qd - 2) + lane of Y (YD lanes 64-127, columns 64 + 16 gi ..)
+            // BK: BLUE on rows t = 32 (qd - 2) + lane of Y (YD lanes 64-127, columns 64 + 16 gi ..); K4 runs in S3
             const int t = 32 * (qd - 2) + lane;
             uint32_t ry[16];
             tmem_ld16_nowait(taddr(YD(jp), 32 * qd, 64 + 16 * gi), ry);
@@ -404,20 +405,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 16; ++u) acc += gv[u] * __uint_as_float(ry[u]);
             sm.blue[jp][gi][t] = acc;
-            // K4: <dS_{c+1}, S_c>, thread u2 takes row u2 / 2, columns 32 (u2 & 1) ..
-            const int u2 = 32 * (4 * (qd - 2) + gi) + lane, r = u2 >> 1;
-            float part = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              float sv[8], dv[8];
-              load_row8(sm.sd[jp].S, r, 4 * (u2 & 1) + c, sv);
-              load_row8(sm.sd[jp].dS, r, 4 * (u2 & 1) + c, dv);
-#pragma unroll
-              for (int e2 = 0; e2 < 8; ++e2) part += dv[e2] * sv[e2];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (lane == 0) sm.k4p[jp][4 * (qd - 2) + gi] = part;
           }
           if (run_end) {
             // the chunk run ends: dB^T and dC^T (lane n, column s or t) to this CTA's partial slot of the chunk;
@@ -442,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int in = i + 1, jn = in & 1, kn = in & 3;
         bool ok = true;
-        if (has_next) {
+        if (tid == 0 && has_next) {
           ok = mbar_wait(&sm.sc_ready[kn], (in >> 2) & 1, status, 110);
           ok = ok && mbar_wait(&sm.xy_full[in % 3], (in / 3) & 1, status, 111);
           if (ok && in >= 2) ok = mbar_wait(&sm.s1b_done[jn], ((in >> 1) - 1) & 1, status, 112);  // 1b(i-1) read dch, dvd
@@ -489,10 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           cbv[0] = u.x, cbv[1] = u.y, cbv[2] = u.z, cbv[3] = u.w;
           cbv[4] = v.x, cbv[5] = v.y, cbv[6] = v.z, cbv[7] = v.w;
         }
+        const int k4w = (warp == 8 || warp == 9 || warp == 12 || warp == 13) ? 2 * ((warp >> 2) - 2) + (warp & 1) : -1;
         bool ok = true;
-        if (has_cur && e_warp) {
-          ok = mbar_wait(&sm.s1a_done[j], (i >> 1) & 1, status, 117);
+        if (tid == 0 && has_cur) {
+          ok = mbar_wait(&sm.sd_full[j], (i >> 1) & 1, status, 127);  // K4
+          ok = ok && mbar_wait(&sm.s1a_done[j], (i >> 1) & 1, status, 117);
           // the bf16 dCB sum of the previous run must have been read by its MMAs
+          // (thread 0 is in an E warp, so seg_e counts its runs)
           if (ok && last && seg_e >= 1) ok = mbar_wait(&sm.chunk_empty, (seg_e - 1) & 1, status, 126);
         }
         fence_proxy_async();
@@ -531,6 +521,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.e_done[j]);
+        } else if (has_cur && k4w >= 0) {
+          // K4 of head i: <dS_{c+1}, S_c>, thread u takes state row n = u of both tiles
+          const int n = 32 * k4w + lane;
+          float part = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            float sv[8], dv[8];
+            load_row8(sm.sd[j].S, n, c, sv);
+            load_row8(sm.sd[j].dS, n, c, dv);
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) part += dv[e2] * sv[e2];
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+          if (lane == 0) sm.k4p[j][k4w] = part;
         } else if (warp == kWarpAs && has_prev) {
           // AS of head i - 1: d cum per position, then the K1 backward (suffix sums) to ddt_raw and dA
           const int ip = i - 1, jp = ip & 1, kp = ip & 3;
@@ -553,9 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float k3sum = de0 * dec0 + de1 * dec1;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) k3sum += __shfl_xor_sync(0xffffffffu, k3sum, o);
-          float k4 = 0.f;
-#pragma unroll
-          for (int w2 = 0; w2 < 8; ++w2) k4 += sm.k4p[jp][w2];
+          const float k4 = (sm.k4p[jp][0] + sm.k4p[jp][1]) + (sm.k4p[jp][2] + sm.k4p[jp][3]);
           if (lane == 31) dc1 += k3sum + sm.aend[kp] * k4;
           // suffix sums (K1 backward): dda[t] = sum_{u >= t} d cum[u]
           const float pair = dc0 + dc1;
