@@ -301,11 +301,14 @@ def run_ours(args, cfg, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)  # 516 MB > L2
 
-    def step(inp):
-        binding.ssd_forward(prob, inp["x"], inp["dt_raw"], inp["A"], inp["B"], inp["C"], inp["s0"], y, sf, wsf, nf,
-                            stream)
+    out0 = dict(g, y=y, s_final=sf)
+
+    def step(inp, out=out0):
+        binding.ssd_forward(prob, inp["x"], inp["dt_raw"], inp["A"], inp["B"], inp["C"], inp["s0"], out["y"],
+                            out["s_final"], wsf, nf, stream)
         binding.ssd_backward(prob, inp["dy"], inp["ds_final"], inp["x"], inp["dt_raw"], inp["A"], inp["B"], inp["C"],
-                             inp["s0"], g["dx"], g["ddt_raw"], g["dA"], g["dB"], g["dC"], g["ds0"], wsb, nb, stream)
+                             inp["s0"], out["dx"], out["ddt_raw"], out["dA"], out["dB"], out["dC"], out["ds0"], wsb, nb,
+                             stream)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -349,35 +352,53 @@ def run_ours(args, cfg, rank, world, local_rank):
         a[1] += ms
     launches_per_step = len(recs) / max(1, args.steps)
 
-    # end to end through the public API with host buffers (pinned)
+    # end to end through the public API with host buffers (pinned).  Every step copies its inputs in from
+    # pinned host memory and all of its outputs back; the copies of neighbouring steps overlap the compute:
+    # two device buffer sets, inputs of step k+1 going in and outputs of step k-1 coming out (on their own
+    # streams, the two copy directions) while step k runs.
     host_in = {k: (None if v is None else v.pin_memory()) for k, v in cpu.items()}
-    host_out = {"y": torch.empty(y.shape, dtype=y.dtype, pin_memory=True),
-                "s_final": torch.empty(sf.shape, dtype=sf.dtype, pin_memory=True)}
-    for k, v in g.items():
-        if v is not None:
-            host_out[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out0.items() if v is not None}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    bufs_in = [t, {k: (None if v is None else torch.empty_like(v)) for k, v in t.items()}]
+    bufs_out = [out0, {k: (None if v is None else torch.empty_like(v)) for k, v in out0.items()}]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k, v in host_in.items():
-            if v is not None:
-                t[k].copy_(v, non_blocking=True)
-        step(t)
-        host_out["y"].copy_(y, non_blocking=True)
-        host_out["s_final"].copy_(sf, non_blocking=True)
-        for k, v in g.items():
-            if v is not None:
-                host_out[k].copy_(v, non_blocking=True)
+    def e2e_run(n):
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for k in range(n):
+            b = k % 2
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(comp_done[b])        # step k-2 has read this input set
+                for name, v in host_in.items():
+                    if v is not None:
+                        bufs_in[b][name].copy_(v, non_blocking=True)
+                in_ready[b].record(s_in)
+            stream.wait_event(in_ready[b])
+            if k >= 2:
+                stream.wait_event(out_done[b])          # step k-2's outputs have been copied out
+            step(bufs_in[b], bufs_out[b])
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                for name, v in host_out.items():
+                    v.copy_(bufs_out[b][name], non_blocking=True)
+                out_done[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
 
     e2e_steps = max(1, min(args.steps, 10))
-    e2e_step()
+    e2e_run(2)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
@@ -476,7 +497,8 @@ def main():
             "gpu_launches": int(round(r["launches_per_step"] * args.steps)),
             "clocks": r["clocks"],
             "e2e": {"value": world * tok * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}}
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                    "overlap": "double-buffered: step k+1's inputs in and step k-1's outputs out during step k"}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # about 10 s of oracle work: the whole workload, repeated until 10 s have passed (at most 8 passes)
         v, dt, cores, desc, _, _ = time_oracle(cfg, whole=True, min_seconds=10.0, max_passes=8)
