@@ -40,7 +40,10 @@ using namespace tc;
 
 constexpr int kL = 64, kP = 64, kN = 128;
 constexpr int kThreads = 352;
-constexpr int kWarpW0 = 4, kWarpScal = 8, kWarpTma = 9, kWarpMma = 10;
+constexpr int kPoolWarps = 8, kPoolThreads = 32 * kPoolWarps;
+constexpr int kWarpScal = 8, kWarpTma = 9, kWarpMma = 10;
+constexpr int kBarPool = 1;  // named barrier of the pool
+constexpr int kSc = 4;       // K1 scalar ring (pairs): read by W of pair k and the epilogue of pair k a phase later
 constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
 constexpr uint32_t kTileNP = kN * kP * 2;  // 16 KB
 constexpr uint32_t kTmemCols = 512;        // per pair slot: y_diag and y_off, 128 columns each
@@ -51,12 +54,12 @@ struct alignas(1024) FwdcSmem {
   uint8_t W[2][2][kTileLP];  // W' [t][s]; a slot's two tiles are one K-major operand of 128 rows
   uint8_t CC[4][kTileLP];    // C atom 0, C atom 0, C atom 1, C atom 1 ([t][64 n]): [C; C] of 128 rows
   uint8_t y[2][2][kTileLP];  // y staging [t][p]
-  // K1 scalars of the pairs in flight, [slot][head].  Gd_s = exp(cum_e(s) - cum_s) dt'_s and E_t[j] =
+  // K1 scalars of the pairs in flight, [ring slot][head].  Gd_s = exp(cum_e(s) - cum_s) dt'_s and E_t[j] =
   // exp(cum_t - cum_e(j)), where e(j) is the last position of 16-block j: for s in an earlier block
   // than t, exp(cum_t - cum_s) dt'_s = E_t[blk(s)] Gd_s (both exponentials <= 1).
-  float cum[2][2][kL], ecum[2][2][kL], dtp[2][2][kL], Gd[2][2][kL];
-  float E[2][2][kL][4];
-  uint64_t slot_full[2], slot_empty[2], sc_ready[2], sc_free[2], w_ready[2], mma_done[2], epi_done[2];
+  float cum[kSc][2][kL], ecum[kSc][2][kL], dtp[kSc][2][kL], Gd[kSc][2][kL];
+  float E[kSc][2][kL][4];
+  uint64_t slot_full[2], slot_empty[2], w_ready[2], mma_done[2], epi_done[2], sc_ready[kSc], sc_free[kSc];
   uint64_t chunk_full, chunk_empty, drain;
   uint32_t tmem_slot;
 };
@@ -107,11 +110,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < 2; ++r) {
       mbar_init(&sm.slot_full[r], 1);
       mbar_init(&sm.slot_empty[r], 1);  // MMA commit
-      mbar_init(&sm.sc_ready[r], 1);
-      mbar_init(&sm.sc_free[r], 2);  // W warps + epilogue warps
       mbar_init(&sm.w_ready[r], 1);
       mbar_init(&sm.mma_done[r], 1);
       mbar_init(&sm.epi_done[r], 1);
+    }
+    for (int r = 0; r < kSc; ++r) {
+      mbar_init(&sm.sc_ready[r], 1);
+      mbar_init(&sm.sc_free[r], kPoolWarps);  // every pool warp after the pair's epilogue
     }
     mbar_init(&sm.chunk_full, 1);
     mbar_init(&sm.chunk_empty, 1);
@@ -187,13 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sm.drain, 0, status, 207);
     }
   } else if (warp == kWarpScal) {
-    // ------------------------------------------------------------ K1 scalars, one pair ahead
+    // ------------------------------------------------------------ K1 scalars, up to kSc pairs ahead
     const int t0 = 2 * lane, t1 = t0 + 1;
     PairCursor u;
     u.seek(geo, q0, q1);
     for (int k = 0; u.a.f < q1; ++k, u.next(geo, q1)) {
-      const int r = k & 1;
-      if (k >= 2 && !mbar_wait(&sm.sc_free[r], ((k >> 1) - 1) & 1, status, 208)) break;
+      const int r = k % kSc;
+      if (k >= kSc && !mbar_wait(&sm.sc_free[r], (k / kSc - 1) & 1, status, 208)) break;
       for (int i = 0; i < u.n; ++i) {
         const int h = u.a.h(geo) + i;
         const float A_h = prm.A[h];
@@ -229,105 +234,111 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sc_ready[r]);
     }
-  } else if (warp >= kWarpW0) {
-    // ------------------------------------------------------------ W' tiles
-    // Row t = 16 (warp - 4) + (lane & 15); lane l < 16 takes columns 16 jj .. 16 jj + 7 of each block jj and
-    // lane l + 16 the other 8, so the branch on the block (before / on the row's block) is uniform across
-    // the warp.  Blocks after the row's block stay zero.
-    const int qw = warp - kWarpW0;
-    const int hl = lane >> 4, t = 16 * qw + (lane & 15);
-    float cbv[32];  // CB[t][16 jj + 8 hl .. + 7] for jj <= qw, loaded once per chunk run
-    PairCursor u;
-    u.seek(geo, q0, q1);
-    for (int k = 0; u.a.f < q1; ++k, u.next(geo, q1)) {
-      const int r = k & 1, ph = (k >> 1) & 1;
-      if (u.a.first(q0)) {
-        const float* cbrow = prm.CB + ((size_t)u.a.k * kL + t) * kL + 8 * hl;
+  } else if (warp < kPoolWarps) {
+    // ------------------------------------------------------------ the pool (warps 0-7).  Iteration k:
+    //   A  W' of pair k: 20 blocks of 16 x 16 (two heads x the ten blocks at or left of the diagonal),
+    //      warp w takes blocks w, w + 8, w + 16 (the other warps' blocks of the same head are independent)
+    //   B  epilogue of pair k - 1: y = y_diag + exp(cum) y_off; warp w reads TMEM lanes 32 (w % 4) ..
+    //      (head w % 4 / 2) and columns 32 (w / 4) .. of that head
+    // The y tiles of pair k - 1 leave (TMA) after the next A barrier.
+    const int qd = warp & 3, hf = warp >> 2;
+    float cbv[24];  // CB of this warp's three blocks (same for both heads), loaded once per chunk run
+    PairCursor uw, ue, us;  // pairs k (W), k - 1 (epilogue), k - 2 (y stores)
+    uw.seek(geo, q0, q1);
+    ue = uw;
+    us = uw;
+    int np = 0;  // pairs of this CTA
+    for (PairCursor c = uw; c.a.f < q1; c.next(geo, q1)) ++np;
+    for (int k = 0; k <= np + 1; ++k) {
+      const bool has_w = k < np, has_e = k >= 1 && k - 1 < np, has_s = k >= 2 && k - 2 < np;
+      // ---------------------------------------------------------- A: W' of pair k
+      {
+        const int r = k & 1, sc = k % kSc;
+        if (has_w && uw.a.first(q0)) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          if (jj <= qw) {
-            const float4 v0 = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj));
-            const float4 v1 = __ldg(reinterpret_cast<const float4*>(cbrow + 16 * jj + 4));
-            cbv[8 * jj + 0] = v0.x;
-            cbv[8 * jj + 1] = v0.y;
-            cbv[8 * jj + 2] = v0.z;
-            cbv[8 * jj + 3] = v0.w;
-            cbv[8 * jj + 4] = v1.x;
-            cbv[8 * jj + 5] = v1.y;
-            cbv[8 * jj + 6] = v1.z;
-            cbv[8 * jj + 7] = v1.w;
+          for (int m = 0; m < 3; ++m) {
+            const int bi = (warp + 8 * m) % 10;
+            const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
+            const float* cbrow = prm.CB + ((size_t)uw.a.k * kL + 16 * q + (lane & 15)) * kL + 16 * jj + 8 * (lane >> 4);
+            const float4 c0 = __ldg(reinterpret_cast<const float4*>(cbrow));
+            const float4 c1 = __ldg(reinterpret_cast<const float4*>(cbrow + 4));
+            cbv[8 * m + 0] = c0.x, cbv[8 * m + 1] = c0.y, cbv[8 * m + 2] = c0.z, cbv[8 * m + 3] = c0.w;
+            cbv[8 * m + 4] = c1.x, cbv[8 * m + 5] = c1.y, cbv[8 * m + 6] = c1.z, cbv[8 * m + 7] = c1.w;
           }
         }
-      }
-      bool ok = mbar_wait(&sm.sc_ready[r], ph, status, 209);
-      if (ok && k >= 2) ok = mbar_wait(&sm.mma_done[r], ph ^ 1, status, 210);  // W[r] read by pair k - 2
-      if (named_bar_or(2, 128, !ok)) break;
+        bool ok = true;
+        if (tid == 0 && has_w) {  // one thread waits; the named barrier passes the inputs to the pool
+          ok = mbar_wait(&sm.sc_ready[sc], (k / kSc) & 1, status, 209);
+          if (ok && k >= 2) ok = mbar_wait(&sm.mma_done[r], ((k >> 1) - 1) & 1, status, 210);  // W[r] read by pair k-2
+        }
+        tc_fence_before();
+        fence_proxy_async();  // the epilogue's y tiles for the TMA stores
+        if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
+        if (tid == 0 && has_s) {
+          const int rs = (k - 2) & 1;
+          for (int i = 0; i < us.n; ++i)
+            tma_store_2d(&tm_y, sm.y[rs][i], (us.a.h(geo) + i) * kP, us.a.b * T + us.a.c * kL);
+          tma_store_commit();
+          mbar_arrive(&sm.epi_done[rs]);
+        }
+        if (has_w) {
 #pragma unroll 1
-      for (int i = 0; i < u.n; ++i) {
-        const float ct = sm.cum[r][i][t];
+          for (int m = 0; m < 3; ++m) {
+            const int task = warp + 8 * m;
+            if (task >= 10 * uw.n) break;
+            const int i = task >= 10 ? 1 : 0, bi = task - 10 * i;
+            const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
+            const int hl = lane >> 4, t = 16 * q + (lane & 15), s0 = 16 * jj + 8 * hl;
+            float cb[8], w[8];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          if (jj > qw) break;
-          const int s0 = 16 * jj + 8 * hl;
-          float w[8];
-          if (jj < qw) {
-            const float f = sm.E[r][i][t][jj];
+            for (int e = 0; e < 8; ++e) cb[e] = m == 0 ? cbv[e] : m == 1 ? cbv[8 + e] : cbv[16 + e];
+            if (jj < q) {  // block before the row's block: exp(cum_t - cum_s) dt'_s = E_t[jj] Gd_s
+              const float f = sm.E[sc][i][t][jj];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = cbv[8 * jj + e] * (f * sm.Gd[r][i][s0 + e]);
-          } else {  // the diagonal block, masked before the exponential
+              for (int e = 0; e < 8; ++e) w[e] = cb[e] * (f * sm.Gd[sc][i][s0 + e]);
+            } else {  // the diagonal block, masked before the exponential
+              const float ct = sm.cum[sc][i][t];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int s = s0 + e;
-              w[e] = (s <= t) ? cbv[8 * jj + e] * __expf(fminf(ct - sm.cum[r][i][s], 0.f)) * sm.dtp[r][i][s] : 0.f;
+              for (int e = 0; e < 8; ++e) {
+                const int s2 = s0 + e;
+                w[e] = (s2 <= t) ? cb[e] * __expf(fminf(ct - sm.cum[sc][i][s2], 0.f)) * sm.dtp[sc][i][s2] : 0.f;
+              }
             }
+            store_row_bf16(sm.W[r][i], t, hl + 2 * jj, w, 1);
           }
-          store_row_bf16(sm.W[r][i], t, hl + 2 * jj, w, 1);
         }
       }
-      fence_proxy_async();
-      named_bar(2, 128);
-      if (tid == 32 * kWarpW0) {
-        mbar_arrive(&sm.w_ready[r]);
-        mbar_arrive(&sm.sc_free[r]);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue warps 0-3
-    // Warps 0-1 hold head a's rows (lanes 0-63 of the pair's accumulators, columns 0-63), warps 2-3 head
-    // b's (lanes 64-127, columns 64-127); thread row t = 32 (warp & 1) + lane.
-    const int hi = warp >> 1, t = 32 * (warp & 1) + lane;
-    PairCursor u;
-    u.seek(geo, q0, q1);
-    for (int k = 0; u.a.f < q1; ++k, u.next(geo, q1)) {
-      const int r = k & 1, ph = (k >> 1) & 1;
-      bool ok = mbar_wait(&sm.mma_done[r], ph, status, 211);
-      ok = ok && mbar_wait(&sm.sc_ready[r], ph, status, 212);
-      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // y[r] (pair k-2) read out
-      if (named_bar_or(1, 128, !ok)) break;
-      tc_fence_after();
-      if (hi < u.n) {
-        const float ec = sm.ecum[r][hi][t];
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t vd[32], vo[32];
-          tmem_ld32_nowait(taddr(TYD(r), 32 * warp, 64 * hi + 32 * hf), vd);
-          tmem_ld32_nowait(taddr(TYO(r), 32 * warp, 64 * hi + 32 * hf), vo);
-          tmem_wait_ld();
-          float yv[32];
+      // ---------------------------------------------------------- B: epilogue of pair k - 1
+      {
+        const int re = (k - 1) & 1, se = (k - 1) % kSc;
+        bool ok = true;
+        if (tid == 0 && has_e) ok = mbar_wait(&sm.mma_done[re], ((k - 1) >> 1) & 1, status, 211);
+        // the y tiles of pair k - 3 (same staging slot) have been read by their stores
+        if (tid == 0 && k >= 3) tma_store_wait_read0();
+        fence_proxy_async();  // W' of pair k for the y_diag MMAs
+        if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
+        if (tid == 0 && has_w) mbar_arrive(&sm.w_ready[k & 1]);
+        if (has_e) {
+          tc_fence_after();
+          const int hi = qd >> 1, t = 32 * (qd & 1) + lane;
+          if (hi < ue.n) {
+            const float ec = sm.ecum[se][hi][t];
+            uint32_t vd[32], vo[32];
+            tmem_ld32_nowait(taddr(TYD(re), 32 * qd, 64 * hi + 32 * hf), vd);
+            tmem_ld32_nowait(taddr(TYO(re), 32 * qd, 64 * hi + 32 * hf), vo);
+            tmem_wait_ld();
+            float yv[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) yv[e] = __uint_as_float(vd[e]) + ec * __uint_as_float(vo[e]);
-          store_row_bf16(sm.y[r][hi], t, 4 * hf, yv, 4);
+            for (int e = 0; e < 32; ++e) yv[e] = __uint_as_float(vd[e]) + ec * __uint_as_float(vo[e]);
+            store_row_bf16(sm.y[re][hi], t, 4 * hf, yv, 4);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.sc_free[se]);  // the pair's last scalar reader
         }
       }
-      tc_fence_before();
-      fence_proxy_async();
-      named_bar(1, 128);
-      if (tid == 0) {
-        for (int i = 0; i < u.n; ++i) tma_store_2d(&tm_y, sm.y[r][i], (u.a.h(geo) + i) * kP, u.a.b * T + u.a.c * kL);
-        tma_store_commit();
-        mbar_arrive(&sm.epi_done[r]);
-        mbar_arrive(&sm.sc_free[r]);
-      }
+      if (has_s) us.next(geo, q1);
+      if (has_e) ue.next(geo, q1);
+      if (has_w) uw.next(geo, q1);
     }
     if (tid == 0) tma_store_wait0();
   }
