@@ -39,9 +39,11 @@ namespace {
 using namespace tc;
 
 constexpr int kL = 64, kP = 64, kN = 128;
-constexpr int kThreads = 352;
-constexpr int kPoolWarps = 8, kPoolThreads = 32 * kPoolWarps;
-constexpr int kWarpScal = 8, kWarpTma = 9, kWarpMma = 10;
+constexpr int kPoolWarps = 16, kPoolThreads = 32 * kPoolWarps;
+constexpr int kWarpScal = kPoolWarps, kWarpTma = kPoolWarps + 1, kWarpMma = kPoolWarps + 2;
+constexpr int kTasks = (20 + kPoolWarps - 1) / kPoolWarps;  // W' blocks per pool warp (20 per pair)
+constexpr int kEpiCols = 64 / (kPoolWarps / 4);             // epilogue columns per pool warp
+constexpr int kThreads = 32 * (kPoolWarps + 3);
 constexpr int kBarPool = 1;  // named barrier of the pool
 constexpr int kSc = 4;       // K1 scalar ring (pairs): read by W of pair k and the epilogue of pair k a phase later
 constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
@@ -72,6 +74,10 @@ struct FwdcParams {
   int T, H, G, hpg, nc;
   int total;  // items b * nc * G * hpg (< 2^31)
 };
+
+// 16 or 32 TMEM columns of this warp's lanes, without the wait.
+__device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[16]) { tmem_ld16_nowait(a, r); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t a, uint32_t (&r)[32]) { tmem_ld32_nowait(a, r); }
 
 // Walks a CTA's items in units of one or two heads of the same chunk.
 struct PairCursor {
@@ -235,14 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.sc_ready[r]);
     }
   } else if (warp < kPoolWarps) {
-    // ------------------------------------------------------------ the pool (warps 0-7).  Iteration k:
+    // ------------------------------------------------------------ the pool (warps 0 .. kPoolWarps-1).
+    //   Iteration k:
     //   A  W' of pair k: 20 blocks of 16 x 16 (two heads x the ten blocks at or left of the diagonal),
-    //      warp w takes blocks w, w + 8, w + 16 (the other warps' blocks of the same head are independent)
+    //      warp w takes blocks w, w + kPoolWarps, ...
     //   B  epilogue of pair k - 1: y = y_diag + exp(cum) y_off; warp w reads TMEM lanes 32 (w % 4) ..
-    //      (head w % 4 / 2) and columns 32 (w / 4) .. of that head
+    //      (head w % 4 / 2) and kEpiCols columns from kEpiCols (w / 4) of that head
     // The y tiles of pair k - 1 leave (TMA) after the next A barrier.
     const int qd = warp & 3, hf = warp >> 2;
-    float cbv[24];  // CB of this warp's three blocks (same for both heads), loaded once per chunk run
+    float cbv[8 * kTasks];  // CB of this warp's blocks (same for both heads), loaded once per chunk run
     PairCursor uw, ue, us;  // pairs k (W), k - 1 (epilogue), k - 2 (y stores)
     uw.seek(geo, q0, q1);
     ue = uw;
@@ -256,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = k & 1, sc = k % kSc;
         if (has_w && uw.a.first(q0)) {
 #pragma unroll
-          for (int m = 0; m < 3; ++m) {
-            const int bi = (warp + 8 * m) % 10;
+          for (int m = 0; m < kTasks; ++m) {
+            const int bi = (warp + kPoolWarps * m) % 10;
             const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
             const float* cbrow = prm.CB + ((size_t)uw.a.k * kL + 16 * q + (lane & 15)) * kL + 16 * jj + 8 * (lane >> 4);
             const float4 c0 = __ldg(reinterpret_cast<const float4*>(cbrow));
@@ -283,15 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (has_w) {
 #pragma unroll 1
-          for (int m = 0; m < 3; ++m) {
-            const int task = warp + 8 * m;
+          for (int m = 0; m < kTasks; ++m) {
+            const int task = warp + kPoolWarps * m;
             if (task >= 10 * uw.n) break;
             const int i = task >= 10 ? 1 : 0, bi = task - 10 * i;
             const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
             const int hl = lane >> 4, t = 16 * q + (lane & 15), s0 = 16 * jj + 8 * hl;
             float cb[8], w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) cb[e] = m == 0 ? cbv[e] : m == 1 ? cbv[8 + e] : cbv[16 + e];
+            for (int e = 0; e < 8; ++e) cb[e] = (kTasks < 2 || m == 0) ? cbv[e] : (kTasks < 3 || m == 1) ? cbv[8 * (kTasks > 1) + e] : cbv[8 * (kTasks - 1) + e];
             if (jj < q) {  // block before the row's block: exp(cum_t - cum_s) dt'_s = E_t[jj] Gd_s
               const float f = sm.E[sc][i][t][jj];
 #pragma unroll
@@ -323,14 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int hi = qd >> 1, t = 32 * (qd & 1) + lane;
           if (hi < ue.n) {
             const float ec = sm.ecum[se][hi][t];
-            uint32_t vd[32], vo[32];
-            tmem_ld32_nowait(taddr(TYD(re), 32 * qd, 64 * hi + 32 * hf), vd);
-            tmem_ld32_nowait(taddr(TYO(re), 32 * qd, 64 * hi + 32 * hf), vo);
+            uint32_t vd[kEpiCols], vo[kEpiCols];
+            tmem_ld_cols(taddr(TYD(re), 32 * qd, 64 * hi + kEpiCols * hf), vd);
+            tmem_ld_cols(taddr(TYO(re), 32 * qd, 64 * hi + kEpiCols * hf), vo);
             tmem_wait_ld();
-            float yv[32];
+            float yv[kEpiCols];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) yv[e] = __uint_as_float(vd[e]) + ec * __uint_as_float(vo[e]);
-            store_row_bf16(sm.y[re][hi], t, 4 * hf, yv, 4);
+            for (int e = 0; e < kEpiCols; ++e) yv[e] = __uint_as_float(vd[e]) + ec * __uint_as_float(vo[e]);
+            store_row_bf16(sm.y[re][hi], t, (kEpiCols / 8) * hf, yv, kEpiCols / 8);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.sc_free[se]);  // the pair's last scalar reader
