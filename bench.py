@@ -23,6 +23,7 @@ import math
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -186,20 +187,34 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            time.sleep(0.5)  # let the sampler start before the timed region
         except OSError:
             self.proc = None
+            return self
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        # nvidia-smi's first query (driver and NVML start-up) can hold up kernel launches for a second
+        # on a fresh machine: the timed region starts only after its first sample has arrived
+        t_end = time.time() + 15.0
+        while not self.lines and self.proc.poll() is None and time.time() < t_end:
+            time.sleep(0.05)
+        time.sleep(0.3)
         return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.lines.append(ln)
 
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+            self.reader.join(timeout=5)
+            self.lines = list(self.lines)
 
     def summary(self):
         rows = []

@@ -58,6 +58,9 @@ using namespace tc;
 constexpr int kL = 64, kP = 64, kN = 128;
 constexpr int kPoolWarps = 16, kPoolThreads = 32 * kPoolWarps;
 constexpr int kWarpScal = 16, kWarpMma = 17, kWarpTma = 18;
+// The pool thread that waits on the mbarriers and issues the dx stores: lane 0 of warp 15, an E warp (row and
+// column block 3) on the one scheduler that hosts no other role
+constexpr int kLead = 32 * 15;
 constexpr int kThreads = 32 * 19;
 constexpr int kBarPool = 1;  // named barrier of the pool
 constexpr int kEWarps = 10;  // pool warps w with w / 4 <= w % 4: one (row block w % 4, column block w / 4) each
@@ -364,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool run_end = has_prev && co.last(geo, q1);
         // one thread waits for the phase's inputs; the named barrier passes them to the pool
         bool ok = true;
-        if (tid == 0 && has_prev) ok = mbar_wait(&sm.s2_done[jp], (ip >> 1) & 1, status, 121);
-        if (tid == 0 && ok && run_end) ok = mbar_wait(&sm.acc_full, (seg_o + 1) & 1, status, 122);
+        if (tid == kLead && has_prev) ok = mbar_wait(&sm.s2_done[jp], (ip >> 1) & 1, status, 121);
+        if (tid == kLead && ok && run_end) ok = mbar_wait(&sm.acc_full, (seg_o + 1) & 1, status, 122);
         if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
         tc_fence_after();
         if (has_prev) {
@@ -429,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int in = i + 1, jn = in & 1, kn = in & 3;
         bool ok = true;
-        if (tid == 0 && has_next) {
+        if (tid == kLead && has_next) {
           ok = mbar_wait(&sm.sc_ready[kn], (in >> 2) & 1, status, 110);
           ok = ok && mbar_wait(&sm.xy_full[in % 3], (in / 3) & 1, status, 111);
           if (ok && in >= 2) ok = mbar_wait(&sm.s1b_done[jn], ((in >> 1) - 1) & 1, status, 112);  // 1b(i-1) read dch, dvd
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         fence_proxy_async();
         if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
-        if (tid == 0 && has_prev) {
+        if (tid == kLead && has_prev) {
           tma_store_2d(&tm_dx, sm.dxs, co.h(geo) * kP, co.b * T + co.c * kL);
           tma_store_commit();
           mbar_arrive(&sm.tmem_free[(i - 1) & 1]);
@@ -478,16 +481,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int k4w = (warp == 8 || warp == 9 || warp == 12 || warp == 13) ? 2 * ((warp >> 2) - 2) + (warp & 1) : -1;
         bool ok = true;
-        if (tid == 0 && has_cur) {
+        if (tid == kLead && has_cur) {
           ok = mbar_wait(&sm.sd_full[j], (i >> 1) & 1, status, 127);  // K4
           ok = ok && mbar_wait(&sm.s1a_done[j], (i >> 1) & 1, status, 117);
           // the bf16 dCB sum of the previous run must have been read by its MMAs
-          // (thread 0 is in an E warp, so seg_e counts its runs)
+          // (the waiting thread is in an E warp, so seg_e counts its runs)
           if (ok && last && seg_e >= 1) ok = mbar_wait(&sm.chunk_empty, (seg_e - 1) & 1, status, 126);
         }
         fence_proxy_async();
         if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
-        if (tid == 0 && has_next) mbar_arrive(&sm.pre_done[(i + 1) & 1]);
+        if (tid == kLead && has_next) mbar_arrive(&sm.pre_done[(i + 1) & 1]);
         if (has_cur && e_warp) {
           tc_fence_after();
           // W, the run's dCB sum and the ORANGE row sums of block (qd, gi): rows t = 16 qd + (lane & 15),
@@ -581,12 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&sm.sc_free[kp]);
         }
         // the dx store of this iteration has been read before the next S1 writes the staging tile
-        if (tid == 0 && has_prev) tma_store_wait_read0();
+        if (tid == kLead && has_prev) tma_store_wait_read0();
       }
       if (has_prev) co.next(geo);
       if (has_cur) ce.next(geo);
     }
-    if (tid == 0) tma_store_wait0();
+    if (tid == kLead) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();

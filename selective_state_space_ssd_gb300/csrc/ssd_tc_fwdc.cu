@@ -45,6 +45,9 @@ constexpr int kTasks = (20 + kPoolWarps - 1) / kPoolWarps;  // W' blocks per poo
 constexpr int kEpiCols = 64 / (kPoolWarps / 4);             // epilogue columns per pool warp
 constexpr int kThreads = 32 * (kPoolWarps + 3);
 constexpr int kBarPool = 1;  // named barrier of the pool
+// The pool thread that waits on the mbarriers and issues the y stores: lane 0 of the last pool warp, which has one
+// W' block (the first warps have two) and shares its scheduler with no other role
+constexpr int kLead = 32 * (kPoolWarps - 1);
 constexpr int kSc = 4;       // K1 scalar ring (pairs): read by W of pair k and the epilogue of pair k a phase later
 constexpr uint32_t kTileLP = kL * kP * 2;  // 8 KB
 constexpr uint32_t kTileNP = kN * kP * 2;  // 16 KB
@@ -274,14 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         bool ok = true;
-        if (tid == 0 && has_w) {  // one thread waits; the named barrier passes the inputs to the pool
+        if (tid == kLead && has_w) {  // one thread waits; the named barrier passes the inputs to the pool
           ok = mbar_wait(&sm.sc_ready[sc], (k / kSc) & 1, status, 209);
           if (ok && k >= 2) ok = mbar_wait(&sm.mma_done[r], ((k >> 1) - 1) & 1, status, 210);  // W[r] read by pair k-2
         }
         tc_fence_before();
         fence_proxy_async();  // the epilogue's y tiles for the TMA stores
         if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
-        if (tid == 0 && has_s) {
+        if (tid == kLead && has_s) {
           const int rs = (k - 2) & 1;
           for (int i = 0; i < us.n; ++i)
             tma_store_2d(&tm_y, sm.y[rs][i], (us.a.h(geo) + i) * kP, us.a.b * T + us.a.c * kL);
@@ -319,12 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int re = (k - 1) & 1, se = (k - 1) % kSc;
         bool ok = true;
-        if (tid == 0 && has_e) ok = mbar_wait(&sm.mma_done[re], ((k - 1) >> 1) & 1, status, 211);
+        if (tid == kLead && has_e) ok = mbar_wait(&sm.mma_done[re], ((k - 1) >> 1) & 1, status, 211);
         // the y tiles of pair k - 3 (same staging slot) have been read by their stores
-        if (tid == 0 && k >= 3) tma_store_wait_read0();
+        if (tid == kLead && k >= 3) tma_store_wait_read0();
         fence_proxy_async();  // W' of pair k for the y_diag MMAs
         if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
-        if (tid == 0 && has_w) mbar_arrive(&sm.w_ready[k & 1]);
+        if (tid == kLead && has_w) mbar_arrive(&sm.w_ready[k & 1]);
         if (has_e) {
           tc_fence_after();
           const int hi = qd >> 1, t = 32 * (qd & 1) + lane;
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (has_e) ue.next(geo, q1);
       if (has_w) uw.next(geo, q1);
     }
-    if (tid == 0) tma_store_wait0();
+    if (tid == kLead) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();
