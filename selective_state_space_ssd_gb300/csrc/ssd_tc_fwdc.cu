@@ -21,12 +21,19 @@
 // is not stored).  The work items and the persistent grid are those of
 // tc_items.cuh; two pairs are in flight.
 //
-// Warp roles (352 threads):
-//   warps 0-3   epilogue: y = y_diag + exp(cum) y_off -> bf16 tiles -> TMA stores
-//   warps 4-7   W' tiles (CB of the chunk run in registers)
-//   warp 8      K1 scalars: softplus, in-chunk cumsum, decay factors
-//   warp 9      TMA producer (C per chunk run, twice; x and S_c per head)
-//   warp 10     MMA issuer and TMEM owner
+// Warp roles (608 threads):
+//   warps 0-15  the pool, one named barrier per pair k, after which every warp runs
+//                    W' tiles of pair k: twenty 16 x 16 blocks (two heads x the ten blocks
+//                    at or left of the diagonal), block w and w + 16 on warp w, CB of the
+//                    chunk run in registers, and then
+//                    the epilogue of pair k-2: y = y_diag + exp(cum) y_off -> bf16 tiles,
+//                    warp w on TMEM lane quadrant w % 4 and 16 columns;
+//               the barrier hands W' of pair k-1 to its MMAs (which run during iteration k)
+//               and the y tiles of pair k-3 to their TMA stores; one pool thread waits on
+//               the mbarriers for the whole pool
+//   warp 16     K1 scalars: softplus, in-chunk cumsum, decay factors (up to four pairs ahead)
+//   warp 17     TMA producer (C per chunk run, twice; x and S_c per head)
+//   warp 18     MMA issuer and TMEM owner
 // Every wait is bounded; on a timeout the kernel records a code in the
 // workspace status word and stops.
 #include "ssd_device.cuh"
@@ -201,18 +208,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sm.drain, 0, status, 207);
     }
   } else if (warp == kWarpScal) {
-    // ------------------------------------------------------------ K1 scalars, up to kSc pairs ahead
+    // ------------------------------------------------------------ K1 scalars, up to kSc pairs ahead.  The
+    //   strided dt_raw reads (and A) of a pair are issued two pairs before its turn: one pair's worth of
+    //   global-memory latency per pair would otherwise set the pace of the whole CTA.
     const int t0 = 2 * lane, t1 = t0 + 1;
-    PairCursor u;
+    struct Raw {
+      float z00, z01, z10, z11, a0, a1;  // dt_raw of rows t0, t1 and A, heads 0 and 1 of the pair
+    };
+    auto fetch = [&](const PairCursor& c, Raw& w) {
+      if (c.a.f >= q1) return;
+      const int h0 = c.a.h(geo);
+      const size_t rr = (size_t)c.a.b * T + c.a.c * kL + t0;
+      w.z00 = __ldcs(prm.dt_raw + rr * H + h0);
+      w.z01 = __ldcs(prm.dt_raw + (rr + 1) * H + h0);
+      w.a0 = __ldg(prm.A + h0);
+      if (c.n > 1) {
+        w.z10 = __ldcs(prm.dt_raw + rr * H + h0 + 1);
+        w.z11 = __ldcs(prm.dt_raw + (rr + 1) * H + h0 + 1);
+        w.a1 = __ldg(prm.A + h0 + 1);
+      }
+    };
+    PairCursor u, u1, u2;  // pairs k, k + 1, k + 2
     u.seek(geo, q0, q1);
-    for (int k = 0; u.a.f < q1; ++k, u.next(geo, q1)) {
+    u1 = u;
+    if (u1.a.f < q1) u1.next(geo, q1);
+    u2 = u1;
+    if (u2.a.f < q1) u2.next(geo, q1);
+    Raw w0{}, w1{}, w2{};
+    fetch(u, w0);
+    fetch(u1, w1);
+    fetch(u2, w2);
+    for (int k = 0; u.a.f < q1; ++k) {
       const int r = k % kSc;
       if (k >= kSc && !mbar_wait(&sm.sc_free[r], (k / kSc - 1) & 1, status, 208)) break;
+#pragma unroll 1
       for (int i = 0; i < u.n; ++i) {
-        const int h = u.a.h(geo) + i;
-        const float A_h = prm.A[h];
-        const size_t rr = (size_t)u.a.b * T + u.a.c * kL + t0;
-        const float d0 = softplus_fast(__ldcs(prm.dt_raw + rr * H + h)), d1 = softplus_fast(__ldcs(prm.dt_raw + (rr + 1) * H + h));
+        const float A_h = i ? w0.a1 : w0.a0;
+        const float d0 = softplus_fast(i ? w0.z10 : w0.z00), d1 = softplus_fast(i ? w0.z11 : w0.z01);
         const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
         float inc = a1;
 #pragma unroll
@@ -242,109 +274,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sc_ready[r]);
+      w0 = w1;
+      w1 = w2;
+      u = u1;
+      u1 = u2;
+      if (u2.a.f < q1) {
+        u2.next(geo, q1);
+        fetch(u2, w2);
+      }
     }
   } else if (warp < kPoolWarps) {
     // ------------------------------------------------------------ the pool (warps 0 .. kPoolWarps-1).
-    //   Iteration k:
-    //   A  W' of pair k: 20 blocks of 16 x 16 (two heads x the ten blocks at or left of the diagonal),
-    //      warp w takes blocks w, w + kPoolWarps, ...
-    //   B  epilogue of pair k - 1: y = y_diag + exp(cum) y_off; warp w reads TMEM lanes 32 (w % 4) ..
-    //      (head w % 4 / 2) and kEpiCols columns from kEpiCols (w / 4) of that head
-    // The y tiles of pair k - 1 leave (TMA) after the next A barrier.
+    //   Iteration k, after one barrier:
+    //     W' of pair k: 20 blocks of 16 x 16 (two heads x the ten blocks at or left of the diagonal),
+    //       warp w takes blocks w, w + kPoolWarps, ...
+    //     epilogue of pair k - 2: y = y_diag + exp(cum) y_off; warp w reads TMEM lanes 32 (w % 4) ..
+    //       (head w % 4 / 2) and kEpiCols columns from kEpiCols (w / 4) of that head
+    //   The barrier releases W' of pair k - 1 to its y_diag MMAs and the y tiles of pair k - 3 to their
+    //   TMA stores; the MMAs of pair k - 1 run during iteration k, one iteration before their epilogue.
     const int qd = warp & 3, hf = warp >> 2;
     float cbv[8 * kTasks];  // CB of this warp's blocks (same for both heads), loaded once per chunk run
-    PairCursor uw, ue, us;  // pairs k (W), k - 1 (epilogue), k - 2 (y stores)
+    PairCursor uw, ue, us;  // pairs k (W), k - 2 (epilogue), k - 3 (y stores)
     uw.seek(geo, q0, q1);
     ue = uw;
     us = uw;
     int np = 0;  // pairs of this CTA
     for (PairCursor c = uw; c.a.f < q1; c.next(geo, q1)) ++np;
-    for (int k = 0; k <= np + 1; ++k) {
-      const bool has_w = k < np, has_e = k >= 1 && k - 1 < np, has_s = k >= 2 && k - 2 < np;
-      // ---------------------------------------------------------- A: W' of pair k
-      {
-        const int r = k & 1, sc = k % kSc;
-        if (has_w && uw.a.first(q0)) {
+    for (int k = 0; k <= np + 2; ++k) {
+      const bool has_w = k < np, has_r = k >= 1 && k - 1 < np, has_e = k >= 2 && k - 2 < np,
+                 has_s = k >= 3 && k - 3 < np;
+      const int r = k & 1, sc = k % kSc;
+      if (has_w && uw.a.first(q0)) {
 #pragma unroll
-          for (int m = 0; m < kTasks; ++m) {
-            const int bi = (warp + kPoolWarps * m) % 10;
-            const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
-            const float* cbrow = prm.CB + ((size_t)uw.a.k * kL + 16 * q + (lane & 15)) * kL + 16 * jj + 8 * (lane >> 4);
-            const float4 c0 = __ldg(reinterpret_cast<const float4*>(cbrow));
-            const float4 c1 = __ldg(reinterpret_cast<const float4*>(cbrow + 4));
-            cbv[8 * m + 0] = c0.x, cbv[8 * m + 1] = c0.y, cbv[8 * m + 2] = c0.z, cbv[8 * m + 3] = c0.w;
-            cbv[8 * m + 4] = c1.x, cbv[8 * m + 5] = c1.y, cbv[8 * m + 6] = c1.z, cbv[8 * m + 7] = c1.w;
-          }
+        for (int m = 0; m < kTasks; ++m) {
+          const int bi = (warp + kPoolWarps * m) % 10;
+          const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
+          const float* cbrow = prm.CB + ((size_t)uw.a.k * kL + 16 * q + (lane & 15)) * kL + 16 * jj + 8 * (lane >> 4);
+          const float4 c0 = __ldg(reinterpret_cast<const float4*>(cbrow));
+          const float4 c1 = __ldg(reinterpret_cast<const float4*>(cbrow + 4));
+          cbv[8 * m + 0] = c0.x, cbv[8 * m + 1] = c0.y, cbv[8 * m + 2] = c0.z, cbv[8 * m + 3] = c0.w;
+          cbv[8 * m + 4] = c1.x, cbv[8 * m + 5] = c1.y, cbv[8 * m + 6] = c1.z, cbv[8 * m + 7] = c1.w;
         }
-        bool ok = true;
-        if (tid == kLead && has_w) {  // one thread waits; the named barrier passes the inputs to the pool
-          ok = mbar_wait(&sm.sc_ready[sc], (k / kSc) & 1, status, 209);
-          if (ok && k >= 2) ok = mbar_wait(&sm.mma_done[r], ((k >> 1) - 1) & 1, status, 210);  // W[r] read by pair k-2
-        }
-        tc_fence_before();
-        fence_proxy_async();  // the epilogue's y tiles for the TMA stores
-        if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
-        if (tid == kLead && has_s) {
-          const int rs = (k - 2) & 1;
+      }
+      bool ok = true;
+      if (tid == kLead) {  // one thread waits; the named barrier passes the inputs to the pool
+        if (has_w) ok = mbar_wait(&sm.sc_ready[sc], (k / kSc) & 1, status, 209);
+        // pair k - 2's MMAs are done: W[r] may be rewritten and its y read out of TMEM
+        if (ok && k >= 2 && k - 2 < np) ok = mbar_wait(&sm.mma_done[r], ((k >> 1) - 1) & 1, status, 210);
+        if (k >= 4) tma_store_wait_read0();  // the y tiles of pair k - 4 (pair k - 2's staging slot) are read
+      }
+      tc_fence_before();
+      fence_proxy_async();  // W' of pair k - 1 for its MMAs; the y tiles of pair k - 3 for their stores
+      if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
+      if (tid == kLead) {
+        if (has_r) mbar_arrive(&sm.w_ready[(k - 1) & 1]);
+        if (has_s) {
+          const int rs = (k - 3) & 1;
           for (int i = 0; i < us.n; ++i)
             tma_store_2d(&tm_y, sm.y[rs][i], (us.a.h(geo) + i) * kP, us.a.b * T + us.a.c * kL);
           tma_store_commit();
-          mbar_arrive(&sm.epi_done[rs]);
-        }
-        if (has_w) {
-#pragma unroll 1
-          for (int m = 0; m < kTasks; ++m) {
-            const int task = warp + kPoolWarps * m;
-            if (task >= 10 * uw.n) break;
-            const int i = task >= 10 ? 1 : 0, bi = task - 10 * i;
-            const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
-            const int hl = lane >> 4, t = 16 * q + (lane & 15), s0 = 16 * jj + 8 * hl;
-            float cb[8], w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) cb[e] = (kTasks < 2 || m == 0) ? cbv[e] : (kTasks < 3 || m == 1) ? cbv[8 * (kTasks > 1) + e] : cbv[8 * (kTasks - 1) + e];
-            if (jj < q) {  // block before the row's block: exp(cum_t - cum_s) dt'_s = E_t[jj] Gd_s
-              const float f = sm.E[sc][i][t][jj];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) w[e] = cb[e] * (f * sm.Gd[sc][i][s0 + e]);
-            } else {  // the diagonal block, masked before the exponential
-              const float ct = sm.cum[sc][i][t];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int s2 = s0 + e;
-                w[e] = (s2 <= t) ? cb[e] * __expf(fminf(ct - sm.cum[sc][i][s2], 0.f)) * sm.dtp[sc][i][s2] : 0.f;
-              }
-            }
-            store_row_bf16(sm.W[r][i], t, hl + 2 * jj, w, 1);
-          }
+          mbar_arrive(&sm.epi_done[rs]);  // pair k - 3's TMEM slot was read out in the last iteration
         }
       }
-      // ---------------------------------------------------------- B: epilogue of pair k - 1
-      {
-        const int re = (k - 1) & 1, se = (k - 1) % kSc;
-        bool ok = true;
-        if (tid == kLead && has_e) ok = mbar_wait(&sm.mma_done[re], ((k - 1) >> 1) & 1, status, 211);
-        // the y tiles of pair k - 3 (same staging slot) have been read by their stores
-        if (tid == kLead && k >= 3) tma_store_wait_read0();
-        fence_proxy_async();  // W' of pair k for the y_diag MMAs
-        if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
-        if (tid == kLead && has_w) mbar_arrive(&sm.w_ready[k & 1]);
-        if (has_e) {
-          tc_fence_after();
-          const int hi = qd >> 1, t = 32 * (qd & 1) + lane;
-          if (hi < ue.n) {
-            const float ec = sm.ecum[se][hi][t];
-            uint32_t vd[kEpiCols], vo[kEpiCols];
-            tmem_ld_cols(taddr(TYD(re), 32 * qd, 64 * hi + kEpiCols * hf), vd);
-            tmem_ld_cols(taddr(TYO(re), 32 * qd, 64 * hi + kEpiCols * hf), vo);
-            tmem_wait_ld();
-            float yv[kEpiCols];
+      if (has_w) {
+#pragma unroll 1
+        for (int m = 0; m < kTasks; ++m) {
+          const int task = warp + kPoolWarps * m;
+          if (task >= 10 * uw.n) break;
+          const int i = task >= 10 ? 1 : 0, bi = task - 10 * i;
+          const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
+          const int hl = lane >> 4, t = 16 * q + (lane & 15), s0 = 16 * jj + 8 * hl;
+          float cb[8], w[8];
 #pragma unroll
-            for (int e = 0; e < kEpiCols; ++e) yv[e] = __uint_as_float(vd[e]) + ec * __uint_as_float(vo[e]);
-            store_row_bf16(sm.y[re][hi], t, (kEpiCols / 8) * hf, yv, kEpiCols / 8);
+          for (int e = 0; e < 8; ++e) cb[e] = (kTasks < 2 || m == 0) ? cbv[e] : (kTasks < 3 || m == 1) ? cbv[8 * (kTasks > 1) + e] : cbv[8 * (kTasks - 1) + e];
+          if (jj < q) {  // block before the row's block: exp(cum_t - cum_s) dt'_s = E_t[jj] Gd_s
+            const float f = sm.E[sc][i][t][jj];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = cb[e] * (f * sm.Gd[sc][i][s0 + e]);
+          } else {  // the diagonal block, masked before the exponential
+            const float ct = sm.cum[sc][i][t];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int s2 = s0 + e;
+              w[e] = (s2 <= t) ? cb[e] * __expf(fminf(ct - sm.cum[sc][i][s2], 0.f)) * sm.dtp[sc][i][s2] : 0.f;
+            }
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.sc_free[se]);  // the pair's last scalar reader
+          store_row_bf16(sm.W[r][i], t, hl + 2 * jj, w, 1);
         }
+      }
+      if (has_e) {
+        const int re = (k - 2) & 1, se = (k - 2) % kSc;
+        tc_fence_after();
+        const int hi = qd >> 1, t = 32 * (qd & 1) + lane;
+        if (hi < ue.n) {
+          const float ec = sm.ecum[se][hi][t];
+          uint32_t vd[kEpiCols], vo[kEpiCols];
+          tmem_ld_cols(taddr(TYD(re), 32 * qd, 64 * hi + kEpiCols * hf), vd);
+          tmem_ld_cols(taddr(TYO(re), 32 * qd, 64 * hi + kEpiCols * hf), vo);
+          tmem_wait_ld();
+          float yv[kEpiCols];
+#pragma unroll
+          for (int e = 0; e < kEpiCols; ++e) yv[e] = __uint_as_float(vd[e]) + ec * __uint_as_float(vo[e]);
+          store_row_bf16(sm.y[re][hi], t, (kEpiCols / 8) * hf, yv, kEpiCols / 8);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sc_free[se]);  // the pair's last scalar reader
       }
       if (has_s) us.next(geo, q1);
       if (has_e) ue.next(geo, q1);
