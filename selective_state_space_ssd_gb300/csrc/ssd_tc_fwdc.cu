@@ -24,8 +24,8 @@
 // Warp roles (608 threads):
 //   warps 0-15  the pool, one named barrier per pair k, after which every warp runs
 //                    W' tiles of pair k: twenty 16 x 16 blocks (two heads x the ten blocks
-//                    at or left of the diagonal), block w and w + 16 on warp w, CB of the
-//                    chunk run in registers, and then
+//                    at or left of the diagonal): the eight diagonal blocks on warps 0-7, the
+//                    twelve others on warps 8-15, CB of the chunk run in registers, and then
 //                    the epilogue of pair k-2: y = y_diag + exp(cum) y_off -> bf16 tiles,
 //                    warp w on TMEM lane quadrant w % 4 and 16 columns;
 //               the barrier hands W' of pair k-1 to its MMAs (which run during iteration k)
@@ -48,7 +48,6 @@ using namespace tc;
 constexpr int kL = 64, kP = 64, kN = 128;
 constexpr int kPoolWarps = 16, kPoolThreads = 32 * kPoolWarps;
 constexpr int kWarpScal = kPoolWarps, kWarpTma = kPoolWarps + 1, kWarpMma = kPoolWarps + 2;
-constexpr int kTasks = (20 + kPoolWarps - 1) / kPoolWarps;  // W' blocks per pool warp (20 per pair)
 constexpr int kEpiCols = 64 / (kPoolWarps / 4);             // epilogue columns per pool warp
 constexpr int kThreads = 32 * (kPoolWarps + 3);
 constexpr int kBarPool = 1;  // named barrier of the pool
@@ -287,13 +286,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ the pool (warps 0 .. kPoolWarps-1).
     //   Iteration k, after one barrier:
     //     W' of pair k: 20 blocks of 16 x 16 (two heads x the ten blocks at or left of the diagonal),
-    //       warp w takes blocks w, w + kPoolWarps, ...
+    //       split by kind between the warps (below)
     //     epilogue of pair k - 2: y = y_diag + exp(cum) y_off; warp w reads TMEM lanes 32 (w % 4) ..
     //       (head w % 4 / 2) and kEpiCols columns from kEpiCols (w / 4) of that head
     //   The barrier releases W' of pair k - 1 to its y_diag MMAs and the y tiles of pair k - 3 to their
     //   TMA stores; the MMAs of pair k - 1 run during iteration k, one iteration before their epilogue.
     const int qd = warp & 3, hf = warp >> 2;
-    float cbv[8 * kTasks];  // CB of this warp's blocks (same for both heads), loaded once per chunk run
+    // W' blocks of a pair: the eight diagonal blocks (masked exponentials) on warps 0-7, one each; the twelve
+    // blocks left of the diagonal (two products from the scalar tables) two each on warps 8-11 and one on
+    // warps 12-15 (which compute theirs twice, so that every off-diagonal warp runs one straight-line path)
+    const bool wdiag = warp < 8;
+    int ti[2], tq[2], tj[2];
+    if (wdiag) {
+      ti[0] = ti[1] = warp >> 2;
+      tq[0] = tq[1] = tj[0] = tj[1] = warp & 3;
+    } else {
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int o = warp < 12 ? 2 * (warp - 8) + m : warp - 4;  // 0 .. 11: head o / 6, block o % 6
+        const int bo = o % 6;
+        ti[m] = o / 6;
+        tq[m] = bo < 1 ? 1 : bo < 3 ? 2 : 3;
+        tj[m] = bo < 1 ? 0 : bo < 3 ? bo - 1 : bo - 3;
+      }
+    }
+    float cbv[16];  // CB of this warp's blocks (the same for both heads), loaded once per chunk run
     PairCursor uw, ue, us;  // pairs k (W), k - 2 (epilogue), k - 3 (y stores)
     uw.seek(geo, q0, q1);
     ue = uw;
@@ -306,10 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = k & 1, sc = k % kSc;
       if (has_w && uw.a.first(q0)) {
 #pragma unroll
-        for (int m = 0; m < kTasks; ++m) {
-          const int bi = (warp + kPoolWarps * m) % 10;
-          const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
-          const float* cbrow = prm.CB + ((size_t)uw.a.k * kL + 16 * q + (lane & 15)) * kL + 16 * jj + 8 * (lane >> 4);
+        for (int m = 0; m < 2; ++m) {
+          const float* cbrow =
+              prm.CB + ((size_t)uw.a.k * kL + 16 * tq[m] + (lane & 15)) * kL + 16 * tj[m] + 8 * (lane >> 4);
           const float4 c0 = __ldg(reinterpret_cast<const float4*>(cbrow));
           const float4 c1 = __ldg(reinterpret_cast<const float4*>(cbrow + 4));
           cbv[8 * m + 0] = c0.x, cbv[8 * m + 1] = c0.y, cbv[8 * m + 2] = c0.z, cbv[8 * m + 3] = c0.w;
@@ -337,29 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (has_w) {
-#pragma unroll 1
-        for (int m = 0; m < kTasks; ++m) {
-          const int task = warp + kPoolWarps * m;
-          if (task >= 10 * uw.n) break;
-          const int i = task >= 10 ? 1 : 0, bi = task - 10 * i;
-          const int q = bi < 1 ? 0 : bi < 3 ? 1 : bi < 6 ? 2 : 3, jj = bi - q * (q + 1) / 2;
-          const int hl = lane >> 4, t = 16 * q + (lane & 15), s0 = 16 * jj + 8 * hl;
-          float cb[8], w[8];
+        const int hl = lane >> 4;
+        if (wdiag) {  // the diagonal block, masked before the exponential
+          const int i = ti[0], t = 16 * tq[0] + (lane & 15), s0 = 16 * tj[0] + 8 * hl;
+          const float ct = sm.cum[sc][i][t];
+          float w[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) cb[e] = (kTasks < 2 || m == 0) ? cbv[e] : (kTasks < 3 || m == 1) ? cbv[8 * (kTasks > 1) + e] : cbv[8 * (kTasks - 1) + e];
-          if (jj < q) {  // block before the row's block: exp(cum_t - cum_s) dt'_s = E_t[jj] Gd_s
-            const float f = sm.E[sc][i][t][jj];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = cb[e] * (f * sm.Gd[sc][i][s0 + e]);
-          } else {  // the diagonal block, masked before the exponential
-            const float ct = sm.cum[sc][i][t];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int s2 = s0 + e;
-              w[e] = (s2 <= t) ? cb[e] * __expf(fminf(ct - sm.cum[sc][i][s2], 0.f)) * sm.dtp[sc][i][s2] : 0.f;
-            }
+          for (int e = 0; e < 8; ++e) {
+            const int s2 = s0 + e;
+            w[e] = (s2 <= t) ? cbv[e] * __expf(fminf(ct - sm.cum[sc][i][s2], 0.f)) * sm.dtp[sc][i][s2] : 0.f;
           }
-          store_row_bf16(sm.W[r][i], t, hl + 2 * jj, w, 1);
+          store_row_bf16(sm.W[r][i], t, hl + 2 * tj[0], w, 1);
+        } else {  // two blocks left of the diagonal: exp(cum_t - cum_s) dt'_s = E_t[jj] Gd_s
+          const int ta = 16 * tq[0] + (lane & 15), tb = 16 * tq[1] + (lane & 15);
+          const int sa = 16 * tj[0] + 8 * hl, sb = 16 * tj[1] + 8 * hl;
+          const float fa = sm.E[sc][ti[0]][ta][tj[0]], fb = sm.E[sc][ti[1]][tb][tj[1]];
+          float wa[8], wb[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            wa[e] = cbv[e] * (fa * sm.Gd[sc][ti[0]][sa + e]);
+            wb[e] = cbv[8 + e] * (fb * sm.Gd[sc][ti[1]][sb + e]);
+          }
+          store_row_bf16(sm.W[r][ti[0]], ta, hl + 2 * tj[0], wa, 1);
+          store_row_bf16(sm.W[r][ti[1]], tb, hl + 2 * tj[1], wb, 1);
         }
       }
       if (has_e) {
