@@ -75,14 +75,33 @@ __device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t phase) {
       : "memory");
   return done != 0;
 }
-// Bounded wait: gives up after ~2^26 polls (seconds), records `code` in
-// *status and returns false.  The caller then skips its remaining work.  The
-// polling loop is one shared out-of-line copy (kernels with many waits stay
-// small in the instruction cache); a phase that has already completed costs
+// try_wait with an explicit suspend-time hint: a thread whose phase is not complete sleeps until the phase
+// completes or the hint (in ns) runs out, instead of returning after the short default limit and spinning;
+// the spinning waiters of the producer and consumer roles took issue slots from the warps beside them.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t phase, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(phase), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: gives up after two seconds of the global timer, records `code` in *status and returns
+// false.  The caller then skips its remaining work.  The waiting loop is one shared out-of-line copy
+// (kernels with many waits stay small in the instruction cache); a phase that has already completed costs
 // one inline probe.
 static __device__ __noinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t phase, int* status, int code) {
-  for (uint32_t it = 0; it < (1u << 26); ++it)
-    if (mbar_test(bar, phase)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_test_sleep(bar, phase, 1000000u)) return true;
+    if (global_ns() - t0 > 2000000000ull) break;
+  }
   if (status) atomicCAS(status, 0, code);
   return false;
 }
