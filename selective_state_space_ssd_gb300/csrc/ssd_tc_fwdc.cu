@@ -70,6 +70,7 @@ struct alignas(1024) FwdcSmem {
   // than t, exp(cum_t - cum_s) dt'_s = E_t[blk(s)] Gd_s (both exponentials <= 1).
   float cum[kSc][2][kL], ecum[kSc][2][kL], dtp[kSc][2][kL], Gd[kSc][2][kL];
   float E[kSc][2][kL][4];
+  float dtraw[4][2][kL], araw[4][2];  // dt_raw and A of the pairs the scalar warp has in flight (cp.async)
   uint64_t slot_full[2], slot_empty[2], w_ready[2], mma_done[2], epi_done[2], sc_ready[kSc], sc_free[kSc];
   uint64_t chunk_full, chunk_empty, drain;
   uint32_t tmem_slot;
@@ -208,42 +209,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpScal) {
     // ------------------------------------------------------------ K1 scalars, up to kSc pairs ahead.  The
-    //   strided dt_raw reads (and A) of a pair are issued two pairs before its turn: one pair's worth of
-    //   global-memory latency per pair would otherwise set the pace of the whole CTA.
+    //   strided dt_raw reads (and A) of pair k + 3 go out as cp.async copies into a ring while pair k is
+    //   formed: global-memory latency under the kernel's own HBM load (~2 us) would otherwise set the pace
+    //   of the whole CTA.
     const int t0 = 2 * lane, t1 = t0 + 1;
-    struct Raw {
-      float z00, z01, z10, z11, a0, a1;  // dt_raw of rows t0, t1 and A, heads 0 and 1 of the pair
-    };
-    auto fetch = [&](const PairCursor& c, Raw& w) {
-      if (c.a.f >= q1) return;
-      const int h0 = c.a.h(geo);
-      const size_t rr = (size_t)c.a.b * T + c.a.c * kL + t0;
-      w.z00 = __ldcs(prm.dt_raw + rr * H + h0);
-      w.z01 = __ldcs(prm.dt_raw + (rr + 1) * H + h0);
-      w.a0 = __ldg(prm.A + h0);
-      if (c.n > 1) {
-        w.z10 = __ldcs(prm.dt_raw + rr * H + h0 + 1);
-        w.z11 = __ldcs(prm.dt_raw + (rr + 1) * H + h0 + 1);
-        w.a1 = __ldg(prm.A + h0 + 1);
+    auto fetch = [&](const PairCursor& c, int slot) {
+      if (c.a.f < q1) {
+        const int h0 = c.a.h(geo);
+        const size_t rr = (size_t)c.a.b * T + c.a.c * kL + t0;
+        for (int i = 0; i < c.n; ++i) {
+          cp_async4(&sm.dtraw[slot][i][t0], prm.dt_raw + rr * H + h0 + i);
+          cp_async4(&sm.dtraw[slot][i][t1], prm.dt_raw + (rr + 1) * H + h0 + i);
+        }
+        if (lane < c.n) cp_async4(&sm.araw[slot][lane], prm.A + h0 + lane);
       }
+      cp_async_commit();  // one group per pair, empty past the last, so that the count stays uniform
     };
-    PairCursor u, u1, u2;  // pairs k, k + 1, k + 2
+    PairCursor u, uf;  // pairs k (formed) and k + 3 (fetched)
     u.seek(geo, q0, q1);
-    u1 = u;
-    if (u1.a.f < q1) u1.next(geo, q1);
-    u2 = u1;
-    if (u2.a.f < q1) u2.next(geo, q1);
-    Raw w0{}, w1{}, w2{};
-    fetch(u, w0);
-    fetch(u1, w1);
-    fetch(u2, w2);
-    for (int k = 0; u.a.f < q1; ++k) {
-      const int r = k % kSc;
+    uf = u;
+    for (int d = 0; d < 3; ++d) {
+      fetch(uf, d);
+      if (uf.a.f < q1) uf.next(geo, q1);
+    }
+    for (int k = 0; u.a.f < q1; ++k, u.next(geo, q1)) {
+      const int r = k % kSc, sl = k & 3;
+      fetch(uf, (k + 3) & 3);  // the slot pair k - 1 used
+      if (uf.a.f < q1) uf.next(geo, q1);
+      cp_async_wait<3>();  // pair k's copies have landed
+      __syncwarp();
       if (k >= kSc && !mbar_wait(&sm.sc_free[r], (k / kSc - 1) & 1, status, 208)) break;
 #pragma unroll 1
       for (int i = 0; i < u.n; ++i) {
-        const float A_h = i ? w0.a1 : w0.a0;
-        const float d0 = softplus_fast(i ? w0.z10 : w0.z00), d1 = softplus_fast(i ? w0.z11 : w0.z01);
+        const float A_h = sm.araw[sl][i];
+        const float d0 = softplus_fast(sm.dtraw[sl][i][t0]), d1 = softplus_fast(sm.dtraw[sl][i][t1]);
         const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
         float inc = a1;
 #pragma unroll
@@ -273,15 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.sc_ready[r]);
-      w0 = w1;
-      w1 = w2;
-      u = u1;
-      u1 = u2;
-      if (u2.a.f < q1) {
-        u2.next(geo, q1);
-        fetch(u2, w2);
-      }
     }
+    cp_async_wait<0>();
   } else if (warp < kPoolWarps) {
     // ------------------------------------------------------------ the pool (warps 0 .. kPoolWarps-1).
     //   Iteration k, after one barrier:

@@ -109,6 +109,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int* st
   return mbar_test(bar, phase) || mbar_wait_loop(bar, phase, status, code);
 }
 
+// ------------------------------------------------------------ cp.async (per-thread global -> shared copies)
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------ proxies
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
