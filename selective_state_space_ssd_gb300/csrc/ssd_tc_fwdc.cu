@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.slot_empty[r], 1);  // MMA commit
       mbar_init(&sm.w_ready[r], 1);
       mbar_init(&sm.mma_done[r], 1);
-      mbar_init(&sm.epi_done[r], 1);
+      mbar_init(&sm.epi_done[r], kPoolWarps);  // every pool warp once its TMEM reads of the pair are done
     }
     for (int r = 0; r < kSc; ++r) {
       mbar_init(&sm.sc_ready[r], 1);
@@ -341,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < us.n; ++i)
             tma_store_2d(&tm_y, sm.y[rs][i], (us.a.h(geo) + i) * kP, us.a.b * T + us.a.c * kL);
           tma_store_commit();
-          mbar_arrive(&sm.epi_done[rs]);  // pair k - 3's TMEM slot was read out in the last iteration
         }
       }
       if (has_w) {
@@ -380,10 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_cols(taddr(TYD(re), 32 * qd, 64 * hi + kEpiCols * hf), vd);
           tmem_ld_cols(taddr(TYO(re), 32 * qd, 64 * hi + kEpiCols * hf), vo);
           tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.epi_done[re]);  // the next MMAs into this TMEM slot may start
           float yv[kEpiCols];
 #pragma unroll
           for (int e = 0; e < kEpiCols; ++e) yv[e] = __uint_as_float(vd[e]) + ec * __uint_as_float(vo[e]);
           store_row_bf16(sm.y[re][hi], t, (kEpiCols / 8) * hf, yv, kEpiCols / 8);
+        } else if (lane == 0) {
+          mbar_arrive(&sm.epi_done[re]);  // a single-head pair: this warp's lanes hold no live rows
         }
         tc_fence_before();
         __syncwarp();
