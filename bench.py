@@ -367,6 +367,44 @@ def run_ours(args, cfg, rank, world, local_rank):
         a[1] += ms
     launches_per_step = len(recs) / max(1, args.steps)
 
+    # the stashed-states variant (ssd_forward_stash + ssd_backward_stashed: the backward reads the chunk states
+    # the forward kept instead of replaying the state scan), timed the same way; reported beside the
+    # recompute step, which stays the headline
+    stash = None
+    try:
+        nst = binding.ssd_states_size(prob)
+    except binding.SSDError:
+        nst = 0
+    if nst:
+        states = torch.empty(nst, dtype=torch.uint8, device=dev)
+
+        def step_stash(inp, out=out0):
+            binding.ssd_forward_stash(prob, inp["x"], inp["dt_raw"], inp["A"], inp["B"], inp["C"], inp["s0"], out["y"],
+                                      out["s_final"], states, nst, wsf, nf, stream)
+            binding.ssd_backward_stashed(prob, inp["dy"], inp["ds_final"], inp["x"], inp["dt_raw"], inp["A"], inp["B"],
+                                         inp["C"], states, nst, out["dx"], out["ddt_raw"], out["dA"], out["dB"],
+                                         out["dC"], out["ds0"], wsb, nb, stream)
+
+        for _ in range(args.warmup):
+            step_stash(t)
+        barrier()
+        s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.zero_()
+            s_ev[k].record(stream)
+            step_stash(t)
+            e_ev[k].record(stream)
+        barrier()
+        stash_ms = sum(a.elapsed_time(b) for a, b in zip(s_ev, e_ev))
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([stash_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            stash_ms = float(tt.item())
+        del states
+        stash = {"total_ms": stash_ms, "states_bytes": nst}
+
     # end to end through the public API with host buffers (pinned).  Every step copies its inputs in from
     # pinned host memory and all of its outputs back; the copies of neighbouring steps overlap the compute:
     # two device buffer sets, inputs of step k+1 going in and outputs of step k-1 coming out (on their own
@@ -423,7 +461,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     return {"total_ms": total_ms, "step_ms": step_ms, "clocks": clocks, "per_kernel": per,
-            "launches_per_step": launches_per_step, "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "h2d": h2d, "d2h": d2h}
+            "launches_per_step": launches_per_step, "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "h2d": h2d, "d2h": d2h,
+            "stash": stash}
 
 
 def main():
@@ -514,6 +553,12 @@ def main():
             "e2e": {"value": world * tok * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "overlap": "double-buffered: step k+1's inputs in and step k-1's outputs out during step k"}}
+    if r["stash"]:
+        line["stashed_states"] = {
+            "value": world * tok * args.steps / (r["stash"]["total_ms"] / 1e3), "unit": "tokens/s",
+            "ms_per_step": r["stash"]["total_ms"] / args.steps, "states_bytes": r["stash"]["states_bytes"],
+            "what": "ssd_forward_stash + ssd_backward_stashed: the backward reads the forward's chunk states "
+                    "instead of replaying the state scan (same bits); not the headline step, which recomputes"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # about 10 s of oracle work: the whole workload, repeated until 10 s have passed (at most 8 passes)
         v, dt, cores, desc, _, _ = time_oracle(cfg, whole=True, min_seconds=10.0, max_passes=8)

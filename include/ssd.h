@@ -163,6 +163,45 @@ ssd_status ssd_backward(const ssd_problem* prob, const void* dy, const float* ds
                         size_t ws_bytes, void* cuda_stream);
 
 /*
+ * Stashed chunk states: a forward that keeps every chunk-input state S_c for
+ * the backward, and a backward that reads them instead of replaying the
+ * forward scan (the "Two things that are easy to get wrong" section, item 2,
+ * of the "S1-31: SSM_SCAN_BACK" page: the backward needs the states the
+ * forward overwrote; storing all of them is the reference, a cheaper scheme
+ * must give the same bits).  The stash holds the same bf16 tiles the
+ * recompute path writes to its workspace, produced by the same kernel from the
+ * same inputs, so ssd_backward_stashed returns bit for bit what ssd_backward
+ * returns for the same leaf inputs.  It saves the backward one pass of the
+ * state scan (about an eighth of a forward + backward step at the Mamba-2
+ * 2.7B layer shape) for b*H*(T/L)*N*P*2 bytes of device memory held from the
+ * forward to the backward.
+ *
+ * Available where the tensor-core path runs: Mamba-2, bf16 io, chunk 64,
+ * headdim 64, dstate 128 (other problems return SSD_ERR_SHAPE).
+ *
+ * ssd_states_size: bytes of the stash for `prob` (bf16 [b, H, T/L][N][P],
+ *   row-major; tile (b, h, c) is the state entering chunk c, S_0 = s0 rounded
+ *   to bf16).  Host-only.
+ * ssd_forward_stash: ssd_forward, plus the stash written to `states`
+ *   (caller-owned device buffer of at least ssd_states_size bytes, 16-byte
+ *   aligned; a smaller states_bytes returns SSD_ERR_WORKSPACE).  y and s_final
+ *   are bit for bit those of ssd_forward.  ws as for ssd_forward.
+ * ssd_backward_stashed: ssd_backward without s0, reading `states` as written
+ *   by ssd_forward_stash for the same x, dt_raw, A, B, s0 (the caller keeps
+ *   the buffer unchanged in between; nothing checks it).  ws as for
+ *   ssd_backward.
+ * Errors and the device status word are those of ssd_forward / ssd_backward.
+ */
+ssd_status ssd_states_size(const ssd_problem* prob, size_t* bytes);
+ssd_status ssd_forward_stash(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
+                             const void* B, const void* C, const float* s0, void* y, float* s_final, void* states,
+                             size_t states_bytes, void* ws, size_t ws_bytes, void* cuda_stream);
+ssd_status ssd_backward_stashed(const ssd_problem* prob, const void* dy, const float* ds_final, const void* x,
+                                const float* dt_raw, const float* A, const void* B, const void* C,
+                                const void* states, size_t states_bytes, void* dx, float* ddt_raw, float* dA,
+                                void* dB, void* dC, float* ds0, void* ws, size_t ws_bytes, void* cuda_stream);
+
+/*
  * Forward scan without a caller workspace, for callers that cannot allocate
  * device memory.  (The pages describe no such call; it is an addition of this
  * library.)

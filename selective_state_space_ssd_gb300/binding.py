@@ -41,7 +41,8 @@ class ssd_problem(ctypes.Structure):
 
 
 EXPORTS = ("ssd_workspace_size", "ssd_forward", "ssd_backward", "ssd_forward_static", "ssd_profile_start",
-           "ssd_profile_stop", "ssd_status_string", "ssd_version")
+           "ssd_profile_stop", "ssd_status_string", "ssd_version", "ssd_states_size", "ssd_forward_stash",
+           "ssd_backward_stashed")
 
 
 class ssd_kernel_time(ctypes.Structure):
@@ -82,6 +83,12 @@ def load(path: str | None = None):
         lib.ssd_profile_stop.restype = i32
         lib.ssd_version.argtypes = []
         lib.ssd_version.restype = i32
+        lib.ssd_states_size.argtypes = [ctypes.POINTER(ssd_problem), ctypes.POINTER(sz)]
+        lib.ssd_states_size.restype = i32
+        lib.ssd_forward_stash.argtypes = [ctypes.POINTER(ssd_problem)] + [vp] * 9 + [sz, vp, sz, vp]
+        lib.ssd_forward_stash.restype = i32
+        lib.ssd_backward_stashed.argtypes = [ctypes.POINTER(ssd_problem)] + [vp] * 8 + [sz] + [vp] * 7 + [sz, vp]
+        lib.ssd_backward_stashed.restype = i32
         _lib = lib
         return lib
 
@@ -143,6 +150,33 @@ def ssd_backward(prob, dy, ds_final, x, dt_raw, A, B, C, s0, dx, ddt_raw, dA, dB
         raise SSDError(st, "ssd_backward")
 
 
+def ssd_states_size(prob: ssd_problem) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().ssd_states_size(ctypes.byref(prob), ctypes.byref(out))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_states_size")
+    return out.value
+
+
+def ssd_forward_stash(prob, x, dt_raw, A, B, C, s0, y, s_final, states, states_bytes, ws, ws_bytes,
+                      stream=None) -> None:
+    st = load().ssd_forward_stash(ctypes.byref(prob), _ptr(x), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(s0),
+                                  _ptr(y), _ptr(s_final), _ptr(states), int(states_bytes), _ptr(ws), int(ws_bytes),
+                                  _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_forward_stash")
+
+
+def ssd_backward_stashed(prob, dy, ds_final, x, dt_raw, A, B, C, states, states_bytes, dx, ddt_raw, dA, dB, dC,
+                         ds0, ws, ws_bytes, stream=None) -> None:
+    st = load().ssd_backward_stashed(ctypes.byref(prob), _ptr(dy), _ptr(ds_final), _ptr(x), _ptr(dt_raw), _ptr(A),
+                                     _ptr(B), _ptr(C), _ptr(states), int(states_bytes), _ptr(dx), _ptr(ddt_raw),
+                                     _ptr(dA), _ptr(dB), _ptr(dC), _ptr(ds0), _ptr(ws), int(ws_bytes),
+                                     _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_backward_stashed")
+
+
 def ssd_profile_start(capacity: int) -> None:
     st = load().ssd_profile_start(int(capacity))
     if st != SSD_OK:
@@ -189,4 +223,32 @@ def backward(cfg: dict, dy, ds_final, x, dt_raw, A, B, C, s0=None, stream=None, 
     ws, n = workspace if workspace is not None else _workspace(prob, True, dev)
     ssd_backward(prob, dy, ds_final, x, dt_raw, A, B, C, s0, out["dx"], out["ddt_raw"], out["dA"], out["dB"],
                  out["dC"], out["ds0"], ws, n, stream)
+    return out
+
+
+def forward_stash(cfg: dict, x, dt_raw, A, B, C, s0=None, stream=None, workspace=None):
+    """``forward`` that also keeps the chunk states; returns (y, s_final, states)
+    with states a uint8 device tensor for ``backward_stashed``."""
+    prob = problem(cfg)
+    dev = x.device
+    y = torch.empty_like(x)
+    s_final = torch.empty((cfg["batch"], cfg["nheads"], cfg["headdim"], cfg["dstate"]), dtype=torch.float32,
+                          device=dev)
+    nst = ssd_states_size(prob)
+    states = torch.empty(nst, dtype=torch.uint8, device=dev)
+    ws, n = workspace if workspace is not None else _workspace(prob, False, dev)
+    ssd_forward_stash(prob, x, dt_raw, A, B, C, s0, y, s_final, states, nst, ws, n, stream)
+    return y, s_final, states
+
+
+def backward_stashed(cfg: dict, dy, ds_final, x, dt_raw, A, B, C, states, stream=None, workspace=None):
+    """``backward`` from the chunk states ``forward_stash`` kept (no s0, no
+    forward replay); returns the same dict."""
+    prob = problem(cfg)
+    dev = x.device
+    out = {"dx": torch.empty_like(x), "ddt_raw": torch.empty_like(dt_raw), "dA": torch.empty_like(A),
+           "dB": torch.empty_like(B), "dC": torch.empty_like(C), "ds0": torch.empty_like(ds_final)}
+    ws, n = workspace if workspace is not None else _workspace(prob, True, dev)
+    ssd_backward_stashed(prob, dy, ds_final, x, dt_raw, A, B, C, states, states.numel(), out["dx"], out["ddt_raw"],
+                         out["dA"], out["dB"], out["dC"], out["ds0"], ws, n, stream)
     return out

@@ -233,4 +233,52 @@ ssd_status ssd_backward(const ssd_problem* prob, const void* dy, const float* ds
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status ssd_states_size(const ssd_problem* prob, size_t* bytes) {
+  if (!bytes) return SSD_ERR_INVALID_ARG;
+  Dims d;
+  ssd_status s = make_dims(prob, &d);
+  if (s != SSD_OK) return s;
+  if (d.variant != kMamba2 || !tc_forward_supported(d)) return SSD_ERR_SHAPE;
+  *bytes = tc_scan_states_bytes(d);
+  return SSD_OK;
+}
+
+ssd_status ssd_forward_stash(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
+                             const void* B, const void* C, const float* s0, void* y, float* s_final, void* states,
+                             size_t states_bytes, void* ws, size_t ws_bytes_given, void* cuda_stream) {
+  Dims d;
+  ssd_status s = make_dims(prob, &d);
+  if (s != SSD_OK) return s;
+  if (d.variant != kMamba2 || !tc_forward_supported(d)) return SSD_ERR_SHAPE;
+  s = check_ptrs({x, dt_raw, A, B, C, y, s_final, states}, {s0});
+  if (s != SSD_OK) return s;
+  if (states_bytes < tc_scan_states_bytes(d) || ws_bytes_given < ws_bytes(d, false)) return SSD_ERR_WORKSPACE;
+  if (!ws) return SSD_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
+  FwdArgs a{x, dt_raw, A, B, C, s0, y, s_final, static_cast<__nv_bfloat16*>(states)};
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  return tc_forward(d, a, ws, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_backward_stashed(const ssd_problem* prob, const void* dy, const float* ds_final, const void* x,
+                                const float* dt_raw, const float* A, const void* B, const void* C,
+                                const void* states, size_t states_bytes, void* dx, float* ddt_raw, float* dA,
+                                void* dB, void* dC, float* ds0, void* ws, size_t ws_bytes_given, void* cuda_stream) {
+  Dims d;
+  ssd_status s = make_dims(prob, &d);
+  if (s != SSD_OK) return s;
+  if (d.variant != kMamba2 || !tc_backward_supported(d)) return SSD_ERR_SHAPE;
+  s = check_ptrs({dy, ds_final, x, dt_raw, A, B, C, states, dx, ddt_raw, dA, dB, dC, ds0}, {});
+  if (s != SSD_OK) return s;
+  if (states_bytes < tc_scan_states_bytes(d) || ws_bytes_given < ws_bytes(d, true)) return SSD_ERR_WORKSPACE;
+  if (!ws) return SSD_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
+  BwdArgs a{dy, ds_final, x, dt_raw, A, B, C, nullptr, dx, ddt_raw, dA, dB, dC, ds0,
+            static_cast<const __nv_bfloat16*>(states)};
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  return tc_backward(d, a, ws, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -31,6 +31,7 @@ struct FwdArgs {
   const float* s0;
   void* y;
   float* s_final;
+  __nv_bfloat16* states_out = nullptr;  // tensor-core path: chunk states to this caller buffer, not the workspace
 };
 
 struct BwdArgs {
@@ -48,6 +49,7 @@ struct BwdArgs {
   void* dB;
   void* dC;
   float* ds0;
+  const __nv_bfloat16* states_in = nullptr;  // tensor-core path: stashed chunk states (no forward replay)
 };
 
 // The first kStatusBytes of every workspace hold the device status word

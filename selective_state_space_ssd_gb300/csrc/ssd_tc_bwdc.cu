@@ -711,8 +711,12 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   Carver cv(ws);
   BwdcWs w = carve(d, lmax, cv);
   int* status = static_cast<int*>(ws);
+  // the chunk states: replayed from the leaf inputs, or the forward's stash (the same kernel on the same
+  // inputs wrote it, so the two give the same bits)
+  const __nv_bfloat16* states = a.states_in ? a.states_in : w.states;
   cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, status, st);
-  if (e == cudaSuccess) e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, nullptr, w.states, status, st);
+  if (e == cudaSuccess && !a.states_in)
+    e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, nullptr, w.states, status, st);
   if (e == cudaSuccess) e = tc_scan(d, true, a.dy, a.C, a.dt_raw, a.A, a.ds_final, a.ds0, w.dstates, status, st);
   if (e != cudaSuccess) return e;
   const uint64_t rows = (uint64_t)d.b * d.T;
@@ -723,7 +727,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdx, a.dx, (uint64_t)d.H * kP, rows, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d_bf16(&tb, a.B, d.N, d.G, rows, 64, 1, 64);
   if (e == cudaSuccess) e = make_tmap_3d_bf16(&tcm, a.C, d.N, d.G, rows, 64, 1, 64);
-  if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, w.states, kP, srows, 64, kN);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, states, kP, srows, 64, kN);
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&tds, w.dstates, kP, srows, 64, kN);
   if (e != cudaSuccess) return e;
   // partial slots use the layout of the launched grid (nseg of the largest grid bounds it)

@@ -440,14 +440,15 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t s
   Carver cv(ws);
   FwdcWs w = carve(d, cv);
   int* status = static_cast<int*>(ws);
+  __nv_bfloat16* states = a.states_out ? a.states_out : w.states;  // a stash for the backward, or scratch
   cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, status, st);
-  if (e == cudaSuccess) e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, a.s_final, w.states, status, st);
+  if (e == cudaSuccess) e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, a.s_final, states, status, st);
   if (e != cudaSuccess) return e;
   const uint64_t rows = (uint64_t)d.b * d.T;
   CUtensorMap tx, tcm, ts, ty;
   e = make_tmap_2d_bf16(&tx, a.x, (uint64_t)d.H * kP, rows, 64, 64);
   if (e == cudaSuccess) e = make_tmap_3d_bf16(&tcm, a.C, d.N, d.G, rows, 64, 1, 64);
-  if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, w.states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, kN);
+  if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, kN);
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&ty, a.y, (uint64_t)d.H * kP, rows, 64, 64);
   if (e != cudaSuccess) return e;
   const long long total = (long long)d.b * d.nc * d.H;

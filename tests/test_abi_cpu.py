@@ -117,3 +117,44 @@ def test_pointer_validation_launches_nothing(cuda_lib):
     st = cuda_lib.ssd_backward(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, None,
                                fake, fake, fake, fake, fake, fake, fake, need - 1, None)
     assert st == 5
+
+
+def test_states_stash_validation(cuda_lib):
+    """The stashed-states pair exists for the tensor-core problems only; its
+    size is the bf16 chunk-state tensor; bad buffers fail on the host."""
+    import torch
+    tc = binding.problem(CONFIGS["mamba2_2p7b_bf16"])
+    c = CONFIGS["mamba2_2p7b_bf16"]
+    assert binding.ssd_states_size(tc) == (c["batch"] * c["nheads"] * (c["seqlen"] // c["chunk"]) * c["dstate"] *
+                                           c["headdim"] * 2)
+    n = ctypes.c_size_t(0)
+    for name in ("mamba2_tiny_fp32", "mamba1_fp32", "mimo_r4_bf16"):
+        p = binding.problem(CONFIGS[name])
+        assert cuda_lib.ssd_states_size(ctypes.byref(p), ctypes.byref(n)) == 2  # SSD_ERR_SHAPE
+    assert cuda_lib.ssd_states_size(ctypes.byref(tc), None) == 1
+    if torch.cuda.is_available():
+        return  # the rest uses fake device addresses
+    fake = 1 << 20
+    need_s = binding.ssd_states_size(tc)
+    need_f = binding.ssd_workspace_size(tc, False)
+    need_b = binding.ssd_workspace_size(tc, True)
+    args = [fake] * 6 + [None, fake, fake]  # x, dt_raw, A, B, C, (s0), y, s_final
+    st = cuda_lib.ssd_forward_stash(ctypes.byref(tc), *args[:5], None, fake, fake, None, need_s, fake, need_f, None)
+    assert st == 1  # no states buffer
+    st = cuda_lib.ssd_forward_stash(ctypes.byref(tc), *args[:5], None, fake, fake, fake, need_s - 1, fake, need_f,
+                                    None)
+    assert st == 5  # states buffer too small
+    st = cuda_lib.ssd_forward_stash(ctypes.byref(tc), *args[:5], None, fake, fake, fake + 8, need_s, fake, need_f,
+                                    None)
+    assert st == 4  # misaligned states buffer
+    # prob, dy, ds_final, x, dt_raw, A, B, C, states, states_bytes, dx, ddt_raw, dA, dB, dC, ds0, ws, ws_bytes, stream
+    st = cuda_lib.ssd_backward_stashed(ctypes.byref(tc), fake, fake, fake, fake, fake, fake, fake, fake, need_s,
+                                       fake, fake, fake, fake, fake, fake, fake, need_b - 1, None)
+    assert st == 5
+    st = cuda_lib.ssd_backward_stashed(ctypes.byref(tc), fake, fake, fake, fake, fake, fake, fake, None, need_s,
+                                       fake, fake, fake, fake, fake, fake, fake, need_b, None)
+    assert st == 1
+    small = binding.problem(CONFIGS["mamba2_tiny_fp32"])
+    st = cuda_lib.ssd_backward_stashed(ctypes.byref(small), fake, fake, fake, fake, fake, fake, fake, fake, need_s,
+                                       fake, fake, fake, fake, fake, fake, fake, need_b, None)
+    assert st == 2

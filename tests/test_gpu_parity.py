@@ -80,6 +80,32 @@ def test_backward_is_bitwise_deterministic(name):
             assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("name", ["m2_bf16_tiles", "m2_bf16_split_runs", "full_2p7b"])
+def test_stashed_states_give_the_recompute_bits(name):
+    """ssd_forward_stash returns ssd_forward's bits and a chunk-state stash;
+    ssd_backward_stashed from that stash returns ssd_backward's bits (which the
+    other tests hold to the oracle), with and without s0."""
+    cfg = CONFIGS["mamba2_2p7b_bf16"] if name == "full_2p7b" else SMALL[name]
+    for zero_s0 in (False, True):
+        dev = to_device(synth.make_inputs(cfg, seed=6, zero_s0=zero_s0))
+        s0 = None if zero_s0 else dev["s0"]
+        y, sf = binding.forward(cfg, dev["x"], dev["dt_raw"], dev["A"], dev["B"], dev["C"], s0)
+        y2, sf2, states = binding.forward_stash(cfg, dev["x"], dev["dt_raw"], dev["A"], dev["B"], dev["C"], s0)
+        g = binding.backward(cfg, dev["dy"], dev["ds_final"], dev["x"], dev["dt_raw"], dev["A"], dev["B"], dev["C"],
+                             s0)
+        g2 = binding.backward_stashed(cfg, dev["dy"], dev["ds_final"], dev["x"], dev["dt_raw"], dev["A"], dev["B"],
+                                      dev["C"], states)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2) and torch.equal(sf, sf2)
+        for k in g:
+            assert torch.equal(g[k], g2[k]), k
+        # the stash's first tile of every (batch, head) is s0 in bf16, laid out [N][P]
+        st = states.view(torch.bfloat16).view(cfg["batch"], cfg["nheads"], cfg["seqlen"] // cfg["chunk"],
+                                              cfg["dstate"], cfg["headdim"])
+        want = torch.zeros_like(st[:, :, 0]) if zero_s0 else dev["s0"].transpose(-1, -2).to(torch.bfloat16)
+        assert torch.equal(st[:, :, 0], want)
+
+
 def test_zero_seed_and_zero_dy():
     """dy = 0 leaves only the decayed seed: ds0 = exp(sum da) ds_final, dC = 0."""
     cfg = SMALL["m2_bf16_tiles"]
