@@ -106,10 +106,13 @@ def kernel_bytes(name, cfg):
         "k_group_sum": part + t["B"],
         "k_dA_sum": small + t["A"],
         # tensor-core kernels (bf16 tiles; chunk states S_c and dS_{c+1} kept as bf16 [N][P] tiles)
-        "k_cb": t["B"] + t["C"] + cbb,
-        "k_tc_states": t["x"] + dtb + t["A"] + t["B"] + t["s0"] + sbf,
+        # the scan launches: each input read once, the chunk states written once per direction, and the
+        # C B^T tiles of every (chunk, group) beside the chains
+        "k_tc_states_cb": t["x"] + dtb + t["A"] + t["B"] + t["C"] + t["s0"] + sbf + t["s0"] + cbb,
+        "k_tc_scan_pair_cb": (2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 2 * t["s0"] + 2 * sbf + t["s0"]
+                              + cbb),                                                        # x, dy, ..., ds0, CB
+        "k_tc_dstates_cb": t["x"] + dtb + t["A"] + t["B"] + t["C"] + t["s0"] + sbf + t["s0"] + cbb,
         "k_tc_fwd_chunk": t["x"] + dtb + t["A"] + t["C"] + cbb + sbf + t["x"],
-        "k_tc_dstates": t["x"] + dtb + t["A"] + t["C"] + t["s0"] + sbf + t["s0"],
         "k_tc_bwd_chunk": (2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + cbb + 2 * sbf      # dy, x, ..., S_c, dS
                            + t["x"] + dtb + small + 2 * cpart),                              # dx, ddt_raw, dA, dB/dC parts
         "k_tc_bwd_sums": 2 * cpart + t["B"] + t["C"] + small + t["A"],
@@ -143,22 +146,24 @@ def peaks():
 
 def ncu_traffic(kernel, workload):
     """Per-launch DRAM bytes from the committed ncu summary of this kernel, if
-    it was taken on the current sources; otherwise None."""
+    the sources it was taken on (the record's list of csrc files) are
+    unchanged; otherwise None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     rec = d.get(f"{kernel}@{workload}")
-    if not rec or rec.get("source_hash") != source_hash():
+    if not rec or rec.get("source_hash") != source_hash(rec.get("sources")):
         return None
     return rec.get("dram_bytes_per_launch")
 
 
-def source_hash():
+def source_hash(files=None):
+    """Hash of the named csrc files (all of them when None)."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "selective_state_space_ssd_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files else os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())

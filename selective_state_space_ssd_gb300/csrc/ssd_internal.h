@@ -81,18 +81,24 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_
 
 // Tensor-core path (Mamba-2, bf16 io, L = 64, P = 64, N = 128).
 bool tc_forward_supported(const Dims& d);
-// K2 pre-pass (ssd_tc_prep.cu): CB[b, c, g] = C B^T of every chunk and group, fp32.
-cudaError_t tc_cb_prepass(const Dims& d, const void* B, const void* C, float* CB, int* status, cudaStream_t st);
 // Chunk-parallel forward (ssd_tc_fwdc.cu): the state scan, then every (chunk, head) output at once.
 size_t tc_forward_ws(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
-// Sequential state scans (ssd_tc_scan.cu): forward writes S_c for every chunk
-// (bf16 [b,H,nc][N][P]) and S_nc into fin (if not null); reverse writes
-// dS_{c+1} for every chunk and dS_0 into fin.  u = x or dy, k = B or C,
-// init = s0 (may be null) or ds_final.
+// Sequential state scans and the K2 tiles, in one launch (ssd_tc_scan.cu).
+// The forward scan (u = x, with B) writes S_c for every chunk (bf16
+// [b,H,nc][N][P]) and S_nc into fin (if not null); the reverse scan (u = dy,
+// with C) writes dS_{c+1} for every chunk and dS_0 into fin.  init = s0 (may
+// be null) or ds_final.  Either side may be absent (null); CB[b, c, g] =
+// C B^T of every chunk and group (fp32) is always written.
+struct ScanSide {
+  const void* u;
+  const float* init;
+  float* fin;
+  __nv_bfloat16* states;
+};
 size_t tc_scan_states_bytes(const Dims& d);
-cudaError_t tc_scan(const Dims& d, bool reverse, const void* u, const void* k, const float* dt_raw, const float* A,
-                    const float* init, float* fin, __nv_bfloat16* states, int* status, cudaStream_t st);
+cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, const void* B, const void* C,
+                     const float* dt_raw, const float* A, float* CB, int* status, cudaStream_t st);
 // Chunk-parallel backward (ssd_tc_bwdc.cu): both scans, then every (chunk, head) at once.
 size_t tc_backward_ws(const Dims& d);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);

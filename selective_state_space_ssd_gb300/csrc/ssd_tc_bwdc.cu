@@ -2,11 +2,12 @@
 // io, chunk L = 64, head dim P = 64, state N = 128).
 //
 // The recompute backward of the burn-mamba page "combined_backward.rs" in
-// three stages:
+// three stages, the first two in one launch (ssd_tc_scan.cu, which also
+// writes the K2 tiles CB = C B^T), since neither needs the other:
 //   1. the forward state scan replays S_c (the state entering chunk c) from
-//      the saved inputs (ssd_tc_scan.cu, forward mode);
+//      the saved inputs;
 //   2. the reverse scan gives dS_{c+1} (the gradient of the state leaving
-//      chunk c) for every chunk, and ds0 (ssd_tc_scan.cu, reverse mode);
+//      chunk c) for every chunk, and ds0;
 //   3. this kernel: with S_c and dS_{c+1} known, every (chunk, head) is
 //      independent, and computes the K5 (BLUE + ORANGE), K4, K3 and K2
 //      backwards of the page:
@@ -714,10 +715,10 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   // the chunk states: replayed from the leaf inputs, or the forward's stash (the same kernel on the same
   // inputs wrote it, so the two give the same bits)
   const __nv_bfloat16* states = a.states_in ? a.states_in : w.states;
-  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, status, st);
-  if (e == cudaSuccess && !a.states_in)
-    e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, nullptr, w.states, status, st);
-  if (e == cudaSuccess) e = tc_scan(d, true, a.dy, a.C, a.dt_raw, a.A, a.ds_final, a.ds0, w.dstates, status, st);
+  // the replay (unless stashed) and the reverse scan are independent: one launch runs both, plus CB
+  const ScanSide fwd{a.x, a.s0, nullptr, w.states};
+  const ScanSide rev{a.dy, a.ds_final, a.ds0, w.dstates};
+  cudaError_t e = tc_scans(d, a.states_in ? nullptr : &fwd, &rev, a.B, a.C, a.dt_raw, a.A, w.CB, status, st);
   if (e != cudaSuccess) return e;
   const uint64_t rows = (uint64_t)d.b * d.T;
   const uint64_t srows = (uint64_t)d.b * d.H * d.nc * kN;

@@ -1,8 +1,9 @@
 // Chunk-parallel forward output of the Mamba-2 scan on tcgen05 tensor cores
 // (bf16 io, chunk L = 64, head dim P = 64, state N = 128).
 //
-// The forward runs as K2 (C B^T per chunk, k_cb), the K3 + K4 state scan
-// (ssd_tc_scan.cu: every chunk-input state S_c and s_final), and this kernel,
+// The forward runs as one launch of the K3 + K4 state scan with the K2 tiles
+// C B^T per chunk beside it (ssd_tc_scan.cu: every chunk-input state S_c,
+// s_final and CB), and this kernel,
 // the K5 output of the burn-mamba page "combined_backward.rs" (BLUE + ORANGE),
 // for which every (chunk, head) is independent once S_c is known:
 //
@@ -441,8 +442,8 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t s
   FwdcWs w = carve(d, cv);
   int* status = static_cast<int*>(ws);
   __nv_bfloat16* states = a.states_out ? a.states_out : w.states;  // a stash for the backward, or scratch
-  cudaError_t e = tc_cb_prepass(d, a.B, a.C, w.CB, status, st);
-  if (e == cudaSuccess) e = tc_scan(d, false, a.x, a.B, a.dt_raw, a.A, a.s0, a.s_final, states, status, st);
+  const ScanSide fwd{a.x, a.s0, a.s_final, states};
+  cudaError_t e = tc_scans(d, &fwd, nullptr, a.B, a.C, a.dt_raw, a.A, w.CB, status, st);
   if (e != cudaSuccess) return e;
   const uint64_t rows = (uint64_t)d.b * d.T;
   CUtensorMap tx, tcm, ts, ty;

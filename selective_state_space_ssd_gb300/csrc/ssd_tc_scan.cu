@@ -27,6 +27,17 @@
 // exponentials), warp 7 TMA producer, warp 8 MMA issuer and TMEM owner.
 // Every wait is bounded; on a timeout the kernel records a code in the
 // workspace status word and stops.
+//
+// One launch carries every independent piece of sequential-scan work a call
+// has, in grid order: the forward chains, the reverse chains, then the K2 tiles
+// CB = C B^T (one (chunk, group) per CTA, fp32; the chunk kernels read them).
+// The backward's forward replay and reverse scan do not depend on each other,
+// so they share the launch: a chain is a latency chain of 64 steps, and the
+// SMs' third CTA slots (left partly idle by 320 chains on 152 SMs) take the
+// other direction's chains.  The CB tiles come last and fill the slots the
+// chains leave free, instead of costing a launch of their own.
+#include <string.h>
+
 #include "ssd_device.cuh"
 #include "ssd_internal.h"
 #include "tc_common.cuh"
@@ -69,14 +80,21 @@ struct ScanParams {
   int T, H, hpg, nc;
 };
 
+// One direction's chains: the tensor maps of U (x or dy), K (B or C) and the state tiles out, and the scalars.
+struct ScanJob {
+  CUtensorMap u, k, out;
+  ScanParams prm;
+};
+
+// One (batch, head) chain, run by the whole CTA.
 template <bool kRev, int kStU>
-__global__ void __launch_bounds__(kThreads, 3)
-    k_scan(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_out, ScanParams prm) {
-  extern __shared__ uint8_t smem_raw[];
-  ScanSmem<kStU>& sm = *reinterpret_cast<ScanSmem<kStU>*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+__device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uint8_t* smem) {
+  ScanSmem<kStU>& sm = *reinterpret_cast<ScanSmem<kStU>*>(smem);
+  const CUtensorMap& tm_u = job.u;
+  const CUtensorMap& tm_k = job.k;
+  const CUtensorMap& tm_out = job.out;
+  const ScanParams& prm = job.prm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, b = blockIdx.y;
   const int T = prm.T, H = prm.H, nc = prm.nc;
   const int g = h / prm.hpg;
   const int row0 = b * T;
@@ -254,7 +272,6 @@ __global__ void __launch_bounds__(kThreads, 3)
     send(chunk_of(0));
     tmem_wait_st();
     for (int r = 0; r < nc; ++r) {
-      const int s = r & 1;
       const int k = r % kScal;
       bool ok = mbar_wait(&sm.sc_ready[k], (r / kScal) & 1, status, 89);
       ok = ok && mbar_wait(&sm.p_ready, r & 1, status, 88);
@@ -304,19 +321,114 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-}  // namespace
+// CB[b][c][g][t][s] = sum_n C[b, c*L+t, g, n] B[b, c*L+s, g, n] (fp32) for one (chunk, group): the C and
+// B tiles come in by TMA (two 64-column atoms each, K-major), one thread issues the eight K = 16 steps of one
+// M = 64, N = 64 MMA, and warps 0-3 write the accumulator rows out; the other warps only join the barriers.
+struct CbJob {
+  CUtensorMap c, b;
+  float* CB;  // [b, nc, G, L, L]
+  int* status;
+  int T, G, nc;
+};
 
-namespace {
+struct alignas(1024) CbSmem {
+  uint8_t C[2][kL * 64 * 2];  // [atom][t][64 n] bf16, SW128
+  uint8_t B[2][kL * 64 * 2];  // [atom][s][64 n]
+  uint64_t full, done;
+  uint32_t tmem_slot;
+};
+static_assert(sizeof(CbSmem) <= sizeof(ScanSmem<2>), "a CB tile runs in a scan CTA's shared memory");
 
-// Three x / dy stages when three CTAs of them still fit an SM (all (batch, head) chains of the workloads
-// stay resident at once), else two.
-template <int kStU, bool kRev>
-cudaError_t launch_stages(const Dims& d, const CUtensorMap& tu, const CUtensorMap& tk, const CUtensorMap& to,
-                          const ScanParams& prm, cudaStream_t st, bool* fits) {
+__device__ __forceinline__ void cb_tile(const CbJob& job, int k, uint8_t* smem) {
+  CbSmem& sm = *reinterpret_cast<CbSmem*>(smem);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int g = k % job.G, bc = k / job.G;
+  const int c = bc % job.nc, b = bc / job.nc;
+  const int row = b * job.T + c * kL;
+  int* status = job.status;
+  if (tid == 0) {
+    mbar_init(&sm.full, 1);
+    mbar_init(&sm.done, 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(&sm.tmem_slot, 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  if (tid == 0) {
+    mbar_expect_tx(&sm.full, 4 * kL * 64 * 2);
+    for (int a = 0; a < 2; ++a) {
+      tma_load_3d(sm.C[a], &job.c, 64 * a, g, row, &sm.full);
+      tma_load_3d(sm.B[a], &job.b, 64 * a, g, row, &sm.full);
+    }
+    if (mbar_wait(&sm.full, 0, status, 61)) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kN; kk += 16)
+        mma_bf16(tmem, kdesc(sm.C[0], kL, kk), kdesc(sm.B[0], kL, kk), idesc_bf16(64, 64, false, false), kk > 0);
+    }
+    mma_commit(&sm.done);  // arrives even when nothing was issued, so the readers below never wait forever
+  }
+  if (warp < 4) {
+    __syncwarp();
+    const bool ok = mbar_wait(&sm.done, 0, status, 62);
+    tc_fence_after();
+    if (ok && *status == 0) {
+      // M = 64 accumulator: row t = 16 warp + (lane & 15) in lane 32 warp + (lane & 15); lanes 16-31 take
+      // columns 32-63
+      const int lane = tid & 31, t = 16 * warp + (lane & 15), s0 = 32 * (lane >> 4);
+      uint32_t v[32];
+      tmem_ld_pair32(taddr(tmem, 32 * warp, 0), v);
+      tmem_wait_ld();
+      float4* out = reinterpret_cast<float4*>(job.CB + ((size_t)k * kL + t) * kL + s0);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        out[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
+                             __uint_as_float(v[4 * e + 3]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+// Everything one launch runs, and how the grid splits: blocks [0, n_fwd) are forward chains, the next n_rev
+// reverse chains (chain i is (batch i / H, head i % H)), the last n_cb CB tiles (tile i is (chunk, group) i).
+struct ScanLaunch {
+  ScanJob fwd, rev;
+  CbJob cb;
+  int n_fwd, n_rev, n_cb, H;
+};
+
+template <int kStU>
+__global__ void __launch_bounds__(kThreads, 3) k_scan(const __grid_constant__ ScanLaunch job) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  int i = blockIdx.x;
+  if (i < job.n_fwd) {
+    scan_chain<false, kStU>(job.fwd, i % job.H, i / job.H, smem);
+    return;
+  }
+  i -= job.n_fwd;
+  if (i < job.n_rev) {
+    scan_chain<true, kStU>(job.rev, i % job.H, i / job.H, smem);
+    return;
+  }
+  cb_tile(job.cb, i - job.n_rev, smem);
+}
+
+// Three x / dy stages when three CTAs of them still fit an SM (all (batch, head) chains of one direction stay
+// resident at once), else two.
+template <int kStU>
+cudaError_t launch_stages(const ScanLaunch& job, const char* name, cudaStream_t st, bool* fits) {
   const int smem = (int)sizeof(ScanSmem<kStU>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_scan<kRev, kStU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(k_scan<kStU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_scan<kRev, kStU>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(k_scan<kStU>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   if (fits) {  // shared memory of three CTAs (each with the per-block reservation) against the SM's
@@ -328,43 +440,52 @@ cudaError_t launch_stages(const Dims& d, const CUtensorMap& tu, const CUtensorMa
     *fits = 3ll * (smem + reserved) <= per_sm;
     if (!*fits) return cudaSuccess;
   }
-  if (kRev) {
-    SSD_LAUNCH("k_tc_dstates", st, k_scan<kRev, kStU><<<dim3(d.H, d.b), kThreads, smem, st>>>(tu, tk, to, prm));
-  } else {
-    SSD_LAUNCH("k_tc_states", st, k_scan<kRev, kStU><<<dim3(d.H, d.b), kThreads, smem, st>>>(tu, tk, to, prm));
-  }
+  const unsigned grid = (unsigned)(job.n_fwd + job.n_rev + job.n_cb);
+  SSD_LAUNCH(name, st, k_scan<kStU><<<grid, kThreads, smem, st>>>(job));
   return cudaGetLastError();
-}
-
-template <bool kRev>
-cudaError_t launch_scan(const Dims& d, const CUtensorMap& tu, const CUtensorMap& tk, const CUtensorMap& to,
-                        const ScanParams& prm, cudaStream_t st) {
-  bool fits = false;
-  cudaError_t e = launch_stages<3, kRev>(d, tu, tk, to, prm, st, &fits);
-  if (e != cudaSuccess || fits) return e;
-  return launch_stages<2, kRev>(d, tu, tk, to, prm, st, nullptr);
 }
 
 }  // namespace
 
 size_t tc_scan_states_bytes(const Dims& d) { return (size_t)d.b * d.H * d.nc * kN * kP * sizeof(__nv_bfloat16); }
 
-cudaError_t tc_scan(const Dims& d, bool reverse, const void* u, const void* k, const float* dt_raw, const float* A,
-                    const float* init, float* fin, __nv_bfloat16* states, int* status, cudaStream_t st) {
-  CUtensorMap tu, tk, to;
+cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, const void* B, const void* C,
+                     const float* dt_raw, const float* A, float* CB, int* status, cudaStream_t st) {
   const uint64_t rows = (uint64_t)d.b * d.T;
-  cudaError_t e = make_tmap_2d_bf16(&tu, u, (uint64_t)d.H * kP, rows, 64, 64);
-  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tk, k, d.N, d.G, rows, 64, 1, 64);
-  if (e == cudaSuccess) e = make_tmap_2d_bf16(&to, states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, 32);
-  if (e != cudaSuccess) return e;
-  ScanParams prm{dt_raw, A, init, fin, status, d.T, d.H, d.hpg, d.nc};
-  if (reverse) {
-    e = launch_scan<true>(d, tu, tk, to, prm, st);
-  } else {
-    e = launch_scan<false>(d, tu, tk, to, prm, st);
+  const uint64_t srows = (uint64_t)d.b * d.H * d.nc * kN;
+  const long long chains = (long long)d.b * d.H, tiles = (long long)d.b * d.nc * d.G;
+  if ((fwd ? chains : 0) + (rev ? chains : 0) + tiles > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  ScanLaunch job;
+  memset(&job, 0, sizeof(job));
+  cudaError_t e = cudaSuccess;
+  const ScanSide* sides[2] = {fwd, rev};
+  ScanJob* jobs[2] = {&job.fwd, &job.rev};
+  for (int r = 0; r < 2 && e == cudaSuccess; ++r) {
+    const ScanSide* s = sides[r];
+    if (!s) continue;
+    ScanJob& j = *jobs[r];
+    e = make_tmap_2d_bf16(&j.u, s->u, (uint64_t)d.H * kP, rows, 64, 64);
+    if (e == cudaSuccess) e = make_tmap_3d_bf16(&j.k, r == 0 ? B : C, d.N, d.G, rows, 64, 1, 64);
+    if (e == cudaSuccess) e = make_tmap_2d_bf16(&j.out, s->states, kP, srows, 64, 32);
+    j.prm = ScanParams{dt_raw, A, s->init, s->fin, status, d.T, d.H, d.hpg, d.nc};
   }
+  if (e == cudaSuccess) e = make_tmap_3d_bf16(&job.cb.c, C, d.N, d.G, rows, 64, 1, 64);
+  if (e == cudaSuccess) e = make_tmap_3d_bf16(&job.cb.b, B, d.N, d.G, rows, 64, 1, 64);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  job.cb.CB = CB;
+  job.cb.status = status;
+  job.cb.T = d.T;
+  job.cb.G = d.G;
+  job.cb.nc = d.nc;
+  job.n_fwd = fwd ? (int)chains : 0;
+  job.n_rev = rev ? (int)chains : 0;
+  job.n_cb = (int)tiles;
+  job.H = d.H;
+  const char* name = fwd && rev ? "k_tc_scan_pair_cb" : fwd ? "k_tc_states_cb" : "k_tc_dstates_cb";
+  bool fits = false;
+  e = launch_stages<3>(job, name, st, &fits);
+  if (e != cudaSuccess || fits) return e;
+  return launch_stages<2>(job, name, st, nullptr);
 }
 
 }  // namespace ssd
