@@ -70,7 +70,7 @@ def tensor_flops(cfg):
         return 0.0
     b, T, H, P, N, L, R = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "chunk", "mimo_rank"))
     G = cfg["ngroups"] if v == "mamba2" else H
-    nc = T // L
+    nc = -(-T // L)
     LR = L * R
     lpn, llp, lln = 2.0 * LR * P * N, 2.0 * LR * LR * P, 2.0 * LR * LR * N
     per_head = 7 * lpn + 3 * llp          # K3, BLUE (fwd); K3 replay, BLUE dS, BLUE dC, K3 bwd x2; ORANGE, dW, dv
@@ -84,7 +84,7 @@ def kernel_bytes(name, cfg):
     t = tensor_bytes(cfg)
     b, T, H, P, N = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate"))
     L = cfg["chunk"]
-    nc = T // L
+    nc = -(-T // L)
     states = b * H * nc * P * N * 4
     small = b * H * nc * 4
     dtb = t["dt_raw"]
@@ -118,7 +118,7 @@ def kernel_bytes(name, cfg):
         "k_tc_bwd_sums": 2 * cpart + t["B"] + t["C"] + small + t["A"],
         "k_m1_forward": 2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 2 * t["s0"],
         "k_m1_backward": 2 * t["x"] + 2 * dtb + t["A"] + t["B"] + t["C"] + 3 * t["s0"] + t["x"]
-                         + 2 * b * T * H * N * 4 + b * H * N * 4 + b * H * (T // L) * N * 4,
+                         + 2 * b * T * H * N * 4 + b * H * N * 4 + b * H * (-(-T // L)) * N * 4,
         "k_m1_channel_sum": b * T * H * N * 4 + t["B"],
         "k_m1_dA_sum": b * H * N * 4 + t["A"],
     }
@@ -480,12 +480,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for ncu captures; not a bench line)")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="override the workload's T (not a multiple of the chunk: a tail chunk); not the headline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = CONFIGS[args.workload]
     if args.batch is not None:
         cfg = scaled(cfg, batch=args.batch)
+    if args.seqlen is not None:
+        cfg = scaled(cfg, seqlen=args.seqlen)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   SSD_OK = 0,
   SSD_ERR_INVALID_ARG = 1, /* NULL where a buffer is required, unknown enum, negative size */
-  SSD_ERR_SHAPE = 2,       /* sizes the method does not allow (T % chunk, H % G, limits) */
+  SSD_ERR_SHAPE = 2,       /* sizes the method does not allow (H % G, limits of this build) */
   SSD_ERR_DTYPE = 3,       /* io dtype not supported for this variant */
   SSD_ERR_ALIGNMENT = 4,   /* a pointer is not 16-byte aligned */
   SSD_ERR_WORKSPACE = 5,   /* ws_bytes smaller than ssd_workspace_size() */
@@ -88,12 +88,20 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  *              Mamba-1 (B, C are shared by all channels) and MIMO (B, C are
  *              per head).
  *   chunk      L, the chunk length of the chunkwise algorithm (Mamba-2,
- *              MIMO): T % L == 0 is required (the chunked layout builds T as
- *              nchunks * chunk_len).  For Mamba-1 it is the replay segment of
- *              the backward and must also divide T.
+ *              MIMO), 1 <= L <= 256; for Mamba-1 the replay segment of the
+ *              backward.  T need not be a multiple of L: the sequence is cut
+ *              into nc = ceil(T / L) chunks, and the last one holds the
+ *              remaining T - (nc - 1) L steps (a tail chunk).  The kernels
+ *              treat its missing steps as steps with dt' = 0 (da = 0) and
+ *              x = B = C = dy = 0, which leave the state unchanged, and store
+ *              nothing for them, so every output equals the serial recurrence
+ *              over the T real steps.  The chunked layout of the pages builds T
+ *              as nchunks * chunk_len; the tail chunk is this library's
+ *              widening, which lets a caller stream a sequence in pieces of
+ *              any length through s0 / ds_final.
  *   mimo_rank  R (MIMO); must be 1 for the other variants.
  * Limits of this build: P <= 256, N <= 256, L * R <= 256 (Mamba-2, MIMO);
- * N <= 32 (Mamba-1).  Larger sizes return SSD_ERR_SHAPE.
+ * N <= 32, L <= 256 (Mamba-1).  Larger sizes return SSD_ERR_SHAPE.
  */
 typedef struct {
   int32_t variant;

@@ -15,6 +15,10 @@ double_ssd/ssd/serial_recalculated):
   mask keeps source s for target t iff ⌊s/R⌋ ≤ ⌊t/R⌋ and is applied as −inf
   before the exponential ("ORANGE backward").
 
+The page builds T as nchunks · chunk_len.  Here T may be any length: the last
+chunk is shorter (T − (nc − 1)·L steps) and every chunk formula runs on the
+steps it has; its chunk end is its own last step.
+
 The backward follows the page's order: recompute K1..K4, walk the chunks in
 reverse carrying the state gradient (BLUE + ORANGE + K4 backward), then the
 K3, K2 and K1 backwards and the sums of all contributions.
@@ -46,14 +50,15 @@ def _unit_forward(v, da, Bm, Cm, s0, L):
     Returns y [T,R,P], s_final [P,N] and the chunk-input states [nc,P,N]."""
     T, R, P = v.shape
     N = Bm.shape[2]
-    nc = T // L
-    LR = L * R
-    keep = _mask_mimo(L, R)
+    nc = -(-T // L)
     S = s0.copy()
     y = np.empty_like(v)
     S_in = np.empty((nc, P, N))
     for c in range(nc):
-        sl = slice(c * L, (c + 1) * L)
+        sl = slice(c * L, min((c + 1) * L, T))
+        Lc = sl.stop - sl.start
+        LR = Lc * R
+        keep = _mask_mimo(Lc, R)
         vf = v[sl].reshape(LR, P)
         Bf = Bm[sl].reshape(LR, N)
         Cf = Cm[sl].reshape(LR, N)
@@ -66,7 +71,7 @@ def _unit_forward(v, da, Bm, Cm, s0, L):
         decay_in = np.exp(diff)
         y_blue = np.exp(cum_f)[:, None] * (Cf @ S.T)     # K5 BLUE
         y_orange = (CB * decay_in) @ vf                  # K5 ORANGE
-        y[sl] = (y_blue + y_orange).reshape(L, R, P)
+        y[sl] = (y_blue + y_orange).reshape(Lc, R, P)
         S_in[c] = S
         S = np.exp(cum[-1]) * S + intra                  # K4
     return y, S, S_in
@@ -76,9 +81,7 @@ def _unit_backward(dy, dS_final, v, da, Bm, Cm, s0, L):
     """Recompute backward of one unit; returns dv, dda, dB, dC, ds0."""
     T, R, P = v.shape
     N = Bm.shape[2]
-    nc = T // L
-    LR = L * R
-    keep = _mask_mimo(L, R)
+    nc = -(-T // L)
     _, _, S_in = _unit_forward(v, da, Bm, Cm, s0, L)     # recompute K1..K4
     dv = np.zeros_like(v)
     dda = np.zeros_like(da)
@@ -86,7 +89,10 @@ def _unit_backward(dy, dS_final, v, da, Bm, Cm, s0, L):
     dC = np.zeros_like(Cm)
     dS = dS_final.copy()
     for c in reversed(range(nc)):
-        sl = slice(c * L, (c + 1) * L)
+        sl = slice(c * L, min((c + 1) * L, T))
+        Lc = sl.stop - sl.start
+        LR = Lc * R
+        keep = _mask_mimo(Lc, R)
         vf = v[sl].reshape(LR, P)
         Bf = Bm[sl].reshape(LR, N)
         Cf = Cm[sl].reshape(LR, N)
@@ -124,12 +130,12 @@ def _unit_backward(dy, dS_final, v, da, Bm, Cm, s0, L):
         dC_k2 = dCB @ Bf
         dB_k2 = dCB.T @ Cf
         # fold the fused positions back onto the chunk's L steps, then K1
-        d_cum = d_cum_f.reshape(L, R).sum(axis=1)
+        d_cum = d_cum_f.reshape(Lc, R).sum(axis=1)
         d_cum[-1] += d_cum_last
         dda[sl] = np.cumsum(d_cum[::-1])[::-1]           # suffix sums
-        dv[sl] = (dv_orange + dv_k3).reshape(L, R, P)
-        dB[sl] = (dB_k2 + dB_k3).reshape(L, R, N)
-        dC[sl] = (dC_k2 + dC_blue).reshape(L, R, N)
+        dv[sl] = (dv_orange + dv_k3).reshape(Lc, R, P)
+        dB[sl] = (dB_k2 + dB_k3).reshape(Lc, R, N)
+        dC[sl] = (dC_k2 + dC_blue).reshape(Lc, R, N)
         dS = a_end * dS + dS_blue
     return dv, dda, dB, dC, dS
 

@@ -31,11 +31,11 @@ ssd_status make_dims(const ssd_problem* pr, Dims* d) {
   d->H = (int)pr->nheads;
   d->P = (int)pr->headdim;
   d->N = (int)pr->dstate;
-  d->L = (int)(pr->chunk < pr->seqlen ? pr->chunk : pr->seqlen);
-  if (pr->chunk > pr->seqlen) return SSD_ERR_SHAPE;
   d->R = (int)pr->mimo_rank;
-  if (pr->seqlen % pr->chunk != 0) return SSD_ERR_SHAPE;  // T = nchunks * chunk_len
-  d->nc = d->T / d->L;
+  if (pr->chunk > 256) return SSD_ERR_SHAPE;
+  // nc chunks of `chunk` steps; the last holds the remaining T - (nc - 1) * chunk steps
+  d->L = (int)pr->chunk;
+  d->nc = (int)((pr->seqlen + pr->chunk - 1) / pr->chunk);
   switch (pr->variant) {
     case SSD_MAMBA2:
       if (pr->ngroups < 1 || pr->nheads % pr->ngroups != 0) return SSD_ERR_SHAPE;
@@ -55,8 +55,6 @@ ssd_status make_dims(const ssd_problem* pr, Dims* d) {
   if (pr->variant != SSD_MAMBA1) {
     if (pr->headdim > 256 || pr->dstate > 256) return SSD_ERR_SHAPE;
     if (pr->chunk * pr->mimo_rank > 256) return SSD_ERR_SHAPE;
-  } else if (pr->chunk > 256) {
-    return SSD_ERR_SHAPE;
   }
   d->LR = d->L * d->R;
   d->hpg = d->H / d->G;
@@ -158,7 +156,7 @@ const char* ssd_status_string(ssd_status s) {
   switch (s) {
     case SSD_OK: return "SSD_OK";
     case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: missing buffer or unknown enum value";
-    case SSD_ERR_SHAPE: return "SSD_ERR_SHAPE: sizes not allowed (T % chunk, H % G, limits of this build)";
+    case SSD_ERR_SHAPE: return "SSD_ERR_SHAPE: sizes not allowed (H % G, limits of this build)";
     case SSD_ERR_DTYPE: return "SSD_ERR_DTYPE: io dtype not supported for this variant";
     case SSD_ERR_ALIGNMENT: return "SSD_ERR_ALIGNMENT: a pointer is not 16-byte aligned";
     case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace smaller than ssd_workspace_size()";

@@ -109,6 +109,16 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, 
                               uint32_t box_outer);
 cudaError_t make_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
                               uint32_t b1, uint32_t b2);
+cudaError_t make_tmap_4d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+                              uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3);
+// The per-token tensors seen by the chunk tiles, with the sequence dimension
+// kept apart from the batch: a tile of the last, partial chunk of a sequence
+// (T not a multiple of 64) reads zeros past the sequence end and a store of
+// it writes nothing there.
+//   [b, T, width] bf16 (x, y, dy, dx with width = H*P): 64 x 64 boxes, coordinates (col, t, b);
+//   [b, T, G, N] bf16 (B, C): 64 x 1 x 64 x 1 boxes, coordinates (n, g, t, b).
+cudaError_t make_tmap_seq_bf16(CUtensorMap* m, const void* base, const Dims& d, uint64_t width);
+cudaError_t make_tmap_bc_bf16(CUtensorMap* m, const void* base, const Dims& d);
 
 // Mamba-1 path (fp32).
 size_t m1_forward_ws(const Dims& d);

@@ -61,13 +61,14 @@ __global__ void __launch_bounds__(kM1Threads)
   const bool act = valid && lane < m.N;
   const int bb = valid ? (int)(unit / m.D) : 0, d = valid ? (int)(unit % m.D) : 0;
   const float a_n = act ? m.A[(size_t)d * m.N + lane] : 0.f;
-  const int nseg = m.T / m.K;
+  const int nseg = (m.T + m.K - 1) / m.K;  // the last segment may be shorter (T not a multiple of K)
   const size_t ck_base = ((size_t)unit * nseg) * m.N + lane;
   // forward replay: the state entering each segment
   float s = (act && m.s0) ? m.s0[((size_t)bb * m.D + d) * m.N + lane] : 0.f;
   for (int k = 0; k < nseg; ++k) {
     if (act) ck[ck_base + (size_t)k * m.N] = s;
-    for (int j = 0; j < m.K; ++j) {
+    const int len = min(m.K, m.T - k * m.K);
+    for (int j = 0; j < len; ++j) {
       const int t = k * m.K + j;
       const size_t td = ((size_t)bb * m.T + t) * m.D + d;
       if (act) {
@@ -83,7 +84,8 @@ __global__ void __launch_bounds__(kM1Threads)
   for (int k = nseg - 1; k >= 0; --k) {
     float r = act ? ck[ck_base + (size_t)k * m.N] : 0.f;
     mine[0] = r;
-    for (int j = 0; j < m.K; ++j) {
+    const int len = min(m.K, m.T - k * m.K);
+    for (int j = 0; j < len; ++j) {
       const int t = k * m.K + j;
       const size_t td = ((size_t)bb * m.T + t) * m.D + d;
       if (act) {
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kM1Threads)
       }
       mine[(j + 1) * stride] = r;
     }
-    for (int j = m.K - 1; j >= 0; --j) {
+    for (int j = len - 1; j >= 0; --j) {
       const int t = k * m.K + j;
       const size_t td = ((size_t)bb * m.T + t) * m.D + d;
       const size_t tn = ((size_t)bb * m.T + t) * m.N + lane;
@@ -171,7 +173,7 @@ struct M1Ws {
 M1Ws carve_m1(const Dims& d, Carver& cv) {
   M1Ws w;
   const size_t units = (size_t)d.b * d.H;
-  w.ck = cv.take<float>(units * (d.T / d.L) * d.N);
+  w.ck = cv.take<float>(units * d.nc * d.N);
   w.dB_part = cv.take<float>((size_t)d.b * d.T * d.H * d.N);
   w.dC_part = cv.take<float>((size_t)d.b * d.T * d.H * d.N);
   w.dA_part = cv.take<float>((size_t)d.b * d.H * d.N);

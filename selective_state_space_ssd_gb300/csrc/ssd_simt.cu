@@ -40,12 +40,20 @@ struct Seq {
                 : (((size_t)b * T + t) * G + h / hpg) * N + n;
   }
   __device__ size_t ti(int b, int t, int h) const { return ((size_t)b * T + t) * H + h; }
+  // The last chunk may be partial (T not a multiple of L): its steps t >= T
+  // read as x = B = C = dy = 0 with dt' = 0 and da = 0 (steps that leave the
+  // state as it is), and nothing is stored for them.
+  __device__ bool in(int t) const { return t < T; }
   // v at fused position (t, r): MIMO reads it, Mamba-2 forms dt' x.
   __device__ float v(int b, int t, int r, int h, int p, float dtp) const {
+    if (!in(t)) return 0.f;
     return MIMO ? ld(x, xi(b, t, r, h, p)) : dtp * ld(x, xi(b, t, r, h, p));
   }
-  __device__ float Bm(int b, int t, int r, int h, int n) const { return ld(B, bi(b, t, r, h, n)); }
-  __device__ float Cm(int b, int t, int r, int h, int n) const { return ld(C, bi(b, t, r, h, n)); }
+  __device__ float Bm(int b, int t, int r, int h, int n) const { return in(t) ? ld(B, bi(b, t, r, h, n)) : 0.f; }
+  __device__ float Cm(int b, int t, int r, int h, int n) const { return in(t) ? ld(C, bi(b, t, r, h, n)) : 0.f; }
+  __device__ float dyv(const TIn* dy, int b, int t, int r, int h, int p) const {
+    return in(t) ? ld(dy, xi(b, t, r, h, p)) : 0.f;
+  }
 };
 
 // K1 for one chunk: s_dtp[l] = dt' (1 for MIMO), s_cum[l] = inclusive cumsum
@@ -54,6 +62,11 @@ template <typename TIn, bool MIMO>
 __device__ void chunk_scalars(const Seq<TIn, MIMO>& s, int b, int h, int c, float* s_cum, float* s_dtp) {
   for (int l = threadIdx.x; l < s.L; l += blockDim.x) {
     const int t = c * s.L + l;
+    if (!s.in(t)) {  // past the end of the sequence: dt' = 0, da = 0
+      s_dtp[l] = MIMO ? 1.f : 0.f;
+      s_cum[l] = 0.f;
+      continue;
+    }
     const float z = s.dt[s.ti(b, t, h)];
     if (MIMO) {
       s_dtp[l] = 1.f;
@@ -152,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) k_chunk_out(Seq<TIn, MIMO> s, const 
         const int lj = j / s.R, rj = j % s.R;
         diag += s_w[j] * s.v(b, c * s.L + lj, rj, h, p, s_dtp[lj]);
       }
-      st(y, s.xi(b, ti, ri, h, p), eci * off + diag);
+      if (s.in(ti)) st(y, s.xi(b, ti, ri, h, p), eci * off + diag);
     }
     __syncthreads();
   }
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) k_dS_blue(Seq<TIn, MIMO> s, const TI
     float acc = 0.f;
     for (int i = 0; i < s.LR; ++i) {
       const int l = i / s.R, r = i % s.R, t = c * s.L + l;
-      acc += ld(dy, s.xi(b, t, r, h, p)) * s_e[l] * s.Cm(b, t, r, h, n);
+      acc += s.dyv(dy, b, t, r, h, p) * s_e[l] * s.Cm(b, t, r, h, n);
     }
     out[e] = acc;
   }
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(kThreads)
       float dcb = 0.f, dd = 0.f;
       if (lj <= li) {
         float dW = 0.f, cb = 0.f;
-        for (int p = 0; p < P; ++p) dW += ld(dy, s.xi(b, ti, ri, h, p)) * s.v(b, tj, rj, h, p, s_dtp[lj]);
+        for (int p = 0; p < P; ++p) dW += s.dyv(dy, b, ti, ri, h, p) * s.v(b, tj, rj, h, p, s_dtp[lj]);
         for (int n = 0; n < N; ++n) cb += s.Cm(b, ti, ri, h, n) * s.Bm(b, tj, rj, h, n);
         const float dec = expf(s_cum[li] - s_cum[lj]);
         dcb = dW * dec;
@@ -268,11 +281,13 @@ __global__ void __launch_bounds__(kThreads)
       float k2 = 0.f;
       for (int jj = 0; jj < (li + 1) * R; ++jj) k2 += s_row[jj] * s.Bm(b, t_of(jj), jj % R, h, n);
       float blue = 0.f;
-      for (int p = 0; p < P; ++p) blue += ld(dy, s.xi(b, ti, ri, h, p)) * Sc[p * N + n];
+      for (int p = 0; p < P; ++p) blue += s.dyv(dy, b, ti, ri, h, p) * Sc[p * N + n];
       blue *= eci;
       const float v = k2 + blue;
-      if (MIMO) st(dC_io, s.bi(b, ti, ri, h, n), v);
-      else dC_dst[(((size_t)b * s.T + ti) * s.H + h) * N + n] = v;
+      if (s.in(ti)) {
+        if (MIMO) st(dC_io, s.bi(b, ti, ri, h, n), v);
+        else dC_dst[(((size_t)b * s.T + ti) * s.H + h) * N + n] = v;
+      }
       s_red[n] = s.Cm(b, ti, ri, h, n) * blue;
     }
     __syncthreads();
@@ -297,7 +312,7 @@ __global__ void __launch_bounds__(kThreads)
       float w = 0.f, dcb = 0.f;
       if (lj <= li) {
         float dW = 0.f, cb = 0.f;
-        for (int p = 0; p < P; ++p) dW += ld(dy, s.xi(b, ti, ri, h, p)) * s.v(b, tj, rj, h, p, s_dtp[lj]);
+        for (int p = 0; p < P; ++p) dW += s.dyv(dy, b, ti, ri, h, p) * s.v(b, tj, rj, h, p, s_dtp[lj]);
         for (int n = 0; n < N; ++n) cb += s.Cm(b, ti, ri, h, n) * s.Bm(b, tj, rj, h, n);
         const float dec = expf(s_cum[li] - s_cum[lj]);
         w = cb * dec;
@@ -310,12 +325,14 @@ __global__ void __launch_bounds__(kThreads)
     const float dec_end = s_dec[lj];
     for (int p = threadIdx.x; p < P; p += blockDim.x) {
       float dvo = 0.f;
-      for (int ii = lj * R; ii < LR; ++ii) dvo += s_row[ii] * ld(dy, s.xi(b, t_of(ii), ii % R, h, p));
+      for (int ii = lj * R; ii < LR; ++ii) dvo += s_row[ii] * s.dyv(dy, b, t_of(ii), ii % R, h, p);
       float ddv = 0.f;  // d decayed_v
       for (int n = 0; n < N; ++n) ddv += s.Bm(b, tj, rj, h, n) * dSn[p * N + n];
       const float dvv = dvo + dec_end * ddv;
-      if (MIMO) st(dx, s.xi(b, tj, rj, h, p), dvv);
-      else dv_ws[s.xi(b, tj, rj, h, p)] = dvv;
+      if (s.in(tj)) {
+        if (MIMO) st(dx, s.xi(b, tj, rj, h, p), dvv);
+        else dv_ws[s.xi(b, tj, rj, h, p)] = dvv;
+      }
       s_red[p] = ddv * s.v(b, tj, rj, h, p, s_dtp[lj]);
     }
     for (int n = threadIdx.x; n < N; n += blockDim.x) {
@@ -324,8 +341,10 @@ __global__ void __launch_bounds__(kThreads)
       float k3 = 0.f;
       for (int p = 0; p < P; ++p) k3 += s.v(b, tj, rj, h, p, s_dtp[lj]) * dSn[p * N + n];
       const float v = k2 + dec_end * k3;
-      if (MIMO) st(dB_io, s.bi(b, tj, rj, h, n), v);
-      else dB_dst[(((size_t)b * s.T + tj) * s.H + h) * N + n] = v;
+      if (s.in(tj)) {
+        if (MIMO) st(dB_io, s.bi(b, tj, rj, h, n), v);
+        else dB_dst[(((size_t)b * s.T + tj) * s.H + h) * N + n] = v;
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -356,15 +375,18 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---- leaves
   if (MIMO) {
-    for (int l = threadIdx.x; l < L; l += blockDim.x) ddt_or_dda[s.ti(b, c * L + l, h)] = s_dda[l];
+    for (int l = threadIdx.x; l < L; l += blockDim.x)
+      if (s.in(c * L + l)) ddt_or_dda[s.ti(b, c * L + l, h)] = s_dda[l];
   } else {
     for (int e = threadIdx.x; e < L * P; e += blockDim.x) {
       const int l = e / P, p = e % P;
+      if (!s.in(c * L + l)) continue;
       const size_t idx = s.xi(b, c * L + l, 0, h, p);
       st(dx, idx, s_dtp[l] * dv_ws[idx]);
     }
     for (int l = threadIdx.x; l < L; l += blockDim.x) {
       const int t = c * L + l;
+      if (!s.in(t)) continue;
       float acc = 0.f;
       for (int p = 0; p < P; ++p) {
         const size_t idx = s.xi(b, t, 0, h, p);

@@ -199,20 +199,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       hp.seek(geo, q0 + 2);
       for (int q = 0; q < nh; ++q, hr.next(geo), hp.next(geo)) {
         const int j = q & 1;
-        const int row = hr.b * T + hr.c * kL;
+        const int t0 = hr.c * kL;
         if (q + 2 < nh) {  // warm L2 with the tiles of head q + 2 while the rings are still busy
-          const int prow = hp.b * T + hp.c * kL;
           const int psrow = (int)((((size_t)hp.b * H + hp.h(geo)) * nc + hp.c) * kN);
-          tma_prefetch_2d(&tm_x, hp.h(geo) * kP, prow);
-          tma_prefetch_2d(&tm_dy, hp.h(geo) * kP, prow);
+          tma_prefetch_3d(&tm_x, hp.h(geo) * kP, hp.c * kL, hp.b);
+          tma_prefetch_3d(&tm_dy, hp.h(geo) * kP, hp.c * kL, hp.b);
           tma_prefetch_2d(&tm_S, 0, psrow);
           tma_prefetch_2d(&tm_dS, 0, psrow);
         }
         const int x3 = q % 3, xr = q / 3;
         if (q >= 3 && !mbar_wait(&sm.xy_empty[x3], (xr - 1) & 1, status, 102)) break;
         mbar_expect_tx(&sm.xy_full[x3], 2 * kTileLP);
-        tma_load_2d(sm.xy[x3].x, &tm_x, hr.h(geo) * kP, row, &sm.xy_full[x3]);
-        tma_load_2d(sm.xy[x3].dy, &tm_dy, hr.h(geo) * kP, row, &sm.xy_full[x3]);
+        tma_load_3d(sm.xy[x3].x, &tm_x, hr.h(geo) * kP, t0, hr.b, &sm.xy_full[x3]);
+        tma_load_3d(sm.xy[x3].dy, &tm_dy, hr.h(geo) * kP, t0, hr.b, &sm.xy_full[x3]);
         if (q >= 2 && !mbar_wait(&sm.sd_empty[j], ((q >> 1) - 1) & 1, status, 99)) break;
         const int srow = (int)((((size_t)hr.b * H + hr.h(geo)) * nc + hr.c) * kN);
         mbar_expect_tx(&sm.sd_full[j], 2 * kTileNP);
@@ -225,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (seg >= 1 && !mbar_wait(&sm.chunk_empty, (seg - 1) & 1, status, 101)) break;
           mbar_expect_tx(&sm.chunk_full, 4 * kTileLP);
           for (int a = 0; a < 2; ++a) {
-            tma_load_3d(sm.BC[2 * a], &tm_B, a * 64, hr.g, row, &sm.chunk_full);
-            tma_load_3d(sm.BC[2 * a + 1], &tm_C, a * 64, hr.g, row, &sm.chunk_full);
+            tma_load_4d(sm.BC[2 * a], &tm_B, a * 64, hr.g, t0, hr.b, &sm.chunk_full);
+            tma_load_4d(sm.BC[2 * a + 1], &tm_C, a * 64, hr.g, t0, hr.b, &sm.chunk_full);
           }
         }
       }
@@ -319,9 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (q >= 4 && !mbar_wait(&sm.sc_free[k], ((q >> 2) - 1) & 1, status, 105)) break;
       const int h = hr.h(geo);
       const float A_h = prm.A[h];
-      const size_t rr = (size_t)hr.b * T + hr.c * kL + t0;
-      // streaming loads: these strided reads must not push CB (read by E) out of L1
-      const float z0 = __ldcs(prm.dt_raw + rr * H + h), z1 = __ldcs(prm.dt_raw + (rr + 1) * H + h);
+      const int tt = hr.c * kL + t0;
+      const size_t rr = (size_t)hr.b * T + tt;
+      // streaming loads: these strided reads must not push CB (read by E) out of L1.  Steps past the end of
+      // the sequence (a partial last chunk) take dt_raw = -inf: dt' = 0 and da = 0, so they hold the state
+      // and (with their zero-filled x, dy, B, C rows) add nothing to any gradient.
+      const float z0 = tt < T ? __ldcs(prm.dt_raw + rr * H + h) : -INFINITY;
+      const float z1 = tt + 1 < T ? __ldcs(prm.dt_raw + (rr + 1) * H + h) : -INFINITY;
       const float d0 = softplus_fast(z0), d1 = softplus_fast(z1);
       const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
       float inc = a1;
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         if (named_bar_or(kBarPool, kPoolThreads, !ok)) break;
         if (tid == kLead && has_prev) {
-          tma_store_2d(&tm_dx, sm.dxs, co.h(geo) * kP, co.b * T + co.c * kL);
+          tma_store_3d(&tm_dx, sm.dxs, co.h(geo) * kP, co.c * kL, co.b);
           tma_store_commit();
           mbar_arrive(&sm.tmem_free[(i - 1) & 1]);
           mbar_arrive(&sm.xy_empty[(i - 1) % 3]);
@@ -574,9 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float dda0 = suf, dda1 = suf - dc0;
           const int h = co.h(geo);
-          const size_t rr = (size_t)co.b * T + co.c * kL + t0;
-          __stcs(prm.ddt_raw + rr * H + h, (vx0 + A_h * dda0) * sigmoid_fast(sm.z[kp][t0]));
-          __stcs(prm.ddt_raw + (rr + 1) * H + h, (vx1 + A_h * dda1) * sigmoid_fast(sm.z[kp][t1]));
+          const int tt = co.c * kL + t0;
+          const size_t rr = (size_t)co.b * T + tt;
+          if (tt < T) __stcs(prm.ddt_raw + rr * H + h, (vx0 + A_h * dda0) * sigmoid_fast(sm.z[kp][t0]));
+          if (tt + 1 < T) __stcs(prm.ddt_raw + (rr + 1) * H + h, (vx1 + A_h * dda1) * sigmoid_fast(sm.z[kp][t1]));
           float dAp = dda0 * sm.dtp[kp][t0] + dda1 * sm.dtp[kp][t1];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
@@ -642,6 +646,7 @@ __global__ void __launch_bounds__(256) k_bwdc_sums(const float* __restrict__ dB_
       sc.x += vc.x, sc.y += vc.y, sc.z += vc.z, sc.w += vc.w;
     }
     const int t = (4 * e4) / kN, n = (4 * e4) % kN;
+    if (c * kL + t >= T) continue;  // past the end of the sequence (a partial last chunk)
     const size_t o = (((size_t)bb * T + c * kL + t) * G + g) * kN + n;
     *reinterpret_cast<uint2*>(dB + o) = make_uint2(pack_bf16(sb.x, sb.y), pack_bf16(sb.z, sb.w));
     *reinterpret_cast<uint2*>(dC + o) = make_uint2(pack_bf16(sc.x, sc.y), pack_bf16(sc.z, sc.w));
@@ -720,14 +725,13 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   const ScanSide rev{a.dy, a.ds_final, a.ds0, w.dstates};
   cudaError_t e = tc_scans(d, a.states_in ? nullptr : &fwd, &rev, a.B, a.C, a.dt_raw, a.A, w.CB, status, st);
   if (e != cudaSuccess) return e;
-  const uint64_t rows = (uint64_t)d.b * d.T;
   const uint64_t srows = (uint64_t)d.b * d.H * d.nc * kN;
   CUtensorMap tx, tdy, tdx, tb, tcm, ts, tds;
-  e = make_tmap_2d_bf16(&tx, a.x, (uint64_t)d.H * kP, rows, 64, 64);
-  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdy, a.dy, (uint64_t)d.H * kP, rows, 64, 64);
-  if (e == cudaSuccess) e = make_tmap_2d_bf16(&tdx, a.dx, (uint64_t)d.H * kP, rows, 64, 64);
-  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tb, a.B, d.N, d.G, rows, 64, 1, 64);
-  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tcm, a.C, d.N, d.G, rows, 64, 1, 64);
+  e = make_tmap_seq_bf16(&tx, a.x, d, (uint64_t)d.H * kP);
+  if (e == cudaSuccess) e = make_tmap_seq_bf16(&tdy, a.dy, d, (uint64_t)d.H * kP);
+  if (e == cudaSuccess) e = make_tmap_seq_bf16(&tdx, a.dx, d, (uint64_t)d.H * kP);
+  if (e == cudaSuccess) e = make_tmap_bc_bf16(&tb, a.B, d);
+  if (e == cudaSuccess) e = make_tmap_bc_bf16(&tcm, a.C, d);
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, states, kP, srows, 64, kN);
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&tds, w.dstates, kP, srows, 64, kN);
   if (e != cudaSuccess) return e;

@@ -161,18 +161,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       PairCursor u;
       u.seek(geo, q0, q1);
       for (int k = 0; u.a.f < q1; ++k, u.next(geo, q1)) {
-        const int r = k & 1, row = u.a.b * T + u.a.c * kL;
+        const int r = k & 1, t0 = u.a.c * kL;
         if (u.a.first(q0)) {
           ++seg;
           if (seg >= 1 && !mbar_wait(&sm.chunk_empty, (seg - 1) & 1, status, 201)) break;
           mbar_expect_tx(&sm.chunk_full, 4 * kTileLP);
-          for (int a = 0; a < 4; ++a) tma_load_3d(sm.CC[a], &tm_C, (a >> 1) * 64, u.a.g, row, &sm.chunk_full);
+          for (int a = 0; a < 4; ++a) tma_load_4d(sm.CC[a], &tm_C, (a >> 1) * 64, u.a.g, t0, u.a.b, &sm.chunk_full);
         }
         if (k >= 2 && !mbar_wait(&sm.slot_empty[r], ((k >> 1) - 1) & 1, status, 202)) break;
         mbar_expect_tx(&sm.slot_full[r], u.n * (kTileLP + kTileNP));
         for (int i = 0; i < u.n; ++i) {
           const int h = u.a.h(geo) + i;
-          tma_load_2d(sm.x[r][i], &tm_x, h * kP, row, &sm.slot_full[r]);
+          tma_load_3d(sm.x[r][i], &tm_x, h * kP, t0, u.a.b, &sm.slot_full[r]);
           tma_load_2d(sm.S[r][i], &tm_S, 0, (int)((((size_t)u.a.b * H + h) * nc + u.a.c) * kN), &sm.slot_full[r]);
         }
       }
@@ -212,15 +212,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ K1 scalars, up to kSc pairs ahead.  The
     //   strided dt_raw reads (and A) of pair k + 3 go out as cp.async copies into a ring while pair k is
     //   formed: global-memory latency under the kernel's own HBM load (~2 us) would otherwise set the pace
-    //   of the whole CTA.
+    //   of the whole CTA.  Steps past the end of the sequence (a partial last chunk) get dt_raw = -inf,
+    //   i.e. dt' = 0: their W' columns vanish, and their y rows are not stored.
     const int t0 = 2 * lane, t1 = t0 + 1;
     auto fetch = [&](const PairCursor& c, int slot) {
       if (c.a.f < q1) {
         const int h0 = c.a.h(geo);
-        const size_t rr = (size_t)c.a.b * T + c.a.c * kL + t0;
+        const int tt = c.a.c * kL + t0;
+        const size_t rr = (size_t)c.a.b * T + tt;
         for (int i = 0; i < c.n; ++i) {
-          cp_async4(&sm.dtraw[slot][i][t0], prm.dt_raw + rr * H + h0 + i);
-          cp_async4(&sm.dtraw[slot][i][t1], prm.dt_raw + (rr + 1) * H + h0 + i);
+          if (tt < T) cp_async4(&sm.dtraw[slot][i][t0], prm.dt_raw + rr * H + h0 + i);
+          else sm.dtraw[slot][i][t0] = -INFINITY;
+          if (tt + 1 < T) cp_async4(&sm.dtraw[slot][i][t1], prm.dt_raw + (rr + 1) * H + h0 + i);
+          else sm.dtraw[slot][i][t1] = -INFINITY;
         }
         if (lane < c.n) cp_async4(&sm.araw[slot][lane], prm.A + h0 + lane);
       }
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (has_s) {
           const int rs = (k - 3) & 1;
           for (int i = 0; i < us.n; ++i)
-            tma_store_2d(&tm_y, sm.y[rs][i], (us.a.h(geo) + i) * kP, us.a.b * T + us.a.c * kL);
+            tma_store_3d(&tm_y, sm.y[rs][i], (us.a.h(geo) + i) * kP, us.a.c * kL, us.a.b);
           tma_store_commit();
         }
       }
@@ -445,12 +449,11 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t s
   const ScanSide fwd{a.x, a.s0, a.s_final, states};
   cudaError_t e = tc_scans(d, &fwd, nullptr, a.B, a.C, a.dt_raw, a.A, w.CB, status, st);
   if (e != cudaSuccess) return e;
-  const uint64_t rows = (uint64_t)d.b * d.T;
   CUtensorMap tx, tcm, ts, ty;
-  e = make_tmap_2d_bf16(&tx, a.x, (uint64_t)d.H * kP, rows, 64, 64);
-  if (e == cudaSuccess) e = make_tmap_3d_bf16(&tcm, a.C, d.N, d.G, rows, 64, 1, 64);
+  e = make_tmap_seq_bf16(&tx, a.x, d, (uint64_t)d.H * kP);
+  if (e == cudaSuccess) e = make_tmap_bc_bf16(&tcm, a.C, d);
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&ts, states, kP, (uint64_t)d.b * d.H * d.nc * kN, 64, kN);
-  if (e == cudaSuccess) e = make_tmap_2d_bf16(&ty, a.y, (uint64_t)d.H * kP, rows, 64, 64);
+  if (e == cudaSuccess) e = make_tmap_seq_bf16(&ty, a.y, d, (uint64_t)d.H * kP);
   if (e != cudaSuccess) return e;
   const long long total = (long long)d.b * d.nc * d.H;
   const int grid = (int)(total < sms ? total : sms);

@@ -97,7 +97,7 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = prm.T, H = prm.H, nc = prm.nc;
   const int g = h / prm.hpg;
-  const int row0 = b * T;
+  const size_t row0 = (size_t)b * T;
   const size_t unit = (size_t)b * H + h;
   int* status = prm.status;
   auto chunk_of = [&](int r) { return kRev ? nc - 1 - r : r; };
@@ -137,11 +137,11 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
         const int sk = r & 1, c = chunk_of(r);
         if (r >= kStU && !mbar_wait(&sm.empty_u[su], pu ^ 1, status, 81)) break;
         mbar_expect_tx(&sm.full_u[su], kTileLP);
-        tma_load_2d(sm.u[su], &tm_u, h * kP, row0 + c * kL, &sm.full_u[su]);
+        tma_load_3d(sm.u[su], &tm_u, h * kP, c * kL, b, &sm.full_u[su]);
         if (r >= kStK && !mbar_wait(&sm.empty_k[sk], ((r >> 1) - 1) & 1, status, 80)) break;
         mbar_expect_tx(&sm.full_k[sk], kTileLN);
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(sm.k[sk] + a * (kTileLN / 2), &tm_k, a * 64, g, row0 + c * kL, &sm.full_k[sk]);
+          tma_load_4d(sm.k[sk] + a * (kTileLN / 2), &tm_k, a * 64, g, c * kL, b, &sm.full_k[sk]);
         if (++su == kStU) su = 0, pu ^= 1;
       }
     }
@@ -173,14 +173,17 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
     }
   } else if (warp == kWarpScal) {
     // ------------------------------------------------------------ K1 scalars.  The dt_raw reads (64
-    //   strided floats per chunk) are issued two chunks ahead of their use.
+    //   strided floats per chunk) are issued two chunks ahead of their use.  Steps past the end of the
+    //   sequence (the tail of a partial last chunk) read dt_raw = -inf: dt' = 0 and da = 0 there, so they
+    //   leave the state as it is, and their U rows are zeros (TMA fill) as well.
     const float A_h = prm.A[h];
     const int t0 = 2 * lane, t1 = t0 + 1;
     auto fetch = [&](int r, float& z0, float& z1) {
       if (r < nc) {
-        const size_t rr = (size_t)row0 + chunk_of(r) * kL + t0;
-        z0 = prm.dt_raw[rr * H + h];
-        z1 = prm.dt_raw[(rr + 1) * H + h];
+        const int tt = chunk_of(r) * kL + t0;
+        const size_t rr = (size_t)row0 + tt;
+        z0 = tt < T ? prm.dt_raw[rr * H + h] : -INFINITY;
+        z1 = tt + 1 < T ? prm.dt_raw[(rr + 1) * H + h] : -INFINITY;
       }
     };
     auto step = [&](int r, float z0, float z1) -> bool {
@@ -328,7 +331,7 @@ struct CbJob {
   CUtensorMap c, b;
   float* CB;  // [b, nc, G, L, L]
   int* status;
-  int T, G, nc;
+  int G, nc;
 };
 
 struct alignas(1024) CbSmem {
@@ -344,7 +347,6 @@ __device__ __forceinline__ void cb_tile(const CbJob& job, int k, uint8_t* smem) 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int g = k % job.G, bc = k / job.G;
   const int c = bc % job.nc, b = bc / job.nc;
-  const int row = b * job.T + c * kL;
   int* status = job.status;
   if (tid == 0) {
     mbar_init(&sm.full, 1);
@@ -359,8 +361,8 @@ __device__ __forceinline__ void cb_tile(const CbJob& job, int k, uint8_t* smem) 
   if (tid == 0) {
     mbar_expect_tx(&sm.full, 4 * kL * 64 * 2);
     for (int a = 0; a < 2; ++a) {
-      tma_load_3d(sm.C[a], &job.c, 64 * a, g, row, &sm.full);
-      tma_load_3d(sm.B[a], &job.b, 64 * a, g, row, &sm.full);
+      tma_load_4d(sm.C[a], &job.c, 64 * a, g, c * kL, b, &sm.full);
+      tma_load_4d(sm.B[a], &job.b, 64 * a, g, c * kL, b, &sm.full);
     }
     if (mbar_wait(&sm.full, 0, status, 61)) {
       tc_fence_after();
@@ -451,7 +453,6 @@ size_t tc_scan_states_bytes(const Dims& d) { return (size_t)d.b * d.H * d.nc * k
 
 cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, const void* B, const void* C,
                      const float* dt_raw, const float* A, float* CB, int* status, cudaStream_t st) {
-  const uint64_t rows = (uint64_t)d.b * d.T;
   const uint64_t srows = (uint64_t)d.b * d.H * d.nc * kN;
   const long long chains = (long long)d.b * d.H, tiles = (long long)d.b * d.nc * d.G;
   if ((fwd ? chains : 0) + (rev ? chains : 0) + tiles > 0x7fffffffll) return cudaErrorInvalidConfiguration;
@@ -464,17 +465,16 @@ cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, co
     const ScanSide* s = sides[r];
     if (!s) continue;
     ScanJob& j = *jobs[r];
-    e = make_tmap_2d_bf16(&j.u, s->u, (uint64_t)d.H * kP, rows, 64, 64);
-    if (e == cudaSuccess) e = make_tmap_3d_bf16(&j.k, r == 0 ? B : C, d.N, d.G, rows, 64, 1, 64);
+    e = make_tmap_seq_bf16(&j.u, s->u, d, (uint64_t)d.H * kP);
+    if (e == cudaSuccess) e = make_tmap_bc_bf16(&j.k, r == 0 ? B : C, d);
     if (e == cudaSuccess) e = make_tmap_2d_bf16(&j.out, s->states, kP, srows, 64, 32);
     j.prm = ScanParams{dt_raw, A, s->init, s->fin, status, d.T, d.H, d.hpg, d.nc};
   }
-  if (e == cudaSuccess) e = make_tmap_3d_bf16(&job.cb.c, C, d.N, d.G, rows, 64, 1, 64);
-  if (e == cudaSuccess) e = make_tmap_3d_bf16(&job.cb.b, B, d.N, d.G, rows, 64, 1, 64);
+  if (e == cudaSuccess) e = make_tmap_bc_bf16(&job.cb.c, C, d);
+  if (e == cudaSuccess) e = make_tmap_bc_bf16(&job.cb.b, B, d);
   if (e != cudaSuccess) return e;
   job.cb.CB = CB;
   job.cb.status = status;
-  job.cb.T = d.T;
   job.cb.G = d.G;
   job.cb.nc = d.nc;
   job.n_fwd = fwd ? (int)chains : 0;

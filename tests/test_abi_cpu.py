@@ -63,11 +63,14 @@ def test_workspace_query_accepts_every_config(cuda_lib, name):
 
 
 @pytest.mark.parametrize("over,code", [
-    (dict(seqlen=100), 2),                  # T % chunk != 0
     (dict(ngroups=3), 2),                   # H % G != 0
     (dict(headdim=0), 2),
     (dict(dstate=300), 2),                  # beyond this build's limit
-    (dict(chunk=128), 2),                   # chunk > T is not allowed (T = 64)
+    (dict(chunk=512), 2),                   # chunk beyond this build's limit
+    (dict(chunk=0), 2),
+    (dict(seqlen=0), 2),
+    (dict(seqlen=100), 0),                  # T % chunk != 0: a tail chunk of 4 steps
+    (dict(chunk=128), 0),                   # chunk > T: one partial chunk
 ])
 def test_shape_validation(cuda_lib, over, code):
     cfg = scaled(CONFIGS["mamba2_tiny_fp32"], **over)
@@ -158,3 +161,12 @@ def test_states_stash_validation(cuda_lib):
     st = cuda_lib.ssd_backward_stashed(ctypes.byref(small), fake, fake, fake, fake, fake, fake, fake, fake, need_s,
                                        fake, fake, fake, fake, fake, fake, fake, need_b, None)
     assert st == 2
+
+
+def test_tail_chunk_sizes_the_workspace_by_ceil(cuda_lib):
+    """T not a multiple of the chunk: the states of nc = ceil(T / L) chunks."""
+    tc = CONFIGS["mamba2_2p7b_bf16"]
+    full = binding.ssd_states_size(binding.problem(scaled(tc, seqlen=4096)))
+    ragged = binding.ssd_states_size(binding.problem(scaled(tc, seqlen=4096 - 63)))
+    assert ragged == full
+    assert binding.ssd_states_size(binding.problem(scaled(tc, seqlen=4096 + 1))) == full * 65 // 64

@@ -39,6 +39,16 @@ SMALL = {
                           mimo_rank=3),
     "mimo_fp32": scaled(MIMO, dtype="f32", batch=1, seqlen=128, nheads=2, ngroups=2, headdim=16, dstate=32,
                         chunk=32),
+    # a tail chunk (T not a multiple of the chunk length): tensor-core path with tails of 17 and 63 steps and
+    # a sequence shorter than one chunk; the CUDA-core paths of every variant
+    "m2_bf16_tail": scaled(M2_BF16, batch=2, seqlen=3 * 64 + 17, nheads=4, ngroups=2),
+    "m2_bf16_tail63": scaled(M2_BF16, batch=3, seqlen=127, nheads=3),
+    "m2_bf16_short": scaled(M2_BF16, batch=3, seqlen=40, nheads=2),
+    "m2_fp32_tail": dict(variant="mamba2", dtype="f32", batch=2, seqlen=100, nheads=6, headdim=5, dstate=7,
+                         ngroups=3, chunk=32, mimo_rank=1),
+    "m1_tail": scaled(M1, batch=2, seqlen=100, nheads=40, chunk=32),
+    "mimo_tail": scaled(MIMO, batch=2, seqlen=50, nheads=2, ngroups=2, headdim=20, dstate=24, chunk=16,
+                        mimo_rank=3),
 }
 
 
@@ -69,7 +79,7 @@ def test_null_s0_equals_zero_state(name):
     compare(cfg, a, run_oracle(cfg, cpu))
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "m2_bf16_tiles", "m1_small", "mimo_bf16_tiles"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "m2_bf16_tiles", "m1_small", "mimo_bf16_tiles", "m2_bf16_tail"])
 def test_backward_is_bitwise_deterministic(name):
     cfg = SMALL[name]
     dev = to_device(synth.make_inputs(cfg, seed=3))
@@ -80,7 +90,7 @@ def test_backward_is_bitwise_deterministic(name):
             assert torch.equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("name", ["m2_bf16_tiles", "m2_bf16_split_runs", "full_2p7b"])
+@pytest.mark.parametrize("name", ["m2_bf16_tiles", "m2_bf16_split_runs", "m2_bf16_tail", "full_2p7b"])
 def test_stashed_states_give_the_recompute_bits(name):
     """ssd_forward_stash returns ssd_forward's bits and a chunk-state stash;
     ssd_backward_stashed from that stash returns ssd_backward's bits (which the
@@ -100,8 +110,8 @@ def test_stashed_states_give_the_recompute_bits(name):
         for k in g:
             assert torch.equal(g[k], g2[k]), k
         # the stash's first tile of every (batch, head) is s0 in bf16, laid out [N][P]
-        st = states.view(torch.bfloat16).view(cfg["batch"], cfg["nheads"], cfg["seqlen"] // cfg["chunk"],
-                                              cfg["dstate"], cfg["headdim"])
+        nc = -(-cfg["seqlen"] // cfg["chunk"])
+        st = states.view(torch.bfloat16).view(cfg["batch"], cfg["nheads"], nc, cfg["dstate"], cfg["headdim"])
         want = torch.zeros_like(st[:, :, 0]) if zero_s0 else dev["s0"].transpose(-1, -2).to(torch.bfloat16)
         assert torch.equal(st[:, :, 0], want)
 
@@ -116,14 +126,16 @@ def test_zero_seed_and_zero_dy():
     compare(cfg, gpu, run_oracle(cfg, cpu))
 
 
-def test_chaining_two_calls_equals_one():
-    """Splitting T at a chunk boundary and chaining s_final -> s0 (forward) and
-    ds0 -> ds_final (backward) reproduces one call."""
+@pytest.mark.parametrize("T0", [128, 100])
+def test_chaining_two_calls_equals_one(T0):
+    """Splitting T and chaining s_final -> s0 (forward) and ds0 -> ds_final
+    (backward) reproduces one call: at a chunk boundary, and at T0 = 100,
+    where both pieces end in a tail chunk (100 = 64 + 36, 156 = 2 * 64 + 28)."""
     cfg = SMALL["m2_bf16_tiles"]
     cpu = synth.make_inputs(cfg, seed=5)
     dev = to_device(cpu)
-    T0 = cfg["seqlen"] // 2
     half = scaled(cfg, seqlen=T0)
+    rest = scaled(cfg, seqlen=cfg["seqlen"] - T0)
 
     def cut(t, lo, hi):
         return t[:, lo:hi].contiguous()
@@ -131,8 +143,8 @@ def test_chaining_two_calls_equals_one():
     first = {k: (v if k in ("A", "s0", "ds_final") else cut(v, 0, T0)) for k, v in dev.items()}
     second = {k: (v if k in ("A", "s0", "ds_final") else cut(v, T0, cfg["seqlen"])) for k, v in dev.items()}
     y1, s1 = binding.forward(half, first["x"], first["dt_raw"], first["A"], first["B"], first["C"], first["s0"])
-    y2, s2 = binding.forward(half, second["x"], second["dt_raw"], second["A"], second["B"], second["C"], s1)
-    g2 = binding.backward(half, second["dy"], second["ds_final"], second["x"], second["dt_raw"], second["A"],
+    y2, s2 = binding.forward(rest, second["x"], second["dt_raw"], second["A"], second["B"], second["C"], s1)
+    g2 = binding.backward(rest, second["dy"], second["ds_final"], second["x"], second["dt_raw"], second["A"],
                           second["B"], second["C"], s1)
     g1 = binding.backward(half, first["dy"], g2["ds0"], first["x"], first["dt_raw"], first["A"], first["B"],
                           first["C"], first["s0"])
@@ -170,3 +182,11 @@ def test_full_size_parity(name):
     if lhs is not None:
         scale = float((dev["dy"].double().abs() * gpu["y"].double().abs()).sum())
         assert abs(lhs - _inner(gpu["dC"], dev["C"])) < 3e-2 * scale
+
+
+def test_full_size_tail_chunk():
+    """The 2.7B layer shape with T = 4063 (63 full chunks and a tail of 31
+    steps) on the tensor-core path, against the oracle on every output."""
+    cfg = scaled(CONFIGS["mamba2_2p7b_bf16"], seqlen=4063)
+    cpu = synth.make_inputs(cfg, seed=0)
+    compare(cfg, run_gpu(cfg, to_device(cpu)), run_oracle(cfg, cpu))

@@ -113,7 +113,9 @@ def test_planted_defects_are_caught_mamba1(mutation):
 
 # --------------------------------------------------------------- chunkwise form
 @pytest.mark.parametrize("cfg", [TINY, M2_GROUPS, scaled(TINY, batch=2, seqlen=96, nheads=3, headdim=5,
-                                                            dstate=7, chunk=32)])
+                                                            dstate=7, chunk=32),
+                                 # a tail chunk: T not a multiple of the chunk length, and T below it
+                                 scaled(M2_GROUPS, seqlen=37), scaled(TINY, seqlen=13)])
 def test_serial_equals_chunkwise_mamba2(cfg):
     inp = f64(cfg)
     L = cfg["chunk"]
@@ -128,7 +130,8 @@ def test_serial_equals_chunkwise_mamba2(cfg):
         assert rel(bc[k], bs[k]) < 1e-11, k
 
 
-@pytest.mark.parametrize("cfg", [MIMO_TINY, scaled(MIMO_TINY, batch=2, seqlen=48, mimo_rank=3, chunk=16)])
+@pytest.mark.parametrize("cfg", [MIMO_TINY, scaled(MIMO_TINY, batch=2, seqlen=48, mimo_rank=3, chunk=16),
+                                 scaled(MIMO_TINY, batch=2, seqlen=19, mimo_rank=3, chunk=8)])
 def test_serial_equals_chunkwise_mimo(cfg):
     inp = f64(cfg)
     L = cfg["chunk"]
@@ -326,3 +329,41 @@ def test_backward_is_independent_of_thread_count():
     g4 = oracle.backward("mamba2", inp, nthreads=4)
     for k in g1:
         assert np.array_equal(g1[k], g4[k]), k
+
+
+@pytest.mark.parametrize("variant,cfg", [("mamba2", scaled(M2_GROUPS, seqlen=21)), ("mamba1", scaled(M1_TINY, seqlen=19)),
+                                         ("mimo", scaled(MIMO_TINY, seqlen=13))])
+def test_tail_steps_are_identity_steps(variant, cfg):
+    """The tail chunk's missing steps, read as dt_raw = -inf (dt' = 0, da = 0;
+    MIMO: da = 0) with x = B = C = dy = 0, leave the state unchanged: the serial recurrence
+    over T steps padded with such steps to the next chunk multiple gives the
+    unpadded outputs on the real steps, the same s_final and ds0, and zero
+    gradients on the padding (but MIMO's da gradient there, which does not
+    vanish at da = 0).  The kernels compute the tail chunk this way and store
+    nothing for the padding."""
+    inp = f64(cfg)
+    T = cfg["seqlen"]
+    Tp = -(-T // cfg["chunk"]) * cfg["chunk"] + cfg["chunk"]  # a whole extra chunk of padding as well
+    pad = {}
+    for k, v in inp.items():
+        if v is None or k in ("A", "s0", "ds_final"):
+            pad[k] = v
+            continue
+        w = np.zeros((v.shape[0], Tp) + v.shape[2:])
+        w[:, :T] = v
+        if k == "dt_raw":  # dt' = softplus(-inf) = 0; MIMO's slot carries da itself, which pads as 0
+            w[:, T:] = 0.0 if variant == "mimo" else -np.inf
+        pad[k] = w
+    f, fp = oracle.forward(variant, inp), oracle.forward(variant, pad)
+    b, bp = oracle.backward(variant, inp), oracle.backward(variant, pad)
+    assert np.array_equal(fp["s_final"], f["s_final"]) and np.array_equal(fp["y"][:, :T], f["y"])
+    assert not np.any(fp["y"][:, T:])
+    for k, v in b.items():
+        if v is None:
+            continue
+        if k in ("ds0", "dA"):
+            assert rel(bp[k], v) < 1e-13, k
+        else:
+            assert rel(bp[k][:, :T], v) < 1e-13, k
+            if not (variant == "mimo" and k == "ddt_raw"):  # MIMO's da gradient is e^da <dS, s>, nonzero
+                assert not np.any(bp[k][:, T:]), k
