@@ -95,6 +95,13 @@ def kernel_bytes(name, cfg):
     cbb = b * nc * G * L * L * 4                 # fp32 C B^T per (chunk, group)
     cpart = b * nc * G * L * N * 4               # fp32 dB (or dC) partial, one slot per chunk
     dvws = b * T * H * P * 4 if m2 else 0
+    # Mamba-1 backward: 128-thread blocks of 128 / w channels (w = threads per channel, 2 states each), a
+    # checkpoint every 8 steps
+    w = 1
+    while w < -(-N // 2):
+        w *= 2
+    m1_part = b * T * (-(-H // (128 // w))) * N * 4
+    m1_ck = b * (-(-T // 8)) * H * N * 4
     table = {
         "k_chunk_state": t["x"] + dtb + t["B"] + states + small,
         "k_state_pass": 2 * states + small + 2 * t["s0"],
@@ -117,12 +124,49 @@ def kernel_bytes(name, cfg):
                            + t["x"] + dtb + small + 2 * cpart),                              # dx, ddt_raw, dA, dB/dC parts
         "k_tc_bwd_sums": 2 * cpart + t["B"] + t["C"] + small + t["A"],
         "k_m1_forward": 2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 2 * t["s0"],
-        "k_m1_backward": 2 * t["x"] + 2 * dtb + t["A"] + t["B"] + t["C"] + 3 * t["s0"] + t["x"]
-                         + 2 * b * T * H * N * 4 + b * H * N * 4 + b * H * (-(-T // L)) * N * 4,
-        "k_m1_channel_sum": b * T * H * N * 4 + t["B"],
+        # x, dt, dy, B, C, A, s0, ds_final in; dx, ddt, ds0, dA part, the per-block dB / dC partials out; the
+        # chunk-entry checkpoints written and read back
+        "k_m1_backward": (2 * t["x"] + dtb + t["B"] + t["C"] + t["A"] + 2 * t["s0"] + t["x"] + dtb + t["s0"]
+                          + b * H * N * 4 + 2 * m1_part + 2 * m1_ck),
+        "k_m1_channel_sum": m1_part + t["B"],
         "k_m1_dA_sum": b * H * N * 4 + t["A"],
     }
     return table.get(name)
+
+
+# Exponentials: the Mamba-1 branch has one decay exp(dt' A[d, n]) per (step, channel, state), so its
+# forward and the backward's replay each need b*T*D*N of them; on this path the special-function units,
+# not HBM, set the bound.  16 exp2 results per clock per SM is the CUDA-core special-function rate of
+# compute capability 9.x / 10.x parts; the peak is that times the SM count and the maximum SM clock.
+MUFU_PER_CLK_PER_SM = 16
+
+
+def exp_count(cfg):
+    """Algorithmic exponentials per forward + backward pair (Mamba-1: the
+    forward's decays and the backward replay's; the other variants have one
+    per (step, head), negligible beside their bytes)."""
+    if cfg["variant"] != "mamba1":
+        return 0.0
+    return 2.0 * cfg["batch"] * cfg["seqlen"] * cfg["nheads"] * cfg["dstate"]
+
+
+def kernel_exps(name, cfg):
+    """Algorithmic exponentials of one launch of the Mamba-1 kernels."""
+    if cfg["variant"] != "mamba1" or name not in ("k_m1_forward", "k_m1_backward"):
+        return None
+    return exp_count(cfg) / 2
+
+
+def exp_peak(pk):
+    """exp results per second: SM count x 16 per clock x maximum SM clock."""
+    sms = 152
+    try:
+        import torch
+        if torch.cuda.is_available():
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return sms * MUFU_PER_CLK_PER_SM * pk["sm_max_mhz"] * 1e6
 
 
 def path_dtype(cfg):
@@ -140,8 +184,10 @@ def peaks():
         with open(p) as f:
             d = json.load(f)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "sm_max_mhz": d.get("sm_max_mhz", 2070.0),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
 
 
 def ncu_traffic(kernel, workload):
@@ -544,12 +590,25 @@ def main():
                 "traffic": ncu_traffic(dom, args.workload), "peak_source": pk["source"],
                 "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_avg_ms,
                 "share_of_step": dom_ms / tot_prof}
+    dom_exps = kernel_exps(dom, cfg) if dom else None
+    xpk = exp_peak(pk)
+    if dom_exps and dom_avg_ms > 0 and dom_exps / xpk > dom_bytes / (pk["hbm_gbs"] * 1e9):
+        # the dominant kernel's exponentials take longer at the special-function peak than its bytes at HBM's
+        ach = dom_exps / (dom_avg_ms / 1e3) / 1e9
+        roofline.update({"bound": "alu", "achieved": ach, "peak": xpk / 1e9, "unit": "Gexp/s", "frac": ach / (xpk / 1e9),
+                         "peak_source": f"{MUFU_PER_CLK_PER_SM} exp/clk/SM x SMs x {pk['sm_max_mhz']:.0f} MHz",
+                         "algorithmic_exps_per_launch": dom_exps,
+                         "hbm_achieved": achieved, "hbm_frac": (achieved / pk["hbm_gbs"]) if achieved else None})
     step_s = ms_per_step / 1e3
     t_hbm = (fb + bb) / (pk["hbm_gbs"] * 1e9)
     t_tc = flops / (pk["bf16_tflops"] * 1e12) if flops else 0.0
-    roof_step = {"bytes": fb + bb, "tensor_flops": flops, "t_hbm_us": 1e6 * t_hbm, "t_tensor_us": 1e6 * t_tc,
-                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "roofline_tokens_per_s": tok / max(t_hbm, t_tc),
-                 "frac": max(t_hbm, t_tc) / step_s}
+    nexp = exp_count(cfg)
+    t_alu = nexp / xpk
+    t_roof = max(t_hbm, t_tc, t_alu)
+    roof_step = {"bytes": fb + bb, "tensor_flops": flops, "exps": nexp, "t_hbm_us": 1e6 * t_hbm,
+                 "t_tensor_us": 1e6 * t_tc, "t_alu_us": 1e6 * t_alu,
+                 "bound": "hbm" if t_roof == t_hbm else ("tensor" if t_roof == t_tc else "alu"),
+                 "roofline_tokens_per_s": tok / t_roof, "frac": t_roof / step_s}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": path_dtype(cfg),

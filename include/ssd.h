@@ -88,8 +88,10 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  *              Mamba-1 (B, C are shared by all channels) and MIMO (B, C are
  *              per head).
  *   chunk      L, the chunk length of the chunkwise algorithm (Mamba-2,
- *              MIMO), 1 <= L <= 256; for Mamba-1 the replay segment of the
- *              backward.  T need not be a multiple of L: the sequence is cut
+ *              MIMO), 1 <= L <= 256.  Mamba-1 has no chunkwise form: its
+ *              kernels walk the sequence step by step (checkpointing the
+ *              state every 8 steps in the backward) and accept any
+ *              1 <= L <= 256 here.  T need not be a multiple of L: the sequence is cut
  *              into nc = ceil(T / L) chunks, and the last one holds the
  *              remaining T - (nc - 1) L steps (a tail chunk).  The kernels
  *              treat its missing steps as steps with dt' = 0 (da = 0) and
