@@ -84,13 +84,16 @@ def kernel_bytes(name, cfg):
     t = tensor_bytes(cfg)
     b, T, H, P, N = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate"))
     L = cfg["chunk"]
+    if tc_path(cfg) and cfg["variant"] == "mimo":
+        # the tensor-core kernels run MIMO as the fused sequence of T * R positions in chunks of 64
+        T, L = T * cfg["mimo_rank"], 64
     nc = -(-T // L)
     states = b * H * nc * P * N * 4
     small = b * H * nc * 4
     dtb = t["dt_raw"]
     m2 = cfg["variant"] == "mamba2"
     part = b * T * H * N * 4 if m2 else 0
-    G = cfg.get("ngroups", 1)
+    G = cfg.get("ngroups", 1) if m2 else H
     sbf = b * H * nc * P * N * 2                 # bf16 chunk states
     cbb = b * nc * G * L * L * 4                 # fp32 C B^T per (chunk, group)
     cpart = b * nc * G * L * N * 4               # fp32 dB (or dC) partial, one slot per chunk
@@ -120,9 +123,10 @@ def kernel_bytes(name, cfg):
                               + cbb),                                                        # x, dy, ..., ds0, CB
         "k_tc_dstates_cb": t["x"] + dtb + t["A"] + t["B"] + t["C"] + t["s0"] + sbf + t["s0"] + cbb,
         "k_tc_fwd_chunk": t["x"] + dtb + t["A"] + t["C"] + cbb + sbf + t["x"],
+        # (one head per group: the chunk kernel writes dB, dC itself instead of fp32 partials)
         "k_tc_bwd_chunk": (2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + cbb + 2 * sbf      # dy, x, ..., S_c, dS
-                           + t["x"] + dtb + small + 2 * cpart),                              # dx, ddt_raw, dA, dB/dC parts
-        "k_tc_bwd_sums": 2 * cpart + t["B"] + t["C"] + small + t["A"],
+                           + t["x"] + dtb + small + (t["B"] + t["C"] if G == H else 2 * cpart)),
+        "k_tc_bwd_sums": (0 if G == H else 2 * cpart + t["B"] + t["C"]) + small + t["A"],
         "k_m1_forward": 2 * t["x"] + dtb + t["A"] + t["B"] + t["C"] + 2 * t["s0"],
         # x, dt, dy, B, C, A, s0, ds_final in; dx, ddt, ds0, dA part, the per-block dB / dC partials out; the
         # chunk-entry checkpoints written and read back
@@ -169,13 +173,23 @@ def exp_peak(pk):
     return sms * MUFU_PER_CLK_PER_SM * pk["sm_max_mhz"] * 1e6
 
 
+def tc_path(cfg):
+    """Whether the library runs cfg on its tensor-core kernels: bf16 io, head
+    dim 64, state 128, and Mamba-2 with chunk 64 or MIMO with a power-of-two
+    rank up to 64."""
+    if cfg["dtype"] != "bf16" or cfg["headdim"] != 64 or cfg["dstate"] != 128:
+        return False
+    if cfg["variant"] == "mamba2":
+        return cfg["chunk"] == 64
+    R = cfg["mimo_rank"]
+    return cfg["variant"] == "mimo" and R <= 64 and R & (R - 1) == 0
+
+
 def path_dtype(cfg):
     """Arithmetic type of the timed path: bf16 tensor-core MMAs (fp32
-    accumulate) for the Mamba-2 bf16 shapes the tcgen05 kernels serve, fp32
-    CUDA-core arithmetic otherwise."""
-    tc = (cfg["variant"] == "mamba2" and cfg["dtype"] == "bf16" and cfg["chunk"] == 64 and cfg["headdim"] == 64
-          and cfg["dstate"] == 128)
-    return "bf16" if tc else "f32"
+    accumulate) for the shapes the tcgen05 kernels serve, fp32 CUDA-core
+    arithmetic otherwise."""
+    return "bf16" if tc_path(cfg) else "f32"
 
 
 def peaks():

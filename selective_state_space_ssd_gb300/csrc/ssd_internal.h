@@ -20,6 +20,7 @@ struct Dims {
   int nc;   // T / L
   int LR;   // fused chunk length L * R
   int hpg;  // heads per group (Mamba-2)
+  int rs = 0;  // tensor-core kernels on a MIMO problem: log2 R (their T is then the fused length T * R)
 };
 
 struct FwdArgs {
@@ -79,8 +80,14 @@ size_t simt_backward_ws(const Dims& d);
 cudaError_t simt_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
 
-// Tensor-core path (Mamba-2, bf16 io, L = 64, P = 64, N = 128).
+// Tensor-core path (bf16 io, P = 64, N = 128): Mamba-2 with chunk 64, and MIMO
+// with a power-of-two rank R <= 64 as a Mamba-2 scan over the fused sequence
+// t * R + r (see tc_dims).
 bool tc_forward_supported(const Dims& d);
+// The sizes the tensor-core kernels run: the problem itself for Mamba-2; for
+// MIMO the fused sequence of T * R positions in chunks of 64 (16 steps of R =
+// 4), one group per head, and rs = log2 R.
+Dims tc_dims(const Dims& d);
 // Chunk-parallel forward (ssd_tc_fwdc.cu): the state scan, then every (chunk, head) output at once.
 size_t tc_forward_ws(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);

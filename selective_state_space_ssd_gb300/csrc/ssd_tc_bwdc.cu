@@ -110,8 +110,13 @@ struct BwdcParams {
   float* dC_part;
   int* status;
   int T, H, G, hpg, nc;
-  int nseg;   // partial slots per chunk
-  int total;  // number of (chunk, group, head) items: b * nc * G * hpg (< 2^31)
+  int nseg;      // partial slots per chunk
+  int total;     // number of (chunk, group, head) items: b * nc * G * hpg (< 2^31)
+  int mimo, rs;  // MIMO: dt_raw holds da [b, T >> rs, H] (dt' = 1) and ddt_raw receives its gradient; A unused
+  // one head per group (hpg == 1): a chunk's accumulators are its final dB, dC, written as bf16 [b, T, G, N]
+  // straight from TMEM instead of through the fp32 partials
+  __nv_bfloat16* dB;
+  __nv_bfloat16* dC;
 };
 
 __device__ __forceinline__ void load_row8(const uint8_t* tile, int r, int j, float* out) {
@@ -317,16 +322,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k = q & 3;
       if (q >= 4 && !mbar_wait(&sm.sc_free[k], ((q >> 2) - 1) & 1, status, 105)) break;
       const int h = hr.h(geo);
-      const float A_h = prm.A[h];
+      const float A_h = prm.mimo ? 1.f : prm.A[h];
       const int tt = hr.c * kL + t0;
-      const size_t rr = (size_t)hr.b * T + tt;
       // streaming loads: these strided reads must not push CB (read by E) out of L1.  Steps past the end of
       // the sequence (a partial last chunk) take dt_raw = -inf: dt' = 0 and da = 0, so they hold the state
-      // and (with their zero-filled x, dy, B, C rows) add nothing to any gradient.
-      const float z0 = tt < T ? __ldcs(prm.dt_raw + rr * H + h) : -INFINITY;
-      const float z1 = tt + 1 < T ? __ldcs(prm.dt_raw + (rr + 1) * H + h) : -INFINITY;
-      const float d0 = softplus_fast(z0), d1 = softplus_fast(z1);
-      const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
+      // and (with their zero-filled x, dy, B, C rows) add nothing to any gradient.  MIMO reads da at the
+      // first rank of each step, 0 at the others and past the end, with dt' = 1.
+      float z0, z1;
+      if (prm.mimo) {
+        const int msk = (1 << prm.rs) - 1;
+        const size_t sr = (size_t)hr.b * (T >> prm.rs);
+        z0 = tt < T && (tt & msk) == 0 ? __ldcs(prm.dt_raw + (sr + (tt >> prm.rs)) * H + h) : 0.f;
+        z1 = tt + 1 < T && ((tt + 1) & msk) == 0 ? __ldcs(prm.dt_raw + (sr + ((tt + 1) >> prm.rs)) * H + h) : 0.f;
+      } else {
+        const size_t rr = (size_t)hr.b * T + tt;
+        z0 = tt < T ? __ldcs(prm.dt_raw + rr * H + h) : -INFINITY;
+        z1 = tt + 1 < T ? __ldcs(prm.dt_raw + (rr + 1) * H + h) : -INFINITY;
+      }
+      const float d0 = prm.mimo ? 1.f : softplus_fast(z0), d1 = prm.mimo ? 1.f : softplus_fast(z1);
+      const float a0 = prm.mimo ? z0 : d0 * A_h, a1 = a0 + (prm.mimo ? z1 : d1 * A_h);
       float inc = a1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -420,15 +434,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             named_bar(kBarPool, kPoolThreads);  // O / BK read their TMEM columns before these loads
             tc_fence_after();
-            const long long slot =
-                (long long)co.k * prm.nseg + ((long long)blockIdx.x - cta_of((long long)co.k * prm.hpg, total, gridDim.x));
-            float* dst = (gi < 2 ? prm.dB_part : prm.dC_part) + (size_t)slot * kL * kN;
             const int n = 32 * qd + lane, col0 = 32 * (gi & 1);
             uint32_t v[32];
             tmem_ld32_nowait(taddr(gi < 2 ? ACC_B : ACC_C, 32 * qd, col0), v);
             tmem_wait_ld();
+            if (prm.dB) {
+              __nv_bfloat16* out = gi < 2 ? prm.dB : prm.dC;
+              const int tb = co.c * kL + col0;
 #pragma unroll
-            for (int e2 = 0; e2 < 32; ++e2) __stcs(dst + (size_t)(col0 + e2) * kN + n, __uint_as_float(v[e2]));
+              for (int e2 = 0; e2 < 32; ++e2)
+                if (tb + e2 < T)
+                  out[(((size_t)co.b * T + tb + e2) * prm.G + co.g) * kN + n] = __float2bfloat16_rn(__uint_as_float(v[e2]));
+            } else {
+              const long long slot = (long long)co.k * prm.nseg +
+                                     ((long long)blockIdx.x - cta_of((long long)co.k * prm.hpg, total, gridDim.x));
+              float* dst = (gi < 2 ? prm.dB_part : prm.dC_part) + (size_t)slot * kL * kN;
+#pragma unroll
+              for (int e2 = 0; e2 < 32; ++e2) __stcs(dst + (size_t)(col0 + e2) * kN + n, __uint_as_float(v[e2]));
+            }
           }
         }
       }
@@ -510,7 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 8; ++e) {
             const int s = s0 + e;
             // exp(cum_t - cum_s), masked before the exponential (cum_t - cum_s <= 0 for s <= t)
-            const float ex = (s <= t) ? __expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
+            // (MIMO: the ranks of one step see each other, cum being flat across them)
+            const float ex = ((s >> prm.rs) <= (t >> prm.rs)) ? __expf(fminf(ct - sm.cum[k][s], 0.f)) : 0.f;
             w[e] = cbv[e] * ex;
             const float dg = __uint_as_float(r8[e]) * sm.dtp[k][s];
             const float dcb = dg * ex;
@@ -578,9 +602,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float dda0 = suf, dda1 = suf - dc0;
           const int h = co.h(geo);
           const int tt = co.c * kL + t0;
-          const size_t rr = (size_t)co.b * T + tt;
-          if (tt < T) __stcs(prm.ddt_raw + rr * H + h, (vx0 + A_h * dda0) * sigmoid_fast(sm.z[kp][t0]));
-          if (tt + 1 < T) __stcs(prm.ddt_raw + (rr + 1) * H + h, (vx1 + A_h * dda1) * sigmoid_fast(sm.z[kp][t1]));
+          if (prm.mimo) {  // d da of a step: the suffix sum from its first rank
+            const int msk = (1 << prm.rs) - 1;
+            const size_t sr = (size_t)co.b * (T >> prm.rs);
+            if (tt < T && (tt & msk) == 0) __stcs(prm.ddt_raw + (sr + (tt >> prm.rs)) * H + h, dda0);
+            if (tt + 1 < T && ((tt + 1) & msk) == 0) __stcs(prm.ddt_raw + (sr + ((tt + 1) >> prm.rs)) * H + h, dda1);
+          } else {
+            const size_t rr = (size_t)co.b * T + tt;
+            if (tt < T) __stcs(prm.ddt_raw + rr * H + h, (vx0 + A_h * dda0) * sigmoid_fast(sm.z[kp][t0]));
+            if (tt + 1 < T) __stcs(prm.ddt_raw + (rr + 1) * H + h, (vx1 + A_h * dda1) * sigmoid_fast(sm.z[kp][t1]));
+          }
           float dAp = dda0 * sm.dtp[kp][t0] + dda1 * sm.dtp[kp][t1];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
@@ -703,13 +734,15 @@ constexpr int kMaxGrid = 1024;
 
 }  // namespace
 
-size_t tc_backward_ws(const Dims& d) {
+size_t tc_backward_ws(const Dims& problem) {
+  const Dims d = tc_dims(problem);
   Carver cv(nullptr);
   carve(d, layout(d, kMaxGrid), cv);
   return cv.off;
 }
 
-cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st) {
+cudaError_t tc_backward(const Dims& problem, const BwdArgs& a, void* ws, cudaStream_t st) {
+  const Dims d = tc_dims(problem);
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const BwdcLayout l = layout(d, sms < kMaxGrid ? sms : kMaxGrid);
@@ -736,18 +769,24 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t 
   if (e == cudaSuccess) e = make_tmap_2d_bf16(&tds, w.dstates, kP, srows, 64, kN);
   if (e != cudaSuccess) return e;
   // partial slots use the layout of the launched grid (nseg of the largest grid bounds it)
+  const bool direct = d.hpg == 1;
   BwdcParams prm{a.dt_raw, a.A,   w.CB, a.ddt_raw, w.dA_part, w.dB_part, w.dC_part, status,
-                 d.T,      d.H,   d.G,  d.hpg,     d.nc,      lmax.nseg, (int)l.total};
+                 d.T,      d.H,   d.G,  d.hpg,     d.nc,      lmax.nseg, (int)l.total, d.variant == kMimo, d.rs,
+                 direct ? static_cast<__nv_bfloat16*>(a.dB) : nullptr,
+                 direct ? static_cast<__nv_bfloat16*>(a.dC) : nullptr};
   const int smem = (int)sizeof(BwdcSmem) + 1024;
   e = cudaFuncSetAttribute(k_tc_bwdc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   SSD_LAUNCH("k_tc_bwd_chunk", st, k_tc_bwdc<<<l.grid, kThreads, smem, st>>>(tx, tdy, tdx, tb, tcm, ts, tds, prm));
-  const long long sum_blocks = 4 * l.nchunks + (d.H + 7) / 8;
+  // dB, dC blocks unless the chunk kernel wrote them; dA blocks unless there is no A (MIMO)
+  const long long nchunks_sum = direct ? 0 : l.nchunks;
+  const long long sum_blocks = 4 * nchunks_sum + (a.dA ? (d.H + 7) / 8 : 0);
   if (sum_blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-  SSD_LAUNCH("k_tc_bwd_sums", st,
-             k_bwdc_sums<<<(unsigned)sum_blocks, 256, 0, st>>>(
-                 w.dB_part, w.dC_part, static_cast<__nv_bfloat16*>(a.dB), static_cast<__nv_bfloat16*>(a.dC), w.dA_part,
-                 a.dA, l.nchunks, lmax.nseg, l.total, l.grid, d.hpg, d.T, d.G, d.nc, d.b, d.H));
+  if (sum_blocks > 0)
+    SSD_LAUNCH("k_tc_bwd_sums", st,
+               k_bwdc_sums<<<(unsigned)sum_blocks, 256, 0, st>>>(
+                   w.dB_part, w.dC_part, static_cast<__nv_bfloat16*>(a.dB), static_cast<__nv_bfloat16*>(a.dC),
+                   w.dA_part, a.dA, nchunks_sum, lmax.nseg, l.total, l.grid, d.hpg, d.T, d.G, d.nc, d.b, d.H));
   return cudaGetLastError();
 }
 

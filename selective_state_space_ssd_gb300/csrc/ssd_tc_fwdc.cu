@@ -83,7 +83,8 @@ struct FwdcParams {
   const float* CB;  // [b, nc, G, L, L] fp32
   int* status;
   int T, H, G, hpg, nc;
-  int total;  // items b * nc * G * hpg (< 2^31)
+  int total;     // items b * nc * G * hpg (< 2^31)
+  int mimo, rs;  // MIMO: dt_raw holds da [b, T >> rs, H] (dt' = 1), A is unused, ranks of a step see each other
 };
 
 // 16 or 32 TMEM columns of this warp's lanes, without the wait.
@@ -214,19 +215,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   formed: global-memory latency under the kernel's own HBM load (~2 us) would otherwise set the pace
     //   of the whole CTA.  Steps past the end of the sequence (a partial last chunk) get dt_raw = -inf,
     //   i.e. dt' = 0: their W' columns vanish, and their y rows are not stored.
+    //   MIMO reads da at the first rank of each step and 0 at the others.
     const int t0 = 2 * lane, t1 = t0 + 1;
+    const int msk = (1 << prm.rs) - 1;
     auto fetch = [&](const PairCursor& c, int slot) {
       if (c.a.f < q1) {
         const int h0 = c.a.h(geo);
         const int tt = c.a.c * kL + t0;
-        const size_t rr = (size_t)c.a.b * T + tt;
-        for (int i = 0; i < c.n; ++i) {
-          if (tt < T) cp_async4(&sm.dtraw[slot][i][t0], prm.dt_raw + rr * H + h0 + i);
-          else sm.dtraw[slot][i][t0] = -INFINITY;
-          if (tt + 1 < T) cp_async4(&sm.dtraw[slot][i][t1], prm.dt_raw + (rr + 1) * H + h0 + i);
-          else sm.dtraw[slot][i][t1] = -INFINITY;
+        if (prm.mimo) {
+          const size_t sr = (size_t)c.a.b * (T >> prm.rs);
+          for (int i = 0; i < c.n; ++i) {
+            if (tt < T && (tt & msk) == 0) cp_async4(&sm.dtraw[slot][i][t0], prm.dt_raw + (sr + (tt >> prm.rs)) * H + h0 + i);
+            else sm.dtraw[slot][i][t0] = 0.f;
+            if (tt + 1 < T && ((tt + 1) & msk) == 0)
+              cp_async4(&sm.dtraw[slot][i][t1], prm.dt_raw + (sr + ((tt + 1) >> prm.rs)) * H + h0 + i);
+            else sm.dtraw[slot][i][t1] = 0.f;
+          }
+          if (lane < c.n) sm.araw[slot][lane] = 1.f;
+        } else {
+          const size_t rr = (size_t)c.a.b * T + tt;
+          for (int i = 0; i < c.n; ++i) {
+            if (tt < T) cp_async4(&sm.dtraw[slot][i][t0], prm.dt_raw + rr * H + h0 + i);
+            else sm.dtraw[slot][i][t0] = -INFINITY;
+            if (tt + 1 < T) cp_async4(&sm.dtraw[slot][i][t1], prm.dt_raw + (rr + 1) * H + h0 + i);
+            else sm.dtraw[slot][i][t1] = -INFINITY;
+          }
+          if (lane < c.n) cp_async4(&sm.araw[slot][lane], prm.A + h0 + lane);
         }
-        if (lane < c.n) cp_async4(&sm.araw[slot][lane], prm.A + h0 + lane);
       }
       cp_async_commit();  // one group per pair, empty past the last, so that the count stays uniform
     };
@@ -247,8 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int i = 0; i < u.n; ++i) {
         const float A_h = sm.araw[sl][i];
-        const float d0 = softplus_fast(sm.dtraw[sl][i][t0]), d1 = softplus_fast(sm.dtraw[sl][i][t1]);
-        const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
+        const float z0 = sm.dtraw[sl][i][t0], z1 = sm.dtraw[sl][i][t1];
+        const float d0 = prm.mimo ? 1.f : softplus_fast(z0), d1 = prm.mimo ? 1.f : softplus_fast(z1);
+        const float a0 = prm.mimo ? z0 : d0 * A_h, a1 = a0 + (prm.mimo ? z1 : d1 * A_h);
         float inc = a1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -357,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int s2 = s0 + e;
-            w[e] = (s2 <= t) ? cbv[e] * __expf(fminf(ct - sm.cum[sc][i][s2], 0.f)) * sm.dtp[sc][i][s2] : 0.f;
+            // (MIMO: the ranks of one step see each other, cum being flat across them)
+            w[e] = ((s2 >> prm.rs) <= (t >> prm.rs)) ? cbv[e] * __expf(fminf(ct - sm.cum[sc][i][s2], 0.f)) * sm.dtp[sc][i][s2]
+                                                     : 0.f;
           }
           store_row_bf16(sm.W[r][i], t, hl + 2 * tj[0], w, 1);
         } else {  // two blocks left of the diagonal: exp(cum_t - cum_s) dt'_s = E_t[jj] Gd_s
@@ -433,13 +451,14 @@ FwdcWs carve(const Dims& d, Carver& cv) {
 
 }  // namespace
 
-size_t tc_forward_ws(const Dims& d) {
+size_t tc_forward_ws(const Dims& problem) {
   Carver cv(nullptr);
-  carve(d, cv);
+  carve(tc_dims(problem), cv);
   return cv.off;
 }
 
-cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st) {
+cudaError_t tc_forward(const Dims& problem, const FwdArgs& a, void* ws, cudaStream_t st) {
+  const Dims d = tc_dims(problem);
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   Carver cv(ws);
@@ -457,7 +476,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t s
   if (e != cudaSuccess) return e;
   const long long total = (long long)d.b * d.nc * d.H;
   const int grid = (int)(total < sms ? total : sms);
-  FwdcParams prm{a.dt_raw, a.A, w.CB, status, d.T, d.H, d.G, d.hpg, d.nc, (int)total};
+  FwdcParams prm{a.dt_raw, a.A, w.CB, status, d.T, d.H, d.G, d.hpg, d.nc, (int)total, d.variant == kMimo, d.rs};
   const int smem = (int)sizeof(FwdcSmem) + 1024;
   e = cudaFuncSetAttribute(k_tc_fwdc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -78,6 +78,7 @@ struct ScanParams {
   float* fin;         // s_final or ds0 [b,H,P,N]; null: not written
   int* status;
   int T, H, hpg, nc;
+  int mimo, rs;  // MIMO: dt_raw holds da [b, T >> rs, H] (the fused positions' dt' is 1), A is unused
 };
 
 // One direction's chains: the tensor maps of U (x or dy), K (B or C) and the state tiles out, and the scalars.
@@ -176,21 +177,29 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
     //   strided floats per chunk) are issued two chunks ahead of their use.  Steps past the end of the
     //   sequence (the tail of a partial last chunk) read dt_raw = -inf: dt' = 0 and da = 0 there, so they
     //   leave the state as it is, and their U rows are zeros (TMA fill) as well.
-    const float A_h = prm.A[h];
+    //   MIMO reads da at the first rank of each step and 0 at the others (dt' = 1 everywhere).
+    const float A_h = prm.mimo ? 1.f : prm.A[h];
     const int t0 = 2 * lane, t1 = t0 + 1;
+    const int msk = (1 << prm.rs) - 1;
+    const size_t srow0 = (size_t)b * (T >> prm.rs);
     auto fetch = [&](int r, float& z0, float& z1) {
       if (r < nc) {
         const int tt = chunk_of(r) * kL + t0;
-        const size_t rr = (size_t)row0 + tt;
-        z0 = tt < T ? prm.dt_raw[rr * H + h] : -INFINITY;
-        z1 = tt + 1 < T ? prm.dt_raw[(rr + 1) * H + h] : -INFINITY;
+        if (prm.mimo) {
+          z0 = tt < T && (tt & msk) == 0 ? prm.dt_raw[(srow0 + (tt >> prm.rs)) * H + h] : 0.f;
+          z1 = tt + 1 < T && ((tt + 1) & msk) == 0 ? prm.dt_raw[(srow0 + ((tt + 1) >> prm.rs)) * H + h] : 0.f;
+        } else {
+          const size_t rr = (size_t)row0 + tt;
+          z0 = tt < T ? prm.dt_raw[rr * H + h] : -INFINITY;
+          z1 = tt + 1 < T ? prm.dt_raw[(rr + 1) * H + h] : -INFINITY;
+        }
       }
     };
     auto step = [&](int r, float z0, float z1) -> bool {
       const int s = r % kScal;
       if (r >= kScal && !mbar_wait(&sm.sc_free[s], (r / kScal - 1) & 1, status, 85)) return false;
-      const float d0 = softplus_fast(z0), d1 = softplus_fast(z1);
-      const float a0 = d0 * A_h, a1 = a0 + d1 * A_h;
+      const float d0 = prm.mimo ? 1.f : softplus_fast(z0), d1 = prm.mimo ? 1.f : softplus_fast(z1);
+      const float a0 = prm.mimo ? z0 : d0 * A_h, a1 = a0 + (prm.mimo ? z1 : d1 * A_h);
       float inc = a1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -468,7 +477,7 @@ cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, co
     e = make_tmap_seq_bf16(&j.u, s->u, d, (uint64_t)d.H * kP);
     if (e == cudaSuccess) e = make_tmap_bc_bf16(&j.k, r == 0 ? B : C, d);
     if (e == cudaSuccess) e = make_tmap_2d_bf16(&j.out, s->states, kP, srows, 64, 32);
-    j.prm = ScanParams{dt_raw, A, s->init, s->fin, status, d.T, d.H, d.hpg, d.nc};
+    j.prm = ScanParams{dt_raw, A, s->init, s->fin, status, d.T, d.H, d.hpg, d.nc, d.variant == kMimo, d.rs};
   }
   if (e == cudaSuccess) e = make_tmap_bc_bf16(&job.cb.c, C, d);
   if (e == cudaSuccess) e = make_tmap_bc_bf16(&job.cb.b, B, d);

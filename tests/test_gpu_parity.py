@@ -49,6 +49,11 @@ SMALL = {
     "m1_tail": scaled(M1, batch=2, seqlen=100, nheads=40, chunk=32),
     "mimo_tail": scaled(MIMO, batch=2, seqlen=50, nheads=2, ngroups=2, headdim=20, dstate=24, chunk=16,
                         mimo_rank=3),
+    # MIMO on the tensor-core kernels (the fused sequence of T * R positions in chunks of 64): rank 4 with a
+    # tail (200 = 3 * 64 + 8 positions), ranks 2 and 1
+    "mimo_tc_tail": scaled(MIMO, batch=2, seqlen=50, nheads=3, ngroups=3),
+    "mimo_tc_r2": scaled(MIMO, batch=1, seqlen=96, nheads=2, ngroups=2, mimo_rank=2),
+    "mimo_tc_r1": scaled(MIMO, batch=2, seqlen=80, nheads=2, ngroups=2, mimo_rank=1),
 }
 
 
@@ -79,7 +84,8 @@ def test_null_s0_equals_zero_state(name):
     compare(cfg, a, run_oracle(cfg, cpu))
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "m2_bf16_tiles", "m1_small", "mimo_bf16_tiles", "m2_bf16_tail"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "m2_bf16_tiles", "m1_small", "mimo_bf16_tiles", "m2_bf16_tail",
+                                  "mimo_tc_tail"])
 def test_backward_is_bitwise_deterministic(name):
     cfg = SMALL[name]
     dev = to_device(synth.make_inputs(cfg, seed=3))
