@@ -27,7 +27,7 @@ CASES = {
     "mamba2_tiny_fp32": CONFIGS["mamba2_tiny_fp32"],
     # tensor-core path: its scratch holds the bf16 chunk states and C B^T
     "mamba2_bf16_tc": scaled(CONFIGS["mamba2_130m_bf16"], batch=2, seqlen=256, nheads=4),
-    # MIMO on CUDA cores: chunk states of 3 heads in the scratch
+    # MIMO on the tensor-core kernels (the fused sequence): chunk states and C B^T of 3 heads in the scratch
     "mimo_bf16": scaled(CONFIGS["mimo_r4_bf16"], batch=1, seqlen=256, nheads=3, ngroups=3),
     "mamba1_fp32": scaled(CONFIGS["mamba1_fp32"], batch=2, seqlen=256, nheads=40),
 }
