@@ -183,13 +183,13 @@ ssd_status ssd_backward(const ssd_problem* prob, const void* dy, const float* ds
  * same inputs, so ssd_backward_stashed returns bit for bit what ssd_backward
  * returns for the same leaf inputs.  It saves the backward one pass of the
  * state scan (about an eighth of a forward + backward step at the Mamba-2
- * 2.7B layer shape) for b*H*(T/L)*N*P*2 bytes of device memory held from the
+ * 2.7B layer shape) for b*H*ceil(T/L)*N*P*2 bytes of device memory held from the
  * forward to the backward.
  *
  * Available where the tensor-core path runs: Mamba-2, bf16 io, chunk 64,
  * headdim 64, dstate 128 (other problems return SSD_ERR_SHAPE).
  *
- * ssd_states_size: bytes of the stash for `prob` (bf16 [b, H, T/L][N][P],
+ * ssd_states_size: bytes of the stash for `prob` (bf16 [b, H, ceil(T/L)][N][P],
  *   row-major; tile (b, h, c) is the state entering chunk c, S_0 = s0 rounded
  *   to bf16).  Host-only.
  * ssd_forward_stash: ssd_forward, plus the stash written to `states`
