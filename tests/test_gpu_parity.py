@@ -47,6 +47,10 @@ SMALL = {
     "m2_fp32_tail": dict(variant="mamba2", dtype="f32", batch=2, seqlen=100, nheads=6, headdim=5, dstate=7,
                          ngroups=3, chunk=32, mimo_rank=1),
     "m1_tail": scaled(M1, batch=2, seqlen=100, nheads=40, chunk=32),
+    # Mamba-1 lane layouts: 16 threads a channel (N = 32), 2 (N = 3) and 1 (N = 2)
+    "m1_n32": scaled(M1, batch=1, seqlen=72, nheads=13, dstate=32),
+    "m1_n3": scaled(M1, batch=2, seqlen=40, nheads=70, dstate=3),
+    "m1_n2": scaled(M1, batch=1, seqlen=33, nheads=150, dstate=2),
     "mimo_tail": scaled(MIMO, batch=2, seqlen=50, nheads=2, ngroups=2, headdim=20, dstate=24, chunk=16,
                         mimo_rank=3),
     # MIMO on the tensor-core kernels (the fused sequence of T * R positions in chunks of 64): rank 4 with a
