@@ -299,6 +299,25 @@ class ClockSampler:
                 "samples": len(busy)}
 
 
+# ------------------------------------------------------------- ranks
+def max_over_ranks(x, world, device):
+    """The largest x over the ranks of the process group (x itself when
+    running alone): a step's time is that of the slowest replica."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(cfg, world, steps, total_ms):
+    """Whole-job throughput of `world` replicas that each ran `steps` steps
+    of cfg's workload in `total_ms` (the slowest rank's time): weak scaling."""
+    return world * tokens(cfg) * steps / (total_ms / 1e3)
+
+
 # ------------------------------------------------------------- CPU oracle
 def _oracle_sample(cfg, frac_t=1.0, whole=False):
     """A bounded sample of the workload for the float64 oracle: one batch
@@ -411,11 +430,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     clocks = clk.summary()
 
     # per-kernel event timing over the same number of steps (separate pass)
@@ -462,11 +477,7 @@ def run_ours(args, cfg, rank, world, local_rank):
             e_ev[k].record(stream)
         barrier()
         stash_ms = sum(a.elapsed_time(b) for a, b in zip(s_ev, e_ev))
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([stash_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            stash_ms = float(tt.item())
+        stash_ms = max_over_ranks(stash_ms, world, dev)
         del states
         stash = {"total_ms": stash_ms, "states_bytes": nst}
 
@@ -520,11 +531,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     return {"total_ms": total_ms, "step_ms": step_ms, "clocks": clocks, "per_kernel": per,
             "launches_per_step": launches_per_step, "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "h2d": h2d, "d2h": d2h,
             "stash": stash}
@@ -589,7 +596,7 @@ def main():
     flops = tensor_flops(cfg)
     pk = peaks()
     tok = tokens(cfg)
-    value = world * tok * args.steps / (r["total_ms"] / 1e3)
+    value = job_tokens_per_s(cfg, world, args.steps, r["total_ms"])
     ms_per_step = r["total_ms"] / args.steps
     # dominant kernel: largest share of the profiled time
     per = r["per_kernel"]
