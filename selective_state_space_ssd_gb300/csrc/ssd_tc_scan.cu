@@ -1,13 +1,13 @@
 // The two sequential state scans of the Mamba-2 chunkwise algorithm on
 // tcgen05 tensor cores (bf16 io, chunk L = 64, head dim P = 64, state N = 128).
 //
-// Forward (the state passing of the "Mamba-2 part III" page, section "The
-// state passing step"; the K3 + K4 pair of the burn-mamba page
-// "combined_backward.rs"):
+// Forward (the K3 chunk state and K4 state passing of the burn-mamba page
+// "combined_backward.rs", section "RECOMPUTE FORWARD INTERMEDIATES"):
 //     S_0 = s0,   S_{c+1} = exp(cum_end) S_c + B_c^T dvd_c,
 //     dvd[s][p] = exp(cum_end - cum_s) dt'_s x[s][p];
 // it writes every chunk-input state S_c (bf16, [n][p] tiles) and S_nc = s_final.
-// Reverse (the same recurrence transposed, the K4 backward):
+// Reverse (the same recurrence transposed: the page's "K4 backward step", which
+// carries d_s_{i+1} back as decay_i d_s_{i+1} plus the BLUE term):
 //     dS_nc = ds_final,   dS_c = exp(cum_end) dS_{c+1} + C_c^T dch_c,
 //     dch[t][p] = exp(cum_t) dy[t][p];
 // it writes dS_{c+1} for every chunk c (bf16 tiles) and dS_0 = ds0.

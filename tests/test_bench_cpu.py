@@ -71,3 +71,33 @@ def test_tensor_core_path_choice():
     assert bench.tc_path(CONFIGS["mamba2_2p7b_bf16"]) and bench.tc_path(CONFIGS["mimo_r4_bf16"])
     assert not bench.tc_path(CONFIGS["mamba2_tiny_fp32"]) and not bench.tc_path(CONFIGS["mamba1_fp32"])
     assert bench.path_dtype(CONFIGS["mimo_r4_bf16"]) == "bf16"
+
+
+def test_roofline_takes_the_bytes_of_the_pass_the_kernel_runs_in():
+    cfg = CONFIGS["mamba2_2p7b_bf16"]
+    fb, bb = bench.algorithmic_bytes(cfg)
+    assert bench.kernel_direction_bytes("k_tc_fwd_chunk", cfg) == fb
+    assert bench.kernel_direction_bytes("k_tc_states_cb", cfg) == fb
+    assert bench.kernel_direction_bytes("k_tc_bwd_chunk", cfg) == bb
+    assert bench.kernel_direction_bytes("k_tc_scan_pair_cb", cfg) == bb
+    # the design bytes of the backward chunk kernel include the chunk states it reads: more than the pass's own
+    assert bench.kernel_bytes("k_tc_bwd_chunk", cfg) > bb
+
+
+def test_parity_errors_are_relative_to_the_reference_maximum():
+    import numpy as np
+    import torch
+    ref = {"y": np.array([1.0, -4.0, 2.0]), "dx": np.array([0.5, 0.25])}
+    gpu = {"y": torch.tensor([1.0, -4.0, 2.2]), "dx": torch.tensor([0.5, 0.25]), "dB": torch.zeros(1)}
+    errs = bench.parity_errors(gpu, ref)
+    assert set(errs) == {"y", "dx"}
+    assert abs(errs["y"] - 0.2 / 4.0) < 1e-6 and errs["dx"] == 0.0
+
+
+def test_mimo_executed_flops_count_the_fused_sequence():
+    cfg = CONFIGS["mimo_r4_bf16"]
+    # the tensor-core kernels run chunks of 64 fused positions instead of the pages' L * R = 256: the L x L terms
+    # shrink by R, the L x N terms stay
+    assert bench.tensor_flops(cfg, executed=True) < bench.tensor_flops(cfg)
+    m2 = CONFIGS["mamba2_2p7b_bf16"]
+    assert bench.tensor_flops(m2, executed=True) == bench.tensor_flops(m2)
