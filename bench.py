@@ -574,6 +574,30 @@ def run_ours(args, cfg, rank, world, local_rank):
             "h2d": h2d, "d2h": d2h, "stash": stash, "outputs": outputs, "inputs_cpu": cpu}
 
 
+def run_once(args):
+    """One forward + backward of the (possibly resized) workload on seeded inputs, then exit 0: the command the
+    ncu captures profile, so that each kernel of the step launches exactly once."""
+    import torch
+    from selective_state_space_ssd_gb300 import binding
+    from selective_state_space_ssd_gb300 import inputs as synth
+
+    cfg = CONFIGS[args.workload]
+    if args.batch is not None:
+        cfg = scaled(cfg, batch=args.batch)
+    if args.seqlen is not None:
+        cfg = scaled(cfg, seqlen=args.seqlen)
+    binding.load()
+    dev = torch.device("cuda", 0)
+    t = {k: (None if v is None else v.to(dev)) for k, v in synth.make_inputs(cfg, seed=0).items()}
+    y, sf = binding.forward(cfg, t["x"], t["dt_raw"], t["A"], t["B"], t["C"], t["s0"])
+    grads = binding.backward(cfg, t["dy"], t["ds_final"], t["x"], t["dt_raw"], t["A"], t["B"], t["C"], t["s0"])
+    torch.cuda.synchronize()
+    print(json.dumps({"once": args.workload, "batch": cfg["batch"], "seqlen": cfg["seqlen"],
+                      "y_finite": bool(torch.isfinite(y.float()).all()),
+                      "dx_finite": bool(torch.isfinite(grads["dx"].float()).all())}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -586,7 +610,12 @@ def main():
                     help="override the workload's batch (small cases for ncu captures; not a bench line)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override the workload's T (not a multiple of the chunk: a tail chunk); not the headline")
+    ap.add_argument("--once", action="store_true",
+                    help="run one forward + backward pass of the workload untimed and exit (for profiler captures: "
+                         "exactly one launch of each kernel of the step, no warm-up, no bench line)")
     args = ap.parse_args()
+    if args.once:
+        return run_once(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = CONFIGS[args.workload]

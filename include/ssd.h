@@ -63,7 +63,7 @@ typedef enum {
   SSD_ERR_ALIGNMENT = 4,   /* a pointer is not 16-byte aligned */
   SSD_ERR_WORKSPACE = 5,   /* ws_bytes smaller than ssd_workspace_size() */
   SSD_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
-  SSD_ERR_TIMEOUT = 7,     /* reserved: a bounded device-side wait gave up */
+  SSD_ERR_TIMEOUT = 7,     /* the device status word is nonzero: a bounded device-side wait gave up */
   SSD_ERR_INTERNAL = 8,    /* a device-side consistency check failed */
   SSD_ERR_TOO_LARGE = 9    /* ssd_forward_static: the problem needs more scratch than its fixed array */
 } ssd_status;
@@ -230,16 +230,59 @@ ssd_status ssd_backward_stashed(const ssd_problem* prob, const void* dy, const f
  * 32 MiB is rejected with SSD_ERR_TOO_LARGE before anything runs.  The call
  * allocates nothing (no cudaMalloc, no allocating library routine).
  *
- * The first call on each device looks up that device's address of the array
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array, which keeps the
- * last call's contents (the status word in its first 4 bytes is reset by
- * every call): calls that may overlap on the GPU, on any streams, race on it
- * and must be serialized by the caller.
+ * Start-up: the array belongs to this library's device module, which the
+ * CUDA runtime loads on a device the first time the library needs it there
+ * (lazy loading, the default).  Loading reserves the 32 MiB, so a caller that
+ * forbids device allocation after start-up calls
+ * ssd_forward_static_status(NULL, stream) once per device at start-up, with
+ * that device current and before any stream capture: it loads the module and
+ * looks up the array's address and does nothing else.  Later calls allocate
+ * nothing.
+ *
+ * All calls share the one array, which keeps the last call's contents (its
+ * first 4 bytes are the device status word, reset to 0 by every call):
+ * calls that may overlap on the GPU, on any streams, race on it and must be
+ * serialized by the caller.
+ *
+ * ssd_forward_static_status(code, stream): with code == NULL, the start-up
+ * step above only.  Otherwise it also copies the status word into *code (a
+ * caller-owned host int32) on `stream`, after the work already enqueued
+ * there, and waits for that stream.  Returns SSD_OK when the word is 0,
+ * SSD_ERR_TIMEOUT when a bounded wait of the last call gave up (its outputs
+ * are then invalid; *code holds the code), SSD_ERR_CUDA if a CUDA call fails.
  */
 ssd_status ssd_forward_static(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
                               const void* B, const void* C, const float* s0, void* y, float* s_final,
                               void* cuda_stream);
+ssd_status ssd_forward_static_status(int32_t* code, void* cuda_stream);
+
+/*
+ * The device status word of a workspace, and a test of the bounded waits.
+ *
+ * Every wait of a kernel of this library on one of its barriers is bounded
+ * (two seconds).  One that runs out writes a nonzero code into the status
+ * word (the first 4 bytes of the call's workspace), stops issuing work and
+ * returns; the host learns of it only from the word, since the call itself
+ * returned before the GPU ran it.  (The pages ask for none of this; it is the
+ * failure detection of this library.)
+ *
+ * ssd_read_status(ws, code, stream): copies the status word at the start of
+ * the device workspace `ws` into *code (host int32) on `stream`, after the
+ * work already enqueued there, and waits for that stream.  Returns SSD_OK for
+ * 0, SSD_ERR_TIMEOUT for a nonzero word, SSD_ERR_INVALID_ARG for NULL
+ * arguments, SSD_ERR_CUDA if a CUDA call fails.  Allocates nothing.
+ *
+ * ssd_wait_selftest(ws, limit_us, stream): resets the status word of `ws`
+ * (device, 16-byte aligned, at least 4 bytes) and launches one warp in which
+ * one thread waits on a barrier that nothing ever completes, with a limit of
+ * limit_us microseconds (1 .. 2 000 000) instead of two seconds.  The wait
+ * runs out, writes code 1 into the word and the kernel returns: a following
+ * ssd_read_status returns SSD_ERR_TIMEOUT with *code == 1, and the stream and
+ * context stay usable.  Returns SSD_ERR_INVALID_ARG for a NULL ws or a limit
+ * outside the range, SSD_ERR_ALIGNMENT, or SSD_ERR_CUDA if the launch fails.
+ */
+ssd_status ssd_read_status(const void* ws, int32_t* code, void* cuda_stream);
+ssd_status ssd_wait_selftest(void* ws, uint32_t limit_us, void* cuda_stream);
 
 /*
  * Per-launch timing, for diagnostics and roofline measurement.

@@ -42,7 +42,7 @@ class ssd_problem(ctypes.Structure):
 
 EXPORTS = ("ssd_workspace_size", "ssd_forward", "ssd_backward", "ssd_forward_static", "ssd_profile_start",
            "ssd_profile_stop", "ssd_status_string", "ssd_version", "ssd_states_size", "ssd_forward_stash",
-           "ssd_backward_stashed")
+           "ssd_backward_stashed", "ssd_forward_static_status", "ssd_read_status", "ssd_wait_selftest")
 
 
 class ssd_kernel_time(ctypes.Structure):
@@ -89,6 +89,12 @@ def load(path: str | None = None):
         lib.ssd_forward_stash.restype = i32
         lib.ssd_backward_stashed.argtypes = [ctypes.POINTER(ssd_problem)] + [vp] * 8 + [sz] + [vp] * 7 + [sz, vp]
         lib.ssd_backward_stashed.restype = i32
+        lib.ssd_forward_static_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+        lib.ssd_forward_static_status.restype = i32
+        lib.ssd_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+        lib.ssd_read_status.restype = i32
+        lib.ssd_wait_selftest.argtypes = [vp, ctypes.c_uint32, vp]
+        lib.ssd_wait_selftest.restype = i32
         _lib = lib
         return lib
 
@@ -139,6 +145,28 @@ def ssd_forward_static(prob, x, dt_raw, A, B, C, s0, y, s_final, stream=None) ->
                                    _ptr(y), _ptr(s_final), _stream(stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_forward_static")
+
+
+def ssd_forward_static_status(stream=None, read: bool = True) -> tuple:
+    """(status, code) of the fixed array's device status word, read after the work enqueued on `stream`;
+    with read=False only the start-up step (module load and address lookup) runs and code is None."""
+    if not read:
+        return load().ssd_forward_static_status(None, _stream(stream)), None
+    code = ctypes.c_int32(-1)
+    st = load().ssd_forward_static_status(ctypes.byref(code), _stream(stream))
+    return st, code.value
+
+
+def ssd_read_status(ws, stream=None) -> tuple:
+    """(status, code) of the device status word in the first 4 bytes of the workspace `ws`."""
+    code = ctypes.c_int32(-1)
+    st = load().ssd_read_status(_ptr(ws), ctypes.byref(code), _stream(stream))
+    return st, code.value
+
+
+def ssd_wait_selftest(ws, limit_us: int, stream=None) -> int:
+    """Launch the kernel whose bounded wait runs out after limit_us; returns the call's status."""
+    return load().ssd_wait_selftest(_ptr(ws), int(limit_us), _stream(stream))
 
 
 def ssd_backward(prob, dy, ds_final, x, dt_raw, A, B, C, s0, dx, ddt_raw, dA, dB, dC, ds0, ws, ws_bytes,

@@ -3,8 +3,6 @@
 // file-scope device array as its scratch.
 #include <stdint.h>
 
-#include <mutex>
-
 #include "../../include/ssd.h"
 #include "ssd_internal.h"
 
@@ -17,23 +15,16 @@ namespace {
 constexpr size_t kStaticScratchBytes = (size_t)32 << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// Device address of the array, looked up once per device.  In host code the
-// symbol g_static_scratch is only a host-side stand-in, so the address a
-// kernel may use must come from cudaGetSymbolAddress with that device current.
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void* g_static_ptr[kMaxDevices] = {};
-
+// Device address of the array on the current device.  In host code the symbol
+// g_static_scratch is only a host-side stand-in, so the address a kernel may
+// use comes from cudaGetSymbolAddress with that device current.  It is looked
+// up on every call (no cache that a device reset or a new context would leave
+// stale); once the module is loaded on the device the lookup allocates
+// nothing.
 ssd_status static_scratch_ptr(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return SSD_ERR_CUDA;
-    g_static_ptr[dev] = p;
-  }
-  *out = g_static_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return SSD_ERR_CUDA;
+  *out = p;
   return SSD_OK;
 }
 
@@ -55,6 +46,17 @@ ssd_status ssd_forward_static(const ssd_problem* prob, const void* x, const floa
   // The same validation, kernels and status-word reset as ssd_forward; only
   // the scratch differs.
   return ssd_forward(prob, x, dt_raw, A, B, C, s0, y, s_final, scratch, ssd::kStaticScratchBytes, cuda_stream);
+}
+
+ssd_status ssd_forward_static_status(int32_t* code, void* cuda_stream) {
+  void* scratch = nullptr;
+  ssd_status s = ssd::static_scratch_ptr(&scratch);
+  if (s != SSD_OK || !code) return s;
+  if (cudaMemcpyAsync(code, scratch, sizeof(int32_t), cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(cuda_stream)) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  return *code == 0 ? SSD_OK : SSD_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -92,15 +92,17 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait: gives up after two seconds of the global timer, records `code` in *status and returns
-// false.  The caller then skips its remaining work.  The waiting loop is one shared out-of-line copy
-// (kernels with many waits stay small in the instruction cache); a phase that has already completed costs
-// one inline probe.
-static __device__ __noinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t phase, int* status, int code) {
+// Bounded wait: gives up after `limit_ns` of the global timer (two seconds in every kernel of the scan),
+// records `code` in *status and returns false.  The caller then skips its remaining work.  The waiting loop
+// is one shared out-of-line copy (kernels with many waits stay small in the instruction cache); a phase that
+// has already completed costs one inline probe.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+static __device__ __noinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t phase, int* status, int code,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = global_ns();
   for (;;) {
     if (mbar_test_sleep(bar, phase, 1000000u)) return true;
-    if (global_ns() - t0 > 2000000000ull) break;
+    if (global_ns() - t0 > limit_ns) break;
   }
   if (status) atomicCAS(status, 0, code);
   return false;

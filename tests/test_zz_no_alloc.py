@@ -5,9 +5,12 @@ workspace and uses the library's fixed 32 MiB device array instead.
 
 Each case calls it through the C ABI twice in a row, on different inputs, and
 compares both results with ssd_forward (which uses a caller workspace) within
-the parity tolerance of the other GPU tests; a problem whose scratch exceeds
-the fixed array must be refused with SSD_ERR_TOO_LARGE before anything runs.
-This file is collected last on purpose.
+the parity tolerance of the other GPU tests.  After each call the array's
+device status word must read 0 (no bounded wait gave up).  The outputs are
+allocated before the calls, and the second call must leave both torch's
+allocated bytes and the device's free bytes unchanged.  A problem whose
+scratch exceeds the fixed array must be refused with SSD_ERR_TOO_LARGE before
+anything runs.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -33,22 +36,25 @@ CASES = {
 }
 
 
-def _static_forward(cfg, t):
-    y = torch.empty_like(t["x"])
-    sf = torch.empty_like(t["ds_final"])
-    binding.ssd_forward_static(binding.problem(cfg), t["x"], t["dt_raw"], t["A"], t["B"], t["C"], t["s0"], y, sf)
-    return y, sf
-
-
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_static_forward_matches_workspace_forward_twice(name, cuda_lib):
     cfg = CASES[name]
     tol = TOL[cfg["dtype"]]
-    for seed in (11, 12):  # two calls in a row, different inputs each time
+    prob = binding.problem(cfg)
+    assert binding.ssd_forward_static_status(read=False)[0] == 0  # the start-up step: module loaded
+    for call, seed in enumerate((11, 12)):  # two calls in a row, different inputs each time
         t = to_device(synth.make_inputs(cfg, seed=seed))
         y_ref, sf_ref = binding.forward(cfg, t["x"], t["dt_raw"], t["A"], t["B"], t["C"], t["s0"])
-        y, sf = _static_forward(cfg, t)
+        y = torch.empty_like(t["x"])
+        sf = torch.empty_like(t["ds_final"])
         torch.cuda.synchronize()
+        before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        binding.ssd_forward_static(prob, t["x"], t["dt_raw"], t["A"], t["B"], t["C"], t["s0"], y, sf)
+        torch.cuda.synchronize()
+        after = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        if call == 1:
+            assert after == before, f"the second call allocated device memory: {before} -> {after}"
+        assert binding.ssd_forward_static_status() == (0, 0)
         assert rel_err(y, y_ref.double().cpu().numpy()) <= tol
         assert rel_err(sf, sf_ref.double().cpu().numpy()) <= tol
 
