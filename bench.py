@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 
 from selective_state_space_ssd_gb300.configs import CONFIGS, HEADLINE, scaled, tokens  # noqa: E402
 
+CKPT_EVERY = 8  # chunks between the checkpoints of the checkpointed variant
 METRIC = "SSD scan fwd+bwd tokens/s on 1 GB300 and % of roofline (HBM vs tensor peak)"
 L2_BYTES = 129 * 2 ** 20
 
@@ -516,6 +517,39 @@ def run_ours(args, cfg, rank, world, local_rank):
         del states
         stash = {"median_ms": stash_ms, "states_bytes": nst}
 
+    # the checkpoint-every-K variant (fp32 checkpoints every 8 chunks; the backward replays the chunk states in
+    # independent 8-chunk segments from them instead of one scan over the sequence), timed the same way
+    ckpt = None
+    try:
+        nck = binding.ssd_checkpoints_size(prob, CKPT_EVERY)
+    except binding.SSDError:
+        nck = 0
+    if nck:
+        ckbuf = torch.empty(nck, dtype=torch.uint8, device=dev)
+
+        def step_ckpt(inp, out=out0):
+            binding.ssd_forward_checkpointed(prob, inp["x"], inp["dt_raw"], inp["A"], inp["B"], inp["C"], inp["s0"],
+                                             out["y"], out["s_final"], CKPT_EVERY, ckbuf, nck, wsf, nf, stream)
+            binding.ssd_backward_checkpointed(prob, inp["dy"], inp["ds_final"], inp["x"], inp["dt_raw"], inp["A"],
+                                              inp["B"], inp["C"], CKPT_EVERY, ckbuf, nck, out["dx"], out["ddt_raw"],
+                                              out["dA"], out["dB"], out["dC"], out["ds0"], wsb, nb, stream)
+
+        for _ in range(args.warmup):
+            step_ckpt(t)
+        barrier()
+        s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(aux_steps)]
+        e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(aux_steps)]
+        for k in range(aux_steps):
+            flush.zero_()
+            s_ev[k].record(stream)
+            step_ckpt(t)
+            e_ev[k].record(stream)
+        barrier()
+        ck_ms = statistics.median(a.elapsed_time(b) for a, b in zip(s_ev, e_ev))
+        ck_ms = max_over_ranks(ck_ms, world, dev)
+        del ckbuf
+        ckpt = {"median_ms": ck_ms, "checkpoint_bytes": nck, "every": CKPT_EVERY}
+
     # end to end through the public API with host buffers (pinned).  Every step copies its inputs in from
     # pinned host memory and all of its outputs back; the copies of neighbouring steps overlap the compute:
     # two device buffer sets, inputs of step k+1 going in and outputs of step k-1 coming out (on their own
@@ -571,7 +605,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     outputs = {k: (None if v is None else v.clone()) for k, v in out0.items()}
     return {"total_ms": total_ms, "median_ms": median_ms, "step_ms": step_ms, "clocks": clocks, "per_kernel": per,
             "launches_per_step": launches_per_step, "aux_steps": aux_steps, "e2e_ms": e2e_ms, "e2e_steps": e2e_steps,
-            "h2d": h2d, "d2h": d2h, "stash": stash, "outputs": outputs, "inputs_cpu": cpu}
+            "h2d": h2d, "d2h": d2h, "stash": stash, "ckpt": ckpt, "outputs": outputs, "inputs_cpu": cpu}
 
 
 def run_once(args):
@@ -719,6 +753,14 @@ def main():
             "e2e": {"value": world * tok * r["e2e_steps"] / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "overlap": "double-buffered: step k+1's inputs in and step k-1's outputs out during step k"}}
+    if r["ckpt"]:
+        line["checkpointed"] = {
+            "value": world * tok / (r["ckpt"]["median_ms"] / 1e3), "unit": "tokens/s",
+            "ms_per_step": r["ckpt"]["median_ms"], "every": r["ckpt"]["every"],
+            "checkpoint_bytes": r["ckpt"]["checkpoint_bytes"],
+            "what": "ssd_forward_checkpointed + ssd_backward_checkpointed: fp32 states every K chunks kept from the "
+                    "forward; the backward replays the chunk states from them in K-chunk segments (same bits); "
+                    "not the headline step, which recomputes from the leaf inputs"}
     if r["stash"]:
         line["stashed_states"] = {
             "value": world * tok / (r["stash"]["median_ms"] / 1e3), "unit": "tokens/s",

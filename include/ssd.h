@@ -212,6 +212,48 @@ ssd_status ssd_backward_stashed(const ssd_problem* prob, const void* dy, const f
                                 void* dB, void* dC, float* ds0, void* ws, size_t ws_bytes, void* cuda_stream);
 
 /*
+ * Checkpoint every K chunks: a forward that keeps the fp32 chain state at
+ * every K-th chunk boundary, and a backward that replays the chunk states from
+ * those checkpoints in independent segments of K chunks instead of one
+ * sequential scan over the whole sequence (the "Two things that are easy to
+ * get wrong" section, item 2, of the "S1-31: SSM_SCAN_BACK" page: checkpoints
+ * every K steps are the cheaper scheme, and must give the bits of storing every
+ * state).  The checkpoints are the exact fp32 states of the forward's scan, and
+ * each segment applies the same operations to them as the whole-sequence
+ * replay, so ssd_backward_checkpointed returns bit for bit what ssd_backward
+ * returns, for any K.  Memory held from the forward to the backward:
+ * b*H*ceil(nc/K)*P*N*4 bytes (nc = ceil(T/L); 84 MB at K = 8 for the Mamba-2
+ * 2.7B layer shape, against 336 MB for the stash of every state).
+ *
+ * Available where the tensor-core path runs: Mamba-2, bf16 io, chunk 64,
+ * headdim 64, dstate 128 (other problems return SSD_ERR_SHAPE).  every = K,
+ * 1 <= K <= 2^30 (SSD_ERR_INVALID_ARG otherwise); K >= nc keeps only s0.
+ *
+ * ssd_checkpoints_size: bytes of the checkpoints (fp32 [b, H, ceil(nc/K)][P][N],
+ *   row-major; entry (b, h, k) is the state entering chunk k*K, entry 0 = s0,
+ *   zeros for a NULL s0).  Host-only.
+ * ssd_forward_checkpointed: ssd_forward, plus the checkpoints written to
+ *   `ckpt` (caller-owned device buffer of at least ssd_checkpoints_size bytes,
+ *   16-byte aligned; a smaller ckpt_bytes returns SSD_ERR_WORKSPACE).  y and
+ *   s_final are bit for bit those of ssd_forward.  ws as for ssd_forward.
+ * ssd_backward_checkpointed: ssd_backward without s0, reading the checkpoints
+ *   written by ssd_forward_checkpointed with the same K for the same x,
+ *   dt_raw, A, B, s0 (the caller keeps the buffer unchanged in between; nothing
+ *   checks it).  ws as for ssd_backward.
+ * Errors and the device status word are those of ssd_forward / ssd_backward.
+ */
+ssd_status ssd_checkpoints_size(const ssd_problem* prob, int64_t every, size_t* bytes);
+ssd_status ssd_forward_checkpointed(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
+                                    const void* B, const void* C, const float* s0, void* y, float* s_final,
+                                    int64_t every, float* ckpt, size_t ckpt_bytes, void* ws, size_t ws_bytes,
+                                    void* cuda_stream);
+ssd_status ssd_backward_checkpointed(const ssd_problem* prob, const void* dy, const float* ds_final, const void* x,
+                                     const float* dt_raw, const float* A, const void* B, const void* C,
+                                     int64_t every, const float* ckpt, size_t ckpt_bytes, void* dx, float* ddt_raw,
+                                     float* dA, void* dB, void* dC, float* ds0, void* ws, size_t ws_bytes,
+                                     void* cuda_stream);
+
+/*
  * Forward scan without a caller workspace, for callers that cannot allocate
  * device memory.  (The pages describe no such call; it is an addition of this
  * library.)

@@ -42,7 +42,8 @@ class ssd_problem(ctypes.Structure):
 
 EXPORTS = ("ssd_workspace_size", "ssd_forward", "ssd_backward", "ssd_forward_static", "ssd_profile_start",
            "ssd_profile_stop", "ssd_status_string", "ssd_version", "ssd_states_size", "ssd_forward_stash",
-           "ssd_backward_stashed", "ssd_forward_static_status", "ssd_read_status", "ssd_wait_selftest")
+           "ssd_backward_stashed", "ssd_forward_static_status", "ssd_read_status", "ssd_wait_selftest",
+           "ssd_checkpoints_size", "ssd_forward_checkpointed", "ssd_backward_checkpointed")
 
 
 class ssd_kernel_time(ctypes.Structure):
@@ -95,6 +96,14 @@ def load(path: str | None = None):
         lib.ssd_read_status.restype = i32
         lib.ssd_wait_selftest.argtypes = [vp, ctypes.c_uint32, vp]
         lib.ssd_wait_selftest.restype = i32
+        i64 = ctypes.c_int64
+        lib.ssd_checkpoints_size.argtypes = [ctypes.POINTER(ssd_problem), i64, ctypes.POINTER(sz)]
+        lib.ssd_checkpoints_size.restype = i32
+        lib.ssd_forward_checkpointed.argtypes = [ctypes.POINTER(ssd_problem)] + [vp] * 8 + [i64, vp, sz, vp, sz, vp]
+        lib.ssd_forward_checkpointed.restype = i32
+        lib.ssd_backward_checkpointed.argtypes = ([ctypes.POINTER(ssd_problem)] + [vp] * 7 + [i64, vp, sz] + [vp] * 6 +
+                                                 [vp, sz, vp])
+        lib.ssd_backward_checkpointed.restype = i32
         _lib = lib
         return lib
 
@@ -195,6 +204,33 @@ def ssd_forward_stash(prob, x, dt_raw, A, B, C, s0, y, s_final, states, states_b
         raise SSDError(st, "ssd_forward_stash")
 
 
+def ssd_checkpoints_size(prob: ssd_problem, every: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().ssd_checkpoints_size(ctypes.byref(prob), int(every), ctypes.byref(out))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_checkpoints_size")
+    return out.value
+
+
+def ssd_forward_checkpointed(prob, x, dt_raw, A, B, C, s0, y, s_final, every, ckpt, ckpt_bytes, ws, ws_bytes,
+                             stream=None) -> None:
+    st = load().ssd_forward_checkpointed(ctypes.byref(prob), _ptr(x), _ptr(dt_raw), _ptr(A), _ptr(B), _ptr(C),
+                                         _ptr(s0), _ptr(y), _ptr(s_final), int(every), _ptr(ckpt), int(ckpt_bytes),
+                                         _ptr(ws), int(ws_bytes), _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_forward_checkpointed")
+
+
+def ssd_backward_checkpointed(prob, dy, ds_final, x, dt_raw, A, B, C, every, ckpt, ckpt_bytes, dx, ddt_raw, dA, dB,
+                              dC, ds0, ws, ws_bytes, stream=None) -> None:
+    st = load().ssd_backward_checkpointed(ctypes.byref(prob), _ptr(dy), _ptr(ds_final), _ptr(x), _ptr(dt_raw), _ptr(A),
+                                          _ptr(B), _ptr(C), int(every), _ptr(ckpt), int(ckpt_bytes), _ptr(dx),
+                                          _ptr(ddt_raw), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(ds0), _ptr(ws),
+                                          int(ws_bytes), _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_backward_checkpointed")
+
+
 def ssd_backward_stashed(prob, dy, ds_final, x, dt_raw, A, B, C, states, states_bytes, dx, ddt_raw, dA, dB, dC,
                          ds0, ws, ws_bytes, stream=None) -> None:
     st = load().ssd_backward_stashed(ctypes.byref(prob), _ptr(dy), _ptr(ds_final), _ptr(x), _ptr(dt_raw), _ptr(A),
@@ -279,4 +315,37 @@ def backward_stashed(cfg: dict, dy, ds_final, x, dt_raw, A, B, C, states, stream
     ws, n = workspace if workspace is not None else _workspace(prob, True, dev)
     ssd_backward_stashed(prob, dy, ds_final, x, dt_raw, A, B, C, states, states.numel(), out["dx"], out["ddt_raw"],
                          out["dA"], out["dB"], out["dC"], out["ds0"], ws, n, stream)
+    return out
+
+
+def forward_checkpointed(cfg: dict, x, dt_raw, A, B, C, s0=None, every: int = 8, stream=None, workspace=None):
+    """``forward`` that also keeps fp32 checkpoints every ``every`` chunks; returns (y, s_final, ckpt) with ckpt
+    a float32 device tensor [b, H, ceil(nc / every), P, N] for ``backward_checkpointed``."""
+    prob = problem(cfg)
+    dev = x.device
+    y = torch.empty_like(x)
+    s_final = torch.empty((cfg["batch"], cfg["nheads"], cfg["headdim"], cfg["dstate"]), dtype=torch.float32,
+                          device=dev)
+    nbytes = ssd_checkpoints_size(prob, every)
+    nc = -(-cfg["seqlen"] // cfg["chunk"])
+    nk = -(-nc // every)
+    ckpt = torch.empty((cfg["batch"], cfg["nheads"], nk, cfg["headdim"], cfg["dstate"]), dtype=torch.float32,
+                       device=dev)
+    assert ckpt.numel() * 4 == nbytes
+    ws, n = workspace if workspace is not None else _workspace(prob, False, dev)
+    ssd_forward_checkpointed(prob, x, dt_raw, A, B, C, s0, y, s_final, every, ckpt, nbytes, ws, n, stream)
+    return y, s_final, ckpt
+
+
+def backward_checkpointed(cfg: dict, dy, ds_final, x, dt_raw, A, B, C, ckpt, every: int = 8, stream=None,
+                          workspace=None):
+    """``backward`` that replays the chunk states from ``forward_checkpointed``'s checkpoints (no s0); returns the
+    same dict."""
+    prob = problem(cfg)
+    dev = x.device
+    out = {"dx": torch.empty_like(x), "ddt_raw": torch.empty_like(dt_raw), "dA": torch.empty_like(A),
+           "dB": torch.empty_like(B), "dC": torch.empty_like(C), "ds0": torch.empty_like(ds_final)}
+    ws, n = workspace if workspace is not None else _workspace(prob, True, dev)
+    ssd_backward_checkpointed(prob, dy, ds_final, x, dt_raw, A, B, C, every, ckpt, ckpt.numel() * 4, out["dx"],
+                              out["ddt_raw"], out["dA"], out["dB"], out["dC"], out["ds0"], ws, n, stream)
     return out

@@ -93,6 +93,16 @@ int g_prof_cap = 0;
 std::vector<ProfRec> g_prof;
 thread_local int t_prof_open = -1;  // record opened by this thread's last prof_begin
 
+// Validation shared by the checkpoint calls: the problem, then 1 <= every <= 2^30 (SSD_ERR_INVALID_ARG),
+// then the tensor-core Mamba-2 path (SSD_ERR_SHAPE otherwise).
+ssd_status checkpoint_dims(const ssd_problem* prob, int64_t every, Dims* d) {
+  ssd_status s = make_dims(prob, d);
+  if (s != SSD_OK) return s;
+  if (every < 1 || every > (int64_t)1 << 30) return SSD_ERR_INVALID_ARG;
+  if (d->variant != kMamba2 || !tc_forward_supported(*d)) return SSD_ERR_SHAPE;
+  return SSD_OK;
+}
+
 }  // namespace
 
 void prof_begin(const char* name, cudaStream_t st) {
@@ -274,6 +284,58 @@ ssd_status ssd_backward_stashed(const ssd_problem* prob, const void* dy, const f
   if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
   BwdArgs a{dy, ds_final, x, dt_raw, A, B, C, nullptr, dx, ddt_raw, dA, dB, dC, ds0,
             static_cast<const __nv_bfloat16*>(states)};
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  return tc_backward(d, a, ws, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_checkpoints_size(const ssd_problem* prob, int64_t every, size_t* bytes) {
+  if (!bytes) return SSD_ERR_INVALID_ARG;
+  Dims d;
+  ssd_status s = checkpoint_dims(prob, every, &d);
+  if (s != SSD_OK) return s;
+  *bytes = tc_checkpoints_bytes(d, (int)every);
+  return SSD_OK;
+}
+
+ssd_status ssd_forward_checkpointed(const ssd_problem* prob, const void* x, const float* dt_raw, const float* A,
+                                    const void* B, const void* C, const float* s0, void* y, float* s_final,
+                                    int64_t every, float* ckpt, size_t ckpt_bytes, void* ws, size_t ws_bytes_given,
+                                    void* cuda_stream) {
+  Dims d;
+  ssd_status s = checkpoint_dims(prob, every, &d);
+  if (s != SSD_OK) return s;
+  s = check_ptrs({x, dt_raw, A, B, C, y, s_final, ckpt}, {s0});
+  if (s != SSD_OK) return s;
+  if (ckpt_bytes < tc_checkpoints_bytes(d, (int)every) || ws_bytes_given < ws_bytes(d, false))
+    return SSD_ERR_WORKSPACE;
+  if (!ws) return SSD_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
+  FwdArgs a{x, dt_raw, A, B, C, s0, y, s_final};
+  a.ckpt_out = ckpt;
+  a.ckpt_every = (int)every;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  return tc_forward(d, a, ws, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_backward_checkpointed(const ssd_problem* prob, const void* dy, const float* ds_final, const void* x,
+                                     const float* dt_raw, const float* A, const void* B, const void* C,
+                                     int64_t every, const float* ckpt, size_t ckpt_bytes, void* dx, float* ddt_raw,
+                                     float* dA, void* dB, void* dC, float* ds0, void* ws, size_t ws_bytes_given,
+                                     void* cuda_stream) {
+  Dims d;
+  ssd_status s = checkpoint_dims(prob, every, &d);
+  if (s != SSD_OK) return s;
+  s = check_ptrs({dy, ds_final, x, dt_raw, A, B, C, ckpt, dx, ddt_raw, dA, dB, dC, ds0}, {});
+  if (s != SSD_OK) return s;
+  if (ckpt_bytes < tc_checkpoints_bytes(d, (int)every) || ws_bytes_given < ws_bytes(d, true))
+    return SSD_ERR_WORKSPACE;
+  if (!ws) return SSD_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return SSD_ERR_ALIGNMENT;
+  BwdArgs a{dy, ds_final, x, dt_raw, A, B, C, nullptr, dx, ddt_raw, dA, dB, dC, ds0};
+  a.ckpt_in = ckpt;
+  a.ckpt_every = (int)every;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
   return tc_backward(d, a, ws, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

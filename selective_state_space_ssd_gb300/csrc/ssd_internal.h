@@ -33,6 +33,8 @@ struct FwdArgs {
   void* y;
   float* s_final;
   __nv_bfloat16* states_out = nullptr;  // tensor-core path: chunk states to this caller buffer, not the workspace
+  float* ckpt_out = nullptr;            // tensor-core path: fp32 checkpoints every ckpt_every chunks
+  int ckpt_every = 0;
 };
 
 struct BwdArgs {
@@ -51,6 +53,8 @@ struct BwdArgs {
   void* dC;
   float* ds0;
   const __nv_bfloat16* states_in = nullptr;  // tensor-core path: stashed chunk states (no forward replay)
+  const float* ckpt_in = nullptr;            // tensor-core path: replay in segments from these checkpoints
+  int ckpt_every = 0;
 };
 
 // The first kStatusBytes of every workspace hold the device status word
@@ -97,13 +101,22 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t s
 // with C) writes dS_{c+1} for every chunk and dS_0 into fin.  init = s0 (may
 // be null) or ds_final.  Either side may be absent (null); CB[b, c, g] =
 // C B^T of every chunk and group (fp32) is always written.
+// Forward side only: ckpt_out (not null) receives the fp32 state entering
+// every `every`-th chunk, [b,H,nk][P][N] with nk = ceil(nc / every) (entry 0 =
+// s0); with ckpt_in (not null) the forward scan runs as b*H*nk independent
+// segments of `every` chunks, each started from its entry, and writes the same
+// S_c tiles as the whole-sequence scan (init and fin unused).
 struct ScanSide {
   const void* u;
   const float* init;
   float* fin;
   __nv_bfloat16* states;
+  float* ckpt_out = nullptr;
+  const float* ckpt_in = nullptr;
+  int every = 0;
 };
 size_t tc_scan_states_bytes(const Dims& d);
+size_t tc_checkpoints_bytes(const Dims& d, int every);
 cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, const void* B, const void* C,
                      const float* dt_raw, const float* A, float* CB, int* status, cudaStream_t st);
 // Chunk-parallel backward (ssd_tc_bwdc.cu): both scans, then every (chunk, head) at once.

@@ -753,8 +753,10 @@ cudaError_t tc_backward(const Dims& problem, const BwdArgs& a, void* ws, cudaStr
   // the chunk states: replayed from the leaf inputs, or the forward's stash (the same kernel on the same
   // inputs wrote it, so the two give the same bits)
   const __nv_bfloat16* states = a.states_in ? a.states_in : w.states;
-  // the replay (unless stashed) and the reverse scan are independent: one launch runs both, plus CB
-  const ScanSide fwd{a.x, a.s0, nullptr, w.states};
+  // the replay (unless stashed) and the reverse scan are independent: one launch runs both, plus CB; from
+  // checkpoints the replay runs as short independent segments, started from the checkpointed fp32 states
+  // (the whole-sequence replay computes the same states with the same operations, so the same bits)
+  const ScanSide fwd{a.x, a.s0, nullptr, w.states, nullptr, a.ckpt_in, a.ckpt_every};
   const ScanSide rev{a.dy, a.ds_final, a.ds0, w.dstates};
   cudaError_t e = tc_scans(d, a.states_in ? nullptr : &fwd, &rev, a.B, a.C, a.dt_raw, a.A, w.CB, status, st);
   if (e != cudaSuccess) return e;

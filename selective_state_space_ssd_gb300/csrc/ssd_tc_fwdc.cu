@@ -465,7 +465,7 @@ cudaError_t tc_forward(const Dims& problem, const FwdArgs& a, void* ws, cudaStre
   FwdcWs w = carve(d, cv);
   int* status = static_cast<int*>(ws);
   __nv_bfloat16* states = a.states_out ? a.states_out : w.states;  // a stash for the backward, or scratch
-  const ScanSide fwd{a.x, a.s0, a.s_final, states};
+  const ScanSide fwd{a.x, a.s0, a.s_final, states, a.ckpt_out, nullptr, a.ckpt_every};
   cudaError_t e = tc_scans(d, &fwd, nullptr, a.B, a.C, a.dt_raw, a.A, w.CB, status, st);
   if (e != cudaSuccess) return e;
   CUtensorMap tx, tcm, ts, ty;

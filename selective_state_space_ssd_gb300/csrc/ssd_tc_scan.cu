@@ -79,6 +79,10 @@ struct ScanParams {
   int* status;
   int T, H, hpg, nc;
   int mimo, rs;  // MIMO: dt_raw holds da [b, T >> rs, H] (the fused positions' dt' is 1), A is unused
+  // checkpoints (forward only), fp32 [b, H, nk][P][N], entry k = the state entering chunk k * every:
+  float* ckpt_out;       // written by the whole-sequence chains (entry 0 = s0), or null
+  const float* ckpt_in;  // not null: the chains are segments of `every` chunks, each started from its entry
+  int every, nk;
 };
 
 // One direction's chains: the tensor maps of U (x or dy), K (B or C) and the state tiles out, and the scalars.
@@ -87,9 +91,10 @@ struct ScanJob {
   ScanParams prm;
 };
 
-// One (batch, head) chain, run by the whole CTA.
+// One (batch, head) chain, run by the whole CTA: the whole sequence, or (forward, from checkpoints) the
+// segment `seg` of `every` chunks, which writes the input states of its chunks and nothing else.
 template <bool kRev, int kStU>
-__device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uint8_t* smem) {
+__device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, int seg, uint8_t* smem) {
   ScanSmem<kStU>& sm = *reinterpret_cast<ScanSmem<kStU>*>(smem);
   const CUtensorMap& tm_u = job.u;
   const CUtensorMap& tm_k = job.k;
@@ -101,7 +106,13 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
   const size_t row0 = (size_t)b * T;
   const size_t unit = (size_t)b * H + h;
   int* status = prm.status;
-  auto chunk_of = [&](int r) { return kRev ? nc - 1 - r : r; };
+  const bool segmented = !kRev && prm.ckpt_in;
+  const int cbeg = segmented ? seg * prm.every : 0;
+  const int clen = segmented ? min(prm.every, nc - cbeg) : nc;
+  // state updates: one per chunk of the whole sequence (the last gives fin), one per chunk but the last of a
+  // segment (its last chunk's input state is the last one it writes)
+  const int nsteps = segmented ? clen - 1 : nc;
+  auto chunk_of = [&](int r) { return kRev ? nc - 1 - r : cbeg + r; };
 
   if (tid == 0) {
     for (int s = 0; s < kStU; ++s) {
@@ -134,7 +145,7 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
       prefetch_tmap(&tm_u);
       prefetch_tmap(&tm_k);
       int su = 0, pu = 0;  // x / dy ring slot and its phase
-      for (int r = 0; r < nc; ++r) {
+      for (int r = 0; r < nsteps; ++r) {
         const int sk = r & 1, c = chunk_of(r);
         if (r >= kStU && !mbar_wait(&sm.empty_u[su], pu ^ 1, status, 81)) break;
         mbar_expect_tx(&sm.full_u[su], kTileLP);
@@ -152,7 +163,7 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
       const uint32_t tP = tmem + 64u;
       bool ok = true;
       int su = 0, pu = 0;
-      for (int r = 0; r < nc && ok; ++r) {
+      for (int r = 0; r < nsteps && ok; ++r) {
         const int sk = r & 1;
         ok = mbar_wait(&sm.pre_done[su], pu, status, 82);
         ok = ok && mbar_wait(&sm.full_k[sk], (r >> 1) & 1, status, 79);
@@ -183,7 +194,7 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
     const int msk = (1 << prm.rs) - 1;
     const size_t srow0 = (size_t)b * (T >> prm.rs);
     auto fetch = [&](int r, float& z0, float& z1) {
-      if (r < nc) {
+      if (r < nsteps) {
         const int tt = chunk_of(r) * kL + t0;
         if (prm.mimo) {
           z0 = tt < T && (tt & msk) == 0 ? prm.dt_raw[(srow0 + (tt >> prm.rs)) * H + h] : 0.f;
@@ -223,10 +234,10 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
     float za0 = 0.f, za1 = 0.f, zb0 = 0.f, zb1 = 0.f;
     fetch(0, za0, za1);
     fetch(1, zb0, zb1);
-    for (int r = 0; r < nc; r += 2) {
+    for (int r = 0; r < nsteps; r += 2) {
       if (!step(r, za0, za1)) break;
       fetch(r + 2, za0, za1);
-      if (r + 1 < nc) {
+      if (r + 1 < nsteps) {
         if (!step(r + 1, zb0, zb1)) break;
         fetch(r + 3, zb0, zb1);
       }
@@ -235,7 +246,7 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
     // ------------------------------------------------------------ scale warps: U *= scale (per row)
     const int pt = tid - 32 * kWarpScale0;  // 0..63
     int s = 0, ps = 0;  // x / dy ring slot and its phase
-    for (int r = 0; r < nc; ++r) {
+    for (int r = 0; r < nsteps; ++r) {
       const int k = r % kScal;
       bool ok = mbar_wait(&sm.sc_ready[k], (r / kScal) & 1, status, 86);
       ok = ok && mbar_wait(&sm.full_u[s], ps, status, 87);
@@ -263,6 +274,12 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
     const int n = tid;
     const uint32_t srow = taddr(tmem, 32 * warp, 0), prow = taddr(tmem, 32 * warp, 64);
     const size_t fbase = unit * kP * kN;
+    const float* init = segmented ? prm.ckpt_in + ((size_t)unit * prm.nk + seg) * kP * kN : prm.init;
+    const size_t ibase = segmented ? 0 : fbase;
+    // checkpoint k of this chain (whole-sequence forward chains only)
+    auto ckpt = [&](int k) -> float* {
+      return !kRev && prm.ckpt_out ? prm.ckpt_out + ((size_t)unit * prm.nk + k) * kP * kN : nullptr;
+    };
     uint8_t* slice = sm.out + 4096 * warp;  // this warp's 32 rows of the out tile
     // this warp's rows of the out tile to the input state of chunk c (rows of 64 bf16, [b,H,nc][N][P])
     auto send = [&](int c) {
@@ -273,24 +290,30 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
         tma_store_commit();
       }
     };
+    float* ck0 = ckpt(0);
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {  // S = init: into TMEM, and out as the first chunk's input state
       float v[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = prm.init ? prm.init[fbase + (size_t)(16 * q + e) * kN + n] : 0.f;
+      for (int e = 0; e < 16; ++e) v[e] = init ? init[ibase + (size_t)(16 * q + e) * kN + n] : 0.f;
       tmem_st16(srow + 16 * q, v);
       store_row_bf16(sm.out, n, 2 * q, v, 2);
+      if (ck0) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ck0[(size_t)(16 * q + e) * kN + n] = v[e];
+      }
     }
     send(chunk_of(0));
     tmem_wait_st();
-    for (int r = 0; r < nc; ++r) {
+    for (int r = 0; r < nsteps; ++r) {
       const int k = r % kScal;
       bool ok = mbar_wait(&sm.sc_ready[k], (r / kScal) & 1, status, 89);
       ok = ok && mbar_wait(&sm.p_ready, r & 1, status, 88);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const float a = sm.aend[k];
-      const bool more = r + 1 < nc;
+      const bool more = r + 1 < clen;
+      float* ckn = !kRev && prm.ckpt_out && more && (r + 1) % prm.every == 0 ? ckpt((r + 1) / prm.every) : nullptr;
       if (more) {  // the previous store has read the slice
         if (lane == 0) tma_store_wait_read0();
         __syncwarp();
@@ -313,6 +336,10 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, uin
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = fmaf(a, __uint_as_float(sv[e]), __uint_as_float(pv[e]));
         tmem_st16(srow + 16 * q, v);
+        if (ckn) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ckn[(size_t)(16 * q + e) * kN + n] = v[e];
+        }
         if (more) {
           store_row_bf16(sm.out, n, 2 * q, v, 2);
         } else if (prm.fin) {
@@ -413,6 +440,8 @@ struct ScanLaunch {
   ScanJob fwd, rev;
   CbJob cb;
   int n_fwd, n_rev, n_cb, H;
+  int nk;         // forward blocks per (batch, head): its segments, or 1
+  int rev_first;  // the reverse chains come first in the grid (the forward ones are short segments)
 };
 
 template <int kStU>
@@ -420,16 +449,27 @@ __global__ void __launch_bounds__(kThreads, 3) k_scan(const __grid_constant__ Sc
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   int i = blockIdx.x;
+  if (job.rev_first) {
+    if (i < job.n_rev) {
+      scan_chain<true, kStU>(job.rev, i % job.H, i / job.H, 0, smem);
+      return;
+    }
+    i -= job.n_rev;
+  }
   if (i < job.n_fwd) {
-    scan_chain<false, kStU>(job.fwd, i % job.H, i / job.H, smem);
+    const int unit = i / job.nk;
+    scan_chain<false, kStU>(job.fwd, unit % job.H, unit / job.H, i - unit * job.nk, smem);
     return;
   }
   i -= job.n_fwd;
-  if (i < job.n_rev) {
-    scan_chain<true, kStU>(job.rev, i % job.H, i / job.H, smem);
-    return;
+  if (!job.rev_first) {
+    if (i < job.n_rev) {
+      scan_chain<true, kStU>(job.rev, i % job.H, i / job.H, 0, smem);
+      return;
+    }
+    i -= job.n_rev;
   }
-  cb_tile(job.cb, i - job.n_rev, smem);
+  cb_tile(job.cb, i, smem);
 }
 
 // Three x / dy stages when three CTAs of them still fit an SM (all (batch, head) chains of one direction stay
@@ -460,11 +500,21 @@ cudaError_t launch_stages(const ScanLaunch& job, const char* name, cudaStream_t 
 
 size_t tc_scan_states_bytes(const Dims& d) { return (size_t)d.b * d.H * d.nc * kN * kP * sizeof(__nv_bfloat16); }
 
+size_t tc_checkpoints_bytes(const Dims& d, int every) {
+  const size_t nk = ((size_t)d.nc + every - 1) / every;
+  return (size_t)d.b * d.H * nk * kP * kN * sizeof(float);
+}
+
 cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, const void* B, const void* C,
                      const float* dt_raw, const float* A, float* CB, int* status, cudaStream_t st) {
   const uint64_t srows = (uint64_t)d.b * d.H * d.nc * kN;
   const long long chains = (long long)d.b * d.H, tiles = (long long)d.b * d.nc * d.G;
-  if ((fwd ? chains : 0) + (rev ? chains : 0) + tiles > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  const bool segmented = fwd && fwd->ckpt_in;
+  const int every = fwd && (fwd->ckpt_in || fwd->ckpt_out) ? fwd->every : 0;
+  if (every < 0 || (fwd && (fwd->ckpt_in || fwd->ckpt_out) && every < 1)) return cudaErrorInvalidValue;
+  const int nk = every > 0 ? (d.nc + every - 1) / every : 1;
+  const long long fwd_blocks = fwd ? chains * (segmented ? nk : 1) : 0;
+  if (fwd_blocks + (rev ? chains : 0) + tiles > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   ScanLaunch job;
   memset(&job, 0, sizeof(job));
   cudaError_t e = cudaSuccess;
@@ -477,7 +527,8 @@ cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, co
     e = make_tmap_seq_bf16(&j.u, s->u, d, (uint64_t)d.H * kP);
     if (e == cudaSuccess) e = make_tmap_bc_bf16(&j.k, r == 0 ? B : C, d);
     if (e == cudaSuccess) e = make_tmap_2d_bf16(&j.out, s->states, kP, srows, 64, 32);
-    j.prm = ScanParams{dt_raw, A, s->init, s->fin, status, d.T, d.H, d.hpg, d.nc, d.variant == kMimo, d.rs};
+    j.prm = ScanParams{dt_raw, A,  s->init, s->fin, status, d.T, d.H, d.hpg, d.nc, d.variant == kMimo, d.rs,
+                       s->ckpt_out, s->ckpt_in, every, nk};
   }
   if (e == cudaSuccess) e = make_tmap_bc_bf16(&job.cb.c, C, d);
   if (e == cudaSuccess) e = make_tmap_bc_bf16(&job.cb.b, B, d);
@@ -486,8 +537,10 @@ cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, co
   job.cb.status = status;
   job.cb.G = d.G;
   job.cb.nc = d.nc;
-  job.n_fwd = fwd ? (int)chains : 0;
+  job.n_fwd = (int)fwd_blocks;
   job.n_rev = rev ? (int)chains : 0;
+  job.nk = segmented ? nk : 1;
+  job.rev_first = segmented ? 1 : 0;
   job.n_cb = (int)tiles;
   job.H = d.H;
   const char* name = fwd && rev ? "k_tc_scan_pair_cb" : fwd ? "k_tc_states_cb" : "k_tc_dstates_cb";

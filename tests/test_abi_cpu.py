@@ -170,3 +170,45 @@ def test_tail_chunk_sizes_the_workspace_by_ceil(cuda_lib):
     ragged = binding.ssd_states_size(binding.problem(scaled(tc, seqlen=4096 - 63)))
     assert ragged == full
     assert binding.ssd_states_size(binding.problem(scaled(tc, seqlen=4096 + 1))) == full * 65 // 64
+
+
+def test_checkpoint_validation(cuda_lib):
+    """The checkpoint pair exists for the tensor-core problems only; its size is
+    b*H*ceil(nc/K)*P*N fp32 values; K < 1 and bad buffers fail on the host."""
+    import torch
+    c = CONFIGS["mamba2_2p7b_bf16"]
+    tc = binding.problem(c)
+    nc = c["seqlen"] // c["chunk"]
+    for every in (1, 3, 8, 64, 1000):
+        nk = -(-nc // every)
+        assert binding.ssd_checkpoints_size(tc, every) == c["batch"] * c["nheads"] * nk * c["headdim"] * c["dstate"] * 4
+    n = ctypes.c_size_t(0)
+    assert cuda_lib.ssd_checkpoints_size(ctypes.byref(tc), 0, ctypes.byref(n)) == 1  # SSD_ERR_INVALID_ARG
+    assert cuda_lib.ssd_checkpoints_size(ctypes.byref(tc), -2, ctypes.byref(n)) == 1
+    assert cuda_lib.ssd_checkpoints_size(ctypes.byref(tc), (1 << 30) + 1, ctypes.byref(n)) == 1
+    assert cuda_lib.ssd_checkpoints_size(ctypes.byref(tc), 8, None) == 1
+    for name in ("mamba2_tiny_fp32", "mamba1_fp32", "mimo_r4_bf16"):
+        p = binding.problem(CONFIGS[name])
+        assert cuda_lib.ssd_checkpoints_size(ctypes.byref(p), 8, ctypes.byref(n)) == 2  # SSD_ERR_SHAPE
+    if torch.cuda.is_available():
+        return  # the rest uses fake device addresses
+    fake = 1 << 20
+    need_k = binding.ssd_checkpoints_size(tc, 8)
+    need_f = binding.ssd_workspace_size(tc, False)
+    need_b = binding.ssd_workspace_size(tc, True)
+    fwd = cuda_lib.ssd_forward_checkpointed
+    # prob, x, dt_raw, A, B, C, s0, y, s_final, every, ckpt, ckpt_bytes, ws, ws_bytes, stream
+    assert fwd(ctypes.byref(tc), fake, fake, fake, fake, fake, None, fake, fake, 8, None, need_k, fake, need_f,
+               None) == 1  # no checkpoint buffer
+    assert fwd(ctypes.byref(tc), fake, fake, fake, fake, fake, None, fake, fake, 8, fake, need_k - 1, fake, need_f,
+               None) == 5  # too small
+    assert fwd(ctypes.byref(tc), fake, fake, fake, fake, fake, None, fake, fake, 8, fake + 8, need_k, fake, need_f,
+               None) == 4  # misaligned
+    assert fwd(ctypes.byref(tc), fake, fake, fake, fake, fake, None, fake, fake, 0, fake, need_k, fake, need_f,
+               None) == 1  # K = 0
+    bwd = cuda_lib.ssd_backward_checkpointed
+    # prob, dy, ds_final, x, dt_raw, A, B, C, every, ckpt, ckpt_bytes, dx, ddt_raw, dA, dB, dC, ds0, ws, ws_bytes, stream
+    assert bwd(ctypes.byref(tc), fake, fake, fake, fake, fake, fake, fake, 8, fake, need_k, fake, fake, fake, fake,
+               fake, fake, fake, need_b - 1, None) == 5  # workspace too small
+    assert bwd(ctypes.byref(tc), fake, fake, fake, fake, fake, fake, fake, 8, fake, need_k, fake, fake, fake, fake,
+               fake, fake, None, need_b, None) == 1  # no workspace

@@ -13,7 +13,8 @@ from selective_state_space_ssd_gb300 import binding
 from selective_state_space_ssd_gb300 import inputs as synth
 from selective_state_space_ssd_gb300.configs import CONFIGS, scaled
 
-from parity import compare, run_gpu, run_oracle, to_device
+import oracle
+from parity import TOL, compare, rel_err, run_gpu, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -124,6 +125,55 @@ def test_stashed_states_give_the_recompute_bits(name):
         st = states.view(torch.bfloat16).view(cfg["batch"], cfg["nheads"], nc, cfg["dstate"], cfg["headdim"])
         want = torch.zeros_like(st[:, :, 0]) if zero_s0 else dev["s0"].transpose(-1, -2).to(torch.bfloat16)
         assert torch.equal(st[:, :, 0], want)
+
+
+@pytest.mark.parametrize("name,every", [("m2_bf16_tiles", 1), ("m2_bf16_tiles", 2), ("m2_bf16_split_runs", 3),
+                                        ("m2_bf16_tail", 2), ("m2_bf16_tail", 64), ("full_2p7b", 8)])
+def test_checkpointed_backward_gives_the_recompute_bits(name, every):
+    """ssd_forward_checkpointed returns ssd_forward's bits plus fp32 checkpoints
+    every K chunks; ssd_backward_checkpointed, which replays the chunk states in
+    segments of K chunks from them, returns ssd_backward's bits (which the other
+    tests hold to the oracle), with and without s0, for K = 1, several K that
+    leave a short last segment, and K >= the chunk count (s0 only)."""
+    cfg = CONFIGS["mamba2_2p7b_bf16"] if name == "full_2p7b" else SMALL[name]
+    for zero_s0 in (False, True):
+        dev = to_device(synth.make_inputs(cfg, seed=7, zero_s0=zero_s0))
+        s0 = None if zero_s0 else dev["s0"]
+        y, sf = binding.forward(cfg, dev["x"], dev["dt_raw"], dev["A"], dev["B"], dev["C"], s0)
+        y2, sf2, ck = binding.forward_checkpointed(cfg, dev["x"], dev["dt_raw"], dev["A"], dev["B"], dev["C"], s0,
+                                                   every=every)
+        g = binding.backward(cfg, dev["dy"], dev["ds_final"], dev["x"], dev["dt_raw"], dev["A"], dev["B"], dev["C"],
+                             s0)
+        g2 = binding.backward_checkpointed(cfg, dev["dy"], dev["ds_final"], dev["x"], dev["dt_raw"], dev["A"],
+                                           dev["B"], dev["C"], ck, every=every)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2) and torch.equal(sf, sf2)
+        for k in g:
+            assert torch.equal(g[k], g2[k]), k
+        # entry 0 of every (batch, head) is s0 itself (fp32, [P][N]), or zeros
+        want = torch.zeros_like(ck[:, :, 0]) if zero_s0 else dev["s0"]
+        assert torch.equal(ck[:, :, 0], want)
+
+
+def test_checkpoints_are_the_states_at_the_chunk_boundaries():
+    """Entry k of the checkpoints is the state entering chunk k*K: the oracle's
+    s_final of the sequence cut after k*K chunks, within the bf16 tolerance."""
+    cfg = SMALL["m2_bf16_split_runs"]
+    every = 2
+    cpu = synth.make_inputs(cfg, seed=8)
+    dev = to_device(cpu)
+    _, _, ck = binding.forward_checkpointed(cfg, dev["x"], dev["dt_raw"], dev["A"], dev["B"], dev["C"], dev["s0"],
+                                            every=every)
+    torch.cuda.synchronize()
+    L = cfg["chunk"]
+    nc = -(-cfg["seqlen"] // L)
+    assert ck.shape[2] == -(-nc // every) >= 2
+    f64 = synth.as_float64(cpu)
+    for k in range(1, ck.shape[2]):
+        T1 = k * every * L
+        cut = dict(f64, x=f64["x"][:, :T1], dt_raw=f64["dt_raw"][:, :T1], B=f64["B"][:, :T1], C=f64["C"][:, :T1])
+        ref = oracle.forward("mamba2", cut)["s_final"]
+        assert rel_err(ck[:, :, k], ref) <= TOL[cfg["dtype"]], k
 
 
 def test_zero_seed_and_zero_dy():
