@@ -15,6 +15,9 @@ Two independent float64 implementations live here:
 * :mod:`oracle.chunkwise` -- the chunkwise (K1..K5) form and its backward,
   written in numpy from the Mamba-3 combined_backward.rs page's algebra.
   It exists to pin the serial oracle (the two must agree to rounding).
+* :mod:`oracle.kda` -- the KDA delta-rule recurrence (the notes page
+  "sec-10.tex": forward F1-F6 and the reverse loop of steps 1-6, store-all),
+  in numpy, a second workload with its own entry points in the library.
 
 Every array argument is converted to contiguous float64; results are new
 float64 arrays.  Shapes follow the library's layouts:

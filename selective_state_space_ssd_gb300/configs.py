@@ -27,6 +27,18 @@ CONFIGS = {
 
 HEADLINE = "mamba2_2p7b_bf16"
 
+# The KDA delta-rule recurrence (a second workload with its own entry points): batch, seqlen T, nheads H (query
+# and key heads), value_heads HV (a multiple of H: each query / key head serves HV / H value heads), key_dim K,
+# value_dim V, fp32 io.  The pages give no sizes for it; these are a head dimension of 128 and a short context.
+KDA_CONFIGS = {
+    # tiny; the float64 oracle's finite differences cover every element of it
+    "kda_tiny_fp32": dict(variant="kda", dtype="f32", batch=1, seqlen=16, nheads=2, value_heads=4, key_dim=8,
+                          value_dim=8),
+    # head dimension 128, 16 value heads over 8 query / key heads, T = 1024
+    "kda_fp32": dict(variant="kda", dtype="f32", batch=2, seqlen=1024, nheads=8, value_heads=16, key_dim=128,
+                     value_dim=128),
+}
+
 
 def tokens(cfg: dict) -> int:
     """Tokens per forward+backward pair: batch x seqlen."""

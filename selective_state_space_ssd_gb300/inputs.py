@@ -72,6 +72,44 @@ def make_inputs(cfg: dict, seed: int = 0, zero_s0: bool = False) -> dict:
     return out
 
 
+def kda_shapes(cfg: dict) -> dict:
+    """Shapes of the KDA inputs (library layouts)."""
+    b, T, H, HV, K, V = (cfg[n] for n in ("batch", "seqlen", "nheads", "value_heads", "key_dim", "value_dim"))
+    return dict(q=(b, T, H, K), k=(b, T, H, K), v=(b, T, HV, V), g=(b, T, HV, K), beta=(b, T, HV),
+                s0=(b, HV, K, V), do=(b, T, HV, V), ds_final=(b, HV, K, V))
+
+
+def make_kda_inputs(cfg: dict, seed: int = 0, zero_s0: bool = False) -> dict:
+    """Draw the KDA inputs on the CPU (fp32), in the fixed order q, k, v, g,
+    beta, s0, do, ds_final:
+
+    * q, v, do, ds_final ~ N(0, 1)
+    * k: N(0, 1) draws scaled to unit length per (b, t, h), so that every step's
+      I - beta k k^T keeps the state bounded over long sequences
+    * g = -U(0.01, 0.5) per key row (exp(g) in (0.61, 0.99))
+    * beta = U(0, 1)
+    * s0 ~ 0.1 * N(0, 1)
+    The attention scale is K^-1/2 (``kda_scale``)."""
+    g = torch.Generator().manual_seed(seed)
+    sh = kda_shapes(cfg)
+    out = {}
+    out["q"] = torch.randn(sh["q"], generator=g).contiguous()
+    kr = torch.randn(sh["k"], generator=g)
+    out["k"] = (kr / kr.norm(dim=-1, keepdim=True)).contiguous()
+    out["v"] = torch.randn(sh["v"], generator=g).contiguous()
+    out["g"] = (-(torch.rand(sh["g"], generator=g) * 0.49 + 0.01)).contiguous()
+    out["beta"] = torch.rand(sh["beta"], generator=g).contiguous()
+    s0 = 0.1 * torch.randn(sh["s0"], generator=g)
+    out["s0"] = torch.zeros_like(s0) if zero_s0 else s0.contiguous()
+    out["do"] = torch.randn(sh["do"], generator=g).contiguous()
+    out["ds_final"] = torch.randn(sh["ds_final"], generator=g).contiguous()
+    return out
+
+
+def kda_scale(cfg: dict) -> float:
+    return 1.0 / math.sqrt(cfg["key_dim"])
+
+
 def as_float64(inputs: dict) -> dict:
     """The same values widened to float64 numpy arrays (for the oracle)."""
     return {k: (None if v is None else v.double().numpy()) for k, v in inputs.items()}
