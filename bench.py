@@ -83,9 +83,46 @@ def tensor_flops(cfg, executed=False):
     return b * nc * (H * per_head + G * per_group)
 
 
+def kda_tensor_bytes(cfg):
+    """Bytes of every KDA input / output tensor (fp32)."""
+    b, T, H, HV, K, V = (cfg[k] for k in ("batch", "seqlen", "nheads", "value_heads", "key_dim", "value_dim"))
+    return {"q": b * T * H * K * 4, "v": b * T * HV * V * 4, "g": b * T * HV * K * 4, "beta": b * T * HV * 4,
+            "s": b * HV * K * V * 4}
+
+
+def kda_algorithmic_bytes(cfg):
+    """Leaf inputs and outputs of the KDA forward and backward: the forward reads q, k, v, g, beta, s0 and writes
+    o, s_final; the backward re-reads them with do, ds_final and writes dq, dk, dv, dg, dbeta, ds0."""
+    t = kda_tensor_bytes(cfg)
+    ins = 2 * t["q"] + t["v"] + t["g"] + t["beta"] + t["s"]
+    fwd = ins + t["v"] + t["s"]
+    bwd = ins + t["v"] + t["s"] + 2 * t["q"] + t["v"] + t["g"] + t["beta"] + t["s"]
+    return fwd, bwd
+
+
+def kda_kernel_bytes(name, cfg):
+    t = kda_tensor_bytes(cfg)
+    b, T, HV, K, V = (cfg[k] for k in ("batch", "seqlen", "value_heads", "key_dim", "value_dim"))
+    ins = 2 * t["q"] + t["v"] + t["g"] + t["beta"] + t["s"]
+    ckpt = b * HV * (-(-T // 16)) * K * V * 4
+    per_head = b * T * HV * K * 4  # dq or dk per value head
+    table = {
+        "k_kda_forward": ins + t["v"] + t["s"],
+        "k_kda_checkpoints": ins + ckpt,
+        # the replay and the reverse pass read the step inputs twice; do, ds_final and the checkpoints in;
+        # dv, dg, dbeta, ds0 and the per-value-head dq, dk out (the replay scratch stays in L2)
+        "k_kda_backward": 2 * (ins - t["s"]) + t["v"] + t["s"] + ckpt + t["v"] + t["g"] + t["beta"] + t["s"]
+                          + 2 * per_head,
+        "k_kda_gva": 2 * per_head + 2 * t["q"],
+    }
+    return table.get(name)
+
+
 def kernel_bytes(name, cfg):
     """Compulsory HBM bytes of one launch of each kernel: what it must read and
     write given its own inputs and outputs (intermediates included)."""
+    if cfg["variant"] == "kda":
+        return kda_kernel_bytes(name, cfg)
     t = tensor_bytes(cfg)
     b, T, H, P, N = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate"))
     L = cfg["chunk"]

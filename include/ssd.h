@@ -327,6 +327,56 @@ ssd_status ssd_read_status(const void* ws, int32_t* code, void* cuda_stream);
 ssd_status ssd_wait_selftest(void* ws, uint32_t limit_us, void* cuda_stream);
 
 /*
+ * KDA: the gated delta-rule recurrence of the notes page "sec-10.tex"
+ * (section "反向传播推导"), a second workload beside the selective scan, and
+ * its BPTT backward (the page's reverse-time steps 1-6).  fp32 io and
+ * arithmetic.  Per batch element and value head, with state S [K, V]:
+ *     S_dec = exp(g_t) (.) S_{t-1}     (one log-decay per key row)
+ *     r_t   = v_t - k_t^T S_dec
+ *     S_t   = S_dec + beta_t k_t (x) r_t
+ *     o_t   = (scale q_t)^T S_t
+ * Value head hv reads query / key head hv / G, G = value_heads / nheads (the
+ * page's grouped value heads); dq, dk of a query / key head are the sums over
+ * its G value heads.
+ *
+ * Layouts (row-major, fp32, 16-byte aligned): q, k, dq, dk [b,T,H,K];
+ * v, o, do, dv [b,T,HV,V]; g, dg [b,T,HV,K]; beta, dbeta [b,T,HV];
+ * s0, s_final, ds_final, ds0 [b,HV,K,V].  s0 may be NULL (zeros).
+ * Limits of this build: key_dim <= 128, value_dim <= 128 (SSD_ERR_SHAPE);
+ * value_heads a multiple of nheads (SSD_ERR_SHAPE).
+ *
+ * ssd_kda_workspace_size: device workspace of the forward (backward == 0) or
+ *   backward; host-only.  The backward's holds fp32 checkpoints of the state
+ *   every 16 steps (b*HV*ceil(T/16)*K*V*4 bytes), a replay scratch of 16
+ *   steps per (b, hv) and the per-value-head dq, dk.  Its first 4 bytes are
+ *   the device status word, as for ssd_forward.
+ * ssd_kda_forward: o and s_final.
+ * ssd_kda_backward: dq, dk, dv, dg, dbeta and ds0 of <do, o> + <ds_final,
+ *   s_final> (ds_final required); recomputes the states from the leaf inputs
+ *   (no forward intermediate is needed).  Deterministic: every sum has a
+ *   fixed order.
+ * Errors as for ssd_forward; every error is returned before anything is
+ * enqueued.
+ */
+typedef struct {
+  int64_t batch;
+  int64_t seqlen;
+  int64_t nheads;      /* H: query / key heads */
+  int64_t value_heads; /* HV: a multiple of H */
+  int64_t key_dim;     /* K */
+  int64_t value_dim;   /* V */
+} ssd_kda_problem;
+
+ssd_status ssd_kda_workspace_size(const ssd_kda_problem* prob, int backward, size_t* bytes);
+ssd_status ssd_kda_forward(const ssd_kda_problem* prob, const float* q, const float* k, const float* v,
+                           const float* g, const float* beta, const float* s0, float scale, float* o, float* s_final,
+                           void* ws, size_t ws_bytes, void* cuda_stream);
+ssd_status ssd_kda_backward(const ssd_kda_problem* prob, const float* dout, const float* ds_final, const float* q,
+                            const float* k, const float* v, const float* g, const float* beta, const float* s0,
+                            float scale, float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ds0,
+                            void* ws, size_t ws_bytes, void* cuda_stream);
+
+/*
  * Per-launch timing, for diagnostics and roofline measurement.
  *
  * ssd_profile_start(capacity): every later ssd_forward / ssd_backward call

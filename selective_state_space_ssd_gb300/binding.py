@@ -43,7 +43,13 @@ class ssd_problem(ctypes.Structure):
 EXPORTS = ("ssd_workspace_size", "ssd_forward", "ssd_backward", "ssd_forward_static", "ssd_profile_start",
            "ssd_profile_stop", "ssd_status_string", "ssd_version", "ssd_states_size", "ssd_forward_stash",
            "ssd_backward_stashed", "ssd_forward_static_status", "ssd_read_status", "ssd_wait_selftest",
-           "ssd_checkpoints_size", "ssd_forward_checkpointed", "ssd_backward_checkpointed")
+           "ssd_checkpoints_size", "ssd_forward_checkpointed", "ssd_backward_checkpointed",
+           "ssd_kda_workspace_size", "ssd_kda_forward", "ssd_kda_backward")
+
+
+class ssd_kda_problem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("value_heads", ctypes.c_int64), ("key_dim", ctypes.c_int64), ("value_dim", ctypes.c_int64)]
 
 
 class ssd_kernel_time(ctypes.Structure):
@@ -104,6 +110,13 @@ def load(path: str | None = None):
         lib.ssd_backward_checkpointed.argtypes = ([ctypes.POINTER(ssd_problem)] + [vp] * 7 + [i64, vp, sz] + [vp] * 6 +
                                                  [vp, sz, vp])
         lib.ssd_backward_checkpointed.restype = i32
+        kp = ctypes.POINTER(ssd_kda_problem)
+        lib.ssd_kda_workspace_size.argtypes = [kp, i32, ctypes.POINTER(sz)]
+        lib.ssd_kda_workspace_size.restype = i32
+        lib.ssd_kda_forward.argtypes = [kp] + [vp] * 6 + [ctypes.c_float, vp, vp, vp, sz, vp]
+        lib.ssd_kda_forward.restype = i32
+        lib.ssd_kda_backward.argtypes = [kp] + [vp] * 8 + [ctypes.c_float] + [vp] * 6 + [vp, sz, vp]
+        lib.ssd_kda_backward.restype = i32
         _lib = lib
         return lib
 
@@ -348,4 +361,63 @@ def backward_checkpointed(cfg: dict, dy, ds_final, x, dt_raw, A, B, C, ckpt, eve
     ws, n = workspace if workspace is not None else _workspace(prob, True, dev)
     ssd_backward_checkpointed(prob, dy, ds_final, x, dt_raw, A, B, C, every, ckpt, ckpt.numel() * 4, out["dx"],
                               out["ddt_raw"], out["dA"], out["dB"], out["dC"], out["ds0"], ws, n, stream)
+    return out
+
+
+# ------------------------------------------------------------- KDA (gated delta rule)
+def kda_problem(cfg: dict) -> ssd_kda_problem:
+    return ssd_kda_problem(cfg["batch"], cfg["seqlen"], cfg["nheads"], cfg["value_heads"], cfg["key_dim"],
+                           cfg["value_dim"])
+
+
+def ssd_kda_workspace_size(prob: ssd_kda_problem, backward: bool) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().ssd_kda_workspace_size(ctypes.byref(prob), int(bool(backward)), ctypes.byref(out))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_kda_workspace_size")
+    return out.value
+
+
+def ssd_kda_forward(prob, q, k, v, g, beta, s0, scale, o, s_final, ws, ws_bytes, stream=None) -> None:
+    st = load().ssd_kda_forward(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0),
+                                float(scale), _ptr(o), _ptr(s_final), _ptr(ws), int(ws_bytes), _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_kda_forward")
+
+
+def ssd_kda_backward(prob, dout, ds_final, q, k, v, g, beta, s0, scale, dq, dk, dv, dg, dbeta, ds0, ws, ws_bytes,
+                     stream=None) -> None:
+    st = load().ssd_kda_backward(ctypes.byref(prob), _ptr(dout), _ptr(ds_final), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(s0), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                                 _ptr(dbeta), _ptr(ds0), _ptr(ws), int(ws_bytes), _stream(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_kda_backward")
+
+
+def _kda_workspace(prob, backward, device):
+    n = ssd_kda_workspace_size(prob, backward)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device), n
+
+
+def kda_forward(cfg: dict, q, k, v, g, beta, s0=None, scale=None, stream=None, workspace=None):
+    """Allocate o, s_final and run ``ssd_kda_forward``; scale defaults to key_dim^-1/2."""
+    prob = kda_problem(cfg)
+    scale = cfg["key_dim"] ** -0.5 if scale is None else scale
+    o = torch.empty_like(v)
+    s_final = torch.empty((cfg["batch"], cfg["value_heads"], cfg["key_dim"], cfg["value_dim"]), dtype=torch.float32,
+                          device=v.device)
+    ws, n = workspace if workspace is not None else _kda_workspace(prob, False, v.device)
+    ssd_kda_forward(prob, q, k, v, g, beta, s0, scale, o, s_final, ws, n, stream)
+    return o, s_final
+
+
+def kda_backward(cfg: dict, dout, ds_final, q, k, v, g, beta, s0=None, scale=None, stream=None, workspace=None):
+    """Allocate the gradients and run ``ssd_kda_backward``; returns dq, dk, dv, dg, dbeta, ds0."""
+    prob = kda_problem(cfg)
+    scale = cfg["key_dim"] ** -0.5 if scale is None else scale
+    out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v), "dg": torch.empty_like(g),
+           "dbeta": torch.empty_like(beta), "ds0": torch.empty_like(ds_final)}
+    ws, n = workspace if workspace is not None else _kda_workspace(prob, True, v.device)
+    ssd_kda_backward(prob, dout, ds_final, q, k, v, g, beta, s0, scale, out["dq"], out["dk"], out["dv"], out["dg"],
+                     out["dbeta"], out["ds0"], ws, n, stream)
     return out

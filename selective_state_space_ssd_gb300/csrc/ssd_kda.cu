@@ -1,0 +1,456 @@
+// The KDA delta-rule recurrence and its BPTT backward (the notes page
+// "sec-10.tex", section "反向传播推导": forward F1-F6, reverse steps 1-6), fp32.
+//
+// Per batch element b and value head hv (query / key head h = hv / G), the
+// state S is K x V.  Each warp owns 8 value columns of one (b, hv) and keeps
+// its K x 8 slice of S in registers: lane l holds rows l, l + 32, l + 64,
+// l + 96.  Column work (p = k^T S_dec, o = q^T S, dr) reduces over the key
+// rows of a column: a warp reduction.  Row work of the backward (dq, da, dk,
+// dg) reduces over the value columns: each warp writes its 8-column partial
+// sums to shared memory, and after one barrier per step the CTA's first K
+// threads add the partials of every warp, in warp order.
+//
+//   forward   k_kda_forward<false>: o and s_final, every warp on its own.
+//   backward  1. k_kda_forward<true> replays the forward from the leaf inputs
+//                and keeps the state entering every 16th step (checkpoints);
+//             2. k_kda_backward, one CTA per (b, hv) with all its column
+//                warps, walks the 16-step segments from the last: it replays
+//                the segment from its checkpoint (S_dec and r of every step to
+//                a per-CTA scratch), then runs steps 1-6 backwards through it,
+//                carrying dS_acc in registers across segments;
+//             3. k_kda_gva adds the per-value-head dq, dk onto their query /
+//                key head in a fixed order (the page's view + sum) and scales
+//                dq.
+#include <math.h>
+#include <stdint.h>
+
+#include <initializer_list>
+
+#include "../../include/ssd.h"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kRows = 4;    // key rows per lane: K <= 128
+constexpr int kCols = 8;    // value columns per warp: V <= 128 in at most 16 warps
+constexpr int kSeg = 16;    // steps per checkpoint segment
+constexpr int kMaxWarps = 16;
+
+struct KdaDims {
+  int b, T, H, HV, G, K, V;
+  int nw;    // column warps per (b, hv): ceil(V / 8)
+  int nseg;  // checkpoint segments: ceil(T / 16)
+};
+
+struct KdaIn {
+  const float* q;  // [b,T,H,K]
+  const float* k;  // [b,T,H,K]
+  const float* v;  // [b,T,HV,V]
+  const float* g;  // [b,T,HV,K]
+  const float* beta;  // [b,T,HV]
+  float scale;
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// The per-step inputs of one warp: its rows of q (scaled), k and exp(g), beta, and its columns of v.
+struct StepIn {
+  float q[kRows], k[kRows], eg[kRows], v[kCols], beta;
+};
+
+__device__ __forceinline__ void load_step(const KdaIn& in, const KdaDims& d, int b, int hv, int t, int lane, int col0,
+                                          StepIn& s) {
+  const int h = hv / d.G;
+  const size_t qk = ((size_t)b * d.T + t) * d.H + h, gv = ((size_t)b * d.T + t) * d.HV + hv;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int r = lane + 32 * i;
+    const bool ok = r < d.K;
+    s.q[i] = ok ? in.q[qk * d.K + r] * in.scale : 0.f;
+    s.k[i] = ok ? in.k[qk * d.K + r] : 0.f;
+    s.eg[i] = ok ? __expf(in.g[gv * d.K + r]) : 1.f;
+  }
+#pragma unroll
+  for (int j = 0; j < kCols; ++j) s.v[j] = col0 + j < d.V ? in.v[gv * d.V + col0 + j] : 0.f;
+  s.beta = in.beta[gv];
+}
+
+// F1-F5 on this warp's slice: S <- S_dec + beta k (x) (v - k^T S_dec); returns r (all lanes).
+__device__ __forceinline__ void delta_step(float (&S)[kRows][kCols], const StepIn& s, float (&r)[kCols]) {
+#pragma unroll
+  for (int i = 0; i < kRows; ++i)
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) S[i][j] *= s.eg[i];  // F1
+#pragma unroll
+  for (int j = 0; j < kCols; ++j) {
+    float p = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) p = fmaf(s.k[i], S[i][j], p);
+    r[j] = s.v[j] - warp_sum(p);  // F2, F3
+  }
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const float a = s.beta * s.k[i];  // F4
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) S[i][j] = fmaf(a, r[j], S[i][j]);  // F5
+  }
+}
+
+// Forward: one warp per 8 columns of one (b, hv); grid (b * HV, ceil(nw / 2)), two warps per CTA.
+// kCkpt: the backward's replay, which writes only the state entering every 16th step (ckpt [b*HV][nseg][K][V]);
+// otherwise o [b,T,HV,V] and s_final [b,HV,K,V].
+template <bool kCkpt>
+__global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const float* __restrict__ s0, float* o,
+                                                    float* s_final, float* ckpt) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.y * 2 + (threadIdx.x >> 5);
+  if (w >= d.nw) return;
+  const int unit = blockIdx.x, b = unit / d.HV, hv = unit - b * d.HV;
+  const int col0 = kCols * w;
+  const size_t sbase = (size_t)unit * d.K * d.V;
+  float S[kRows][kCols];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i)
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) {
+      const int r = lane + 32 * i, c = col0 + j;
+      S[i][j] = s0 && r < d.K && c < d.V ? s0[sbase + (size_t)r * d.V + c] : 0.f;
+    }
+  for (int t = 0; t < d.T; ++t) {
+    if (kCkpt && t % kSeg == 0) {
+      float* dst = ckpt + ((size_t)unit * d.nseg + t / kSeg) * d.K * d.V;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i)
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          const int r = lane + 32 * i, c = col0 + j;
+          if (r < d.K && c < d.V) dst[(size_t)r * d.V + c] = S[i][j];
+        }
+    }
+    StepIn s;
+    load_step(in, d, b, hv, t, lane, col0, s);
+    float r[kCols];
+    delta_step(S, s, r);
+    if (!kCkpt) {
+      float out = 0.f;  // o[col0 + lane] for lanes 0-7
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        float x = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) x = fmaf(s.q[i], S[i][j], x);  // F6
+        x = warp_sum(x);
+        if (lane == j) out = x;
+      }
+      if (lane < kCols && col0 + lane < d.V) o[(((size_t)b * d.T + t) * d.HV + hv) * d.V + col0 + lane] = out;
+    }
+  }
+  if (!kCkpt) {
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        const int r = lane + 32 * i, c = col0 + j;
+        if (r < d.K && c < d.V) s_final[sbase + (size_t)r * d.V + c] = S[i][j];
+      }
+  }
+}
+
+struct KdaBwdOut {
+  const float* dout;      // do [b,T,HV,V]
+  const float* ds_final;  // [b,HV,K,V]
+  float* dq_e;            // [b,T,HV,K]: per value head, w.r.t. the scaled q
+  float* dk_e;            // [b,T,HV,K]
+  float* dv;              // [b,T,HV,V]
+  float* dg;              // [b,T,HV,K]
+  float* dbeta;           // [b,T,HV]
+  float* ds0;             // [b,HV,K,V]
+  const float* ckpt;      // [b*HV][nseg][K][V]
+  float* scratch;         // per CTA: kSeg steps x (nw warps x 32 values x 32 lanes of S_dec, then V values of r)
+};
+
+// Backward: one CTA per (b, hv), d.nw warps (32 * nw threads).  Dynamic shared memory: the per-step row
+// partials of the column warps, double-buffered, [buf][warp][dq, da, dk_r, dg][row 0..127], then the dbeta
+// partial of each warp, [buf][warp].
+__global__ void __launch_bounds__(32 * kMaxWarps) k_kda_backward(KdaIn in, KdaDims d, KdaBwdOut out) {
+  extern __shared__ float kda_smem[];
+  constexpr int kPartRow = 32 * kRows;
+  auto part = [&](int buf, int w, int m) { return kda_smem + ((size_t)(buf * d.nw + w) * 4 + m) * kPartRow; };
+  float* dbp = kda_smem + (size_t)2 * d.nw * 4 * kPartRow;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int unit = blockIdx.x, b = unit / d.HV, hv = unit - b * d.HV;
+  const int col0 = kCols * w;
+  const size_t sbase = (size_t)unit * d.K * d.V;
+  const size_t step_floats = (size_t)d.nw * 32 * kRows * kCols + d.V;  // one step of the scratch
+  float* scr = out.scratch + (size_t)unit * kSeg * step_floats;
+  // this lane's S_dec of row slot i, column j, in scratch step st: lane-contiguous, so a warp's access is coalesced
+  auto sd_at = [&](float* st, int i, int j) -> float& {
+    return st[(size_t)w * 32 * kRows * kCols + (i * kCols + j) * 32 + lane];
+  };
+  float dS[kRows][kCols];  // dS_acc, seeded with ds_final
+#pragma unroll
+  for (int i = 0; i < kRows; ++i)
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) {
+      const int r = lane + 32 * i, c = col0 + j;
+      dS[i][j] = r < d.K && c < d.V ? out.ds_final[sbase + (size_t)r * d.V + c] : 0.f;
+    }
+  int step = 0;  // steps done, for the double buffer
+  for (int sg = d.nseg - 1; sg >= 0; --sg) {
+    const int t0 = sg * kSeg, t1 = min(d.T, t0 + kSeg);
+    // replay the segment from its checkpoint: S_dec and r of every step to the scratch
+    {
+      float S[kRows][kCols];
+      const float* src = out.ckpt + ((size_t)unit * d.nseg + sg) * d.K * d.V;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i)
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          const int r = lane + 32 * i, c = col0 + j;
+          S[i][j] = r < d.K && c < d.V ? src[(size_t)r * d.V + c] : 0.f;
+        }
+      for (int t = t0; t < t1; ++t) {
+        StepIn s;
+        load_step(in, d, b, hv, t, lane, col0, s);
+        float r[kCols];
+        float* st = scr + (size_t)(t - t0) * step_floats;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i)
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) sd_at(st, i, j) = S[i][j] * s.eg[i];
+        delta_step(S, s, r);
+        float rv = r[0];
+#pragma unroll
+        for (int j = 1; j < kCols; ++j)
+          if (lane == j) rv = r[j];
+        if (lane < kCols && col0 + lane < d.V) st[(size_t)d.nw * 32 * kRows * kCols + col0 + lane] = rv;
+      }
+    }
+    __syncwarp();  // the r values of the warp's columns, written by lanes 0-7, are read by every lane
+    // steps 1-6 backwards through the segment
+    for (int t = t1 - 1; t >= t0; --t, ++step) {
+      StepIn s;
+      load_step(in, d, b, hv, t, lane, col0, s);
+      float* st = scr + (size_t)(t - t0) * step_floats;
+      const size_t gv = ((size_t)b * d.T + t) * d.HV + hv;
+      float r[kCols], dov[kCols], u[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        const bool ok = col0 + j < d.V;
+        r[j] = ok ? st[(size_t)d.nw * 32 * kRows * kCols + col0 + j] : 0.f;
+        dov[j] = ok ? out.dout[gv * d.V + col0 + j] : 0.f;
+      }
+      const int pb = step & 1;
+      // step 1: dS_acc += q (x) do;  dq = S_t do with S_t = S_dec + beta k (x) r;  step 2: da = dS_acc r
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const float a = s.beta * s.k[i];
+        float xq = 0.f, xa = 0.f;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          dS[i][j] = fmaf(s.q[i], dov[j], dS[i][j]);
+          xq = fmaf(dov[j], fmaf(a, r[j], sd_at(st, i, j)), xq);
+          xa = fmaf(r[j], dS[i][j], xa);
+        }
+        part(pb, w, 0)[lane + 32 * i] = xq;
+        part(pb, w, 1)[lane + 32 * i] = xa;
+      }
+      // step 2: dr = a^T dS_acc = beta u with u = k^T dS_acc per column (a warp reduction);
+      // step 3: dbeta = sum_k k da = sum_v r u
+      float dbw = 0.f;
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        float x = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) x = fmaf(s.k[i], dS[i][j], x);
+        u[j] = warp_sum(x);
+        dbw = fmaf(r[j], u[j], dbw);
+      }
+      // step 4: dv = dr,  dk_r = -S_dec dr;  step 5: dS_dec = dS_acc - k (x) dr (both paths),
+      // dg = rowsum(S_dec o dS_dec),  dS_{t-1} = exp(g) o dS_dec
+      float dvo = 0.f;
+#pragma unroll
+      for (int j = 0; j < kCols; ++j)
+        if (lane == j) dvo = s.beta * u[j];
+      if (lane < kCols && col0 + lane < d.V) out.dv[gv * d.V + col0 + lane] = dvo;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        float xk = 0.f, xg = 0.f;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          const float dr = s.beta * u[j];
+          const float sdv = sd_at(st, i, j);
+          xk = fmaf(-sdv, dr, xk);
+          const float tot = fmaf(-s.k[i], dr, dS[i][j]);
+          xg = fmaf(sdv, tot, xg);
+          dS[i][j] = s.eg[i] * tot;
+        }
+        part(pb, w, 2)[lane + 32 * i] = xk;
+        part(pb, w, 3)[lane + 32 * i] = xg;
+      }
+      if (lane == 0) dbp[pb * d.nw + w] = dbw;
+      __syncthreads();
+      // the rows: partials of every column warp added in warp order
+      for (int row = threadIdx.x; row < d.K; row += blockDim.x) {
+        float q_ = 0.f, a_ = 0.f, k_ = 0.f, g_ = 0.f;
+        for (int ww = 0; ww < d.nw; ++ww) {
+          q_ += part(pb, ww, 0)[row];
+          a_ += part(pb, ww, 1)[row];
+          k_ += part(pb, ww, 2)[row];
+          g_ += part(pb, ww, 3)[row];
+        }
+        const size_t gk = gv * d.K + row;
+        out.dq_e[gk] = q_;
+        out.dk_e[gk] = fmaf(s.beta, a_, k_);  // step 6: dk = beta da + dk_r
+        out.dg[gk] = g_;
+      }
+      if (threadIdx.x == 0) {
+        float x = 0.f;
+        for (int ww = 0; ww < d.nw; ++ww) x += dbp[pb * d.nw + ww];
+        out.dbeta[gv] = x;
+      }
+    }
+    __syncwarp();  // this segment's scratch has been read before the next replay overwrites it
+  }
+#pragma unroll
+  for (int i = 0; i < kRows; ++i)
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) {
+      const int r = lane + 32 * i, c = col0 + j;
+      if (r < d.K && c < d.V) out.ds0[sbase + (size_t)r * d.V + c] = dS[i][j];
+    }
+}
+
+// dq[b,t,h,:] = scale * sum_{j < G} dq_e[b,t,h*G+j,:],  dk[b,t,h,:] = sum_{j < G} dk_e[b,t,h*G+j,:]  (j ascending)
+__global__ void k_kda_gva(const float* __restrict__ dq_e, const float* __restrict__ dk_e, float* dq, float* dk,
+                          long long n, int G, int K, float scale) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / K, kk = i - row * K;  // row = (b*T + t)*H + h
+    const size_t src = ((size_t)row * G) * K + kk;
+    float sq = 0.f, sk = 0.f;
+    for (int j = 0; j < G; ++j) {
+      sq += dq_e[src + (size_t)j * K];
+      sk += dk_e[src + (size_t)j * K];
+    }
+    dq[i] = sq * scale;
+    dk[i] = sk;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ssd_status kda_dims(const ssd_kda_problem* p, KdaDims* d) {
+  if (!p) return SSD_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->seqlen < 1 || p->nheads < 1 || p->value_heads < 1 || p->key_dim < 1 || p->value_dim < 1)
+    return SSD_ERR_INVALID_ARG;
+  if (p->value_heads % p->nheads) return SSD_ERR_SHAPE;
+  if (p->key_dim > 32 * kRows || p->value_dim > kCols * kMaxWarps) return SSD_ERR_SHAPE;
+  const long long units = p->batch * p->value_heads;
+  if (units > 0x7fffffffll || p->seqlen > 0x7fffffffll || p->batch * p->seqlen * p->value_heads > (1ll << 40))
+    return SSD_ERR_SHAPE;
+  d->b = (int)p->batch;
+  d->T = (int)p->seqlen;
+  d->H = (int)p->nheads;
+  d->HV = (int)p->value_heads;
+  d->G = d->HV / d->H;
+  d->K = (int)p->key_dim;
+  d->V = (int)p->value_dim;
+  d->nw = (d->V + kCols - 1) / kCols;
+  d->nseg = (d->T + kSeg - 1) / kSeg;
+  return SSD_OK;
+}
+
+struct KdaWs {
+  float *ckpt, *scratch, *dq_e, *dk_e;
+};
+
+KdaWs kda_carve(const KdaDims& d, Carver& cv) {
+  KdaWs w;
+  const size_t units = (size_t)d.b * d.HV;
+  w.ckpt = cv.take<float>(units * d.nseg * d.K * d.V);
+  w.scratch = cv.take<float>(units * kSeg * ((size_t)d.nw * 32 * kRows * kCols + d.V));
+  w.dq_e = cv.take<float>((size_t)d.b * d.T * d.HV * d.K);
+  w.dk_e = cv.take<float>((size_t)d.b * d.T * d.HV * d.K);
+  return w;
+}
+
+ssd_status check_ptrs16(std::initializer_list<const void*> req, const void* opt) {
+  for (const void* p : req) {
+    if (!p) return SSD_ERR_INVALID_ARG;
+    if (!aligned16(p)) return SSD_ERR_ALIGNMENT;
+  }
+  if (opt && !aligned16(opt)) return SSD_ERR_ALIGNMENT;
+  return SSD_OK;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+ssd_status ssd_kda_workspace_size(const ssd_kda_problem* prob, int backward, size_t* bytes) {
+  if (!bytes) return SSD_ERR_INVALID_ARG;
+  KdaDims d;
+  ssd_status s = kda_dims(prob, &d);
+  if (s != SSD_OK) return s;
+  Carver cv(nullptr);
+  if (backward) kda_carve(d, cv);
+  *bytes = cv.off;
+  return SSD_OK;
+}
+
+ssd_status ssd_kda_forward(const ssd_kda_problem* prob, const float* q, const float* k, const float* v,
+                           const float* g, const float* beta, const float* s0, float scale, float* o, float* s_final,
+                           void* ws, size_t ws_bytes, void* cuda_stream) {
+  KdaDims d;
+  ssd_status s = kda_dims(prob, &d);
+  if (s != SSD_OK) return s;
+  s = check_ptrs16({q, k, v, g, beta, o, s_final, ws}, s0);
+  if (s != SSD_OK) return s;
+  Carver cv(nullptr);
+  if (ws_bytes < cv.off) return SSD_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  const KdaIn in{q, k, v, g, beta, scale};
+  const dim3 grid((unsigned)(d.b * d.HV), (unsigned)((d.nw + 1) / 2));
+  SSD_LAUNCH("k_kda_forward", st, k_kda_forward<false><<<grid, 64, 0, st>>>(in, d, s0, o, s_final, nullptr));
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_kda_backward(const ssd_kda_problem* prob, const float* dout, const float* ds_final, const float* q,
+                            const float* k, const float* v, const float* g, const float* beta, const float* s0,
+                            float scale, float* dq, float* dk, float* dv, float* dg, float* dbeta, float* ds0,
+                            void* ws, size_t ws_bytes, void* cuda_stream) {
+  KdaDims d;
+  ssd_status s = kda_dims(prob, &d);
+  if (s != SSD_OK) return s;
+  s = check_ptrs16({dout, ds_final, q, k, v, g, beta, dq, dk, dv, dg, dbeta, ds0, ws}, s0);
+  if (s != SSD_OK) return s;
+  Carver need(nullptr);
+  kda_carve(d, need);
+  if (ws_bytes < need.off) return SSD_ERR_WORKSPACE;
+  Carver cv(ws);
+  const KdaWs w = kda_carve(d, cv);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+  const KdaIn in{q, k, v, g, beta, scale};
+  const dim3 grid((unsigned)(d.b * d.HV), (unsigned)((d.nw + 1) / 2));
+  SSD_LAUNCH("k_kda_checkpoints", st, k_kda_forward<true><<<grid, 64, 0, st>>>(in, d, s0, nullptr, nullptr, w.ckpt));
+  const KdaBwdOut out{dout, ds_final, w.dq_e, w.dk_e, dv, dg, dbeta, ds0, w.ckpt, w.scratch};
+  const int smem = (int)(((size_t)2 * d.nw * 4 * 32 * kRows + 2 * d.nw) * sizeof(float));
+  if (cudaFuncSetAttribute(k_kda_backward, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  SSD_LAUNCH("k_kda_backward", st, k_kda_backward<<<(unsigned)(d.b * d.HV), 32 * d.nw, smem, st>>>(in, d, out));
+  const long long n = (long long)d.b * d.T * d.H * d.K;
+  const unsigned blocks = (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  SSD_LAUNCH("k_kda_gva", st, k_kda_gva<<<blocks, 256, 0, st>>>(w.dq_e, w.dk_e, dq, dk, n, d.G, d.K, scale));
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // extern "C"

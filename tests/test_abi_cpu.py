@@ -212,3 +212,32 @@ def test_checkpoint_validation(cuda_lib):
                fake, fake, fake, need_b - 1, None) == 5  # workspace too small
     assert bwd(ctypes.byref(tc), fake, fake, fake, fake, fake, fake, fake, 8, fake, need_k, fake, fake, fake, fake,
                fake, fake, None, need_b, None) == 1  # no workspace
+
+
+def test_kda_validation(cuda_lib):
+    """KDA sizes: the forward needs only the status word; the backward's workspace holds the checkpoints every
+    16 steps, the 16-step replay scratch and the per-value-head dq, dk; bad sizes are refused on the host."""
+    from selective_state_space_ssd_gb300.configs import KDA_CONFIGS
+    c = KDA_CONFIGS["kda_fp32"]
+    p = binding.kda_problem(c)
+    assert binding.ssd_kda_workspace_size(p, False) == 256
+    b, T, HV, K, V = c["batch"], c["seqlen"], c["value_heads"], c["key_dim"], c["value_dim"]
+    need = binding.ssd_kda_workspace_size(p, True)
+    floats = b * HV * (-(-T // 16)) * K * V + b * HV * 16 * ((V // 8) * 32 * 32 + V) + 2 * b * T * HV * K
+    assert floats * 4 <= need <= floats * 4 + 256 * 5
+    n = ctypes.c_size_t(0)
+    for over, code in [(dict(key_dim=129), 2), (dict(value_dim=129), 2), (dict(value_heads=6, nheads=4), 2),
+                       (dict(seqlen=0), 1), (dict(key_dim=0), 1)]:
+        bad = binding.kda_problem(dict(c, **over))
+        assert cuda_lib.ssd_kda_workspace_size(ctypes.byref(bad), 1, ctypes.byref(n)) == code, over
+    assert cuda_lib.ssd_kda_workspace_size(ctypes.byref(p), 1, None) == 1
+    fake = 1 << 20
+    # prob, q, k, v, g, beta, s0, scale, o, s_final, ws, ws_bytes, stream: NULL q, misaligned o, small workspace
+    assert cuda_lib.ssd_kda_forward(ctypes.byref(p), None, fake, fake, fake, fake, None, 0.1, fake, fake, fake, 256,
+                                    None) == 1
+    assert cuda_lib.ssd_kda_forward(ctypes.byref(p), fake, fake, fake, fake, fake, None, 0.1, fake + 4, fake, fake,
+                                    256, None) == 4
+    assert cuda_lib.ssd_kda_forward(ctypes.byref(p), fake, fake, fake, fake, fake, None, 0.1, fake, fake, fake, 255,
+                                    None) == 5
+    args = [fake] * 7 + [None]  # do, ds_final, q, k, v, g, beta, (s0)
+    assert cuda_lib.ssd_kda_backward(ctypes.byref(p), *args, 0.1, *([fake] * 6), fake, need - 1, None) == 5

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
-from selective_state_space_ssd_gb300.configs import CONFIGS  # noqa: E402
+from selective_state_space_ssd_gb300.configs import CONFIGS, KDA_CONFIGS  # noqa: E402
 
 CSRC = os.path.join(ROOT, "selective_state_space_ssd_gb300", "csrc")
 
@@ -55,9 +55,14 @@ def _launch_names():
 def test_every_launch_has_a_byte_count():
     names = _launch_names()
     assert {"k_tc_bwd_chunk", "k_tc_fwd_chunk", "k_tc_scan_pair_cb", "k_m1_backward", "k_chunk_bwd"} <= names
+    kda = {n for n in names if n.startswith("k_kda")}
+    assert kda == {"k_kda_forward", "k_kda_checkpoints", "k_kda_backward", "k_kda_gva"}
     for cfg in CONFIGS.values():
-        for n in names:
+        for n in names - kda:
             assert bench.kernel_bytes(n, cfg) is not None, (n, cfg["variant"])
+    for cfg in KDA_CONFIGS.values():
+        for n in kda:
+            assert bench.kernel_bytes(n, cfg) > 0, n
 
 
 @pytest.mark.parametrize("name", sorted(CONFIGS))
