@@ -30,7 +30,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from selective_state_space_ssd_gb300.configs import CONFIGS, HEADLINE, scaled, tokens  # noqa: E402
+from selective_state_space_ssd_gb300.configs import CONFIGS, HEADLINE, KDA_CONFIGS, scaled, tokens  # noqa: E402
 
 CKPT_EVERY = 8  # chunks between the checkpoints of the checkpointed variant
 METRIC = "SSD scan fwd+bwd tokens/s on 1 GB300 and % of roofline (HBM vs tensor peak)"
@@ -669,13 +669,188 @@ def run_once(args):
     return 0
 
 
+def run_kda(args):
+    """The KDA delta-rule workload: one step = ssd_kda_forward + ssd_kda_backward over the whole batch, timed like
+    the scan (median of the timed steps, L2 flushed before each, clocks sampled), with parity against the float64
+    oracle on one query / key head group and the oracle timed on that group.  Replicas only (no exchange)."""
+    import numpy as np
+    import torch
+    from oracle.kda import kda_backward, kda_forward
+    from selective_state_space_ssd_gb300 import binding
+    from selective_state_space_ssd_gb300 import inputs as synth
+
+    cfg = dict(KDA_CONFIGS[args.workload])
+    if args.batch is not None:
+        cfg["batch"] = args.batch
+    if args.seqlen is not None:
+        cfg["seqlen"] = args.seqlen
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        # the oracle on one query / key head group per step, extrapolated to the whole batch
+        G = cfg["value_heads"] // cfg["nheads"]
+        sub = dict(cfg, batch=1, nheads=1, value_heads=G)
+        f = synth.as_float64(synth.make_kda_inputs(sub, seed=0))
+        scale = synth.kda_scale(cfg)
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            kda_forward(f["q"], f["k"], f["v"], f["g"], f["beta"], f["s0"], scale)
+            kda_backward(f["do"], f["ds_final"], f["q"], f["k"], f["v"], f["g"], f["beta"], f["s0"], scale)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        groups = cfg["batch"] * cfg["nheads"]
+        med = statistics.median(times) * groups
+        value = cfg["batch"] * cfg["seqlen"] / med
+        line = {"impl": "reference", "metric": "KDA fwd+bwd tokens/s on 1 GB300", "value": value, "unit": "tokens/s",
+                "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * med,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded)", "config": {"workload": args.workload, **cfg},
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"one query / key head group of {groups}, T {cfg['seqlen']}; extrapolated"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    binding.load()
+    cpu = synth.make_kda_inputs(cfg, seed=0)
+    t = {k: v.to(dev) for k, v in cpu.items()}
+    prob = binding.kda_problem(cfg)
+    scale = synth.kda_scale(cfg)
+    nf, nb = binding.ssd_kda_workspace_size(prob, False), binding.ssd_kda_workspace_size(prob, True)
+    wsf = torch.empty(max(nf, 256), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    out = {"o": torch.empty_like(t["v"]), "s_final": torch.empty_like(t["s0"]), "dq": torch.empty_like(t["q"]),
+           "dk": torch.empty_like(t["k"]), "dv": torch.empty_like(t["v"]), "dg": torch.empty_like(t["g"]),
+           "dbeta": torch.empty_like(t["beta"]), "ds0": torch.empty_like(t["s0"])}
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(i, o):
+        binding.ssd_kda_forward(prob, i["q"], i["k"], i["v"], i["g"], i["beta"], i["s0"], scale, o["o"], o["s_final"],
+                                wsf, nf, stream)
+        binding.ssd_kda_backward(prob, i["do"], i["ds_final"], i["q"], i["k"], i["v"], i["g"], i["beta"], i["s0"],
+                                 scale, o["dq"], o["dk"], o["dv"], o["dg"], o["dbeta"], o["ds0"], wsb, nb, stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    steps = min(args.steps, 20)  # a step is milliseconds long: 20 timed steps are plenty
+    for _ in range(args.warmup):
+        step(t, out)
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(local_rank) as clk:
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            step(t, out)
+            b.record(stream)
+        barrier()
+    med = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in ev), world, dev)
+    binding.ssd_profile_start(1 << 12)
+    for _ in range(3):
+        flush.zero_()
+        step(t, out)
+    barrier()
+    per = {}
+    for rec in binding.ssd_profile_stop(1 << 12):
+        n, ms = per.get(rec[0], (0, 0.0))
+        per[rec[0]] = (n + 1, ms + rec[1])
+    # end to end: inputs in from pinned host memory and all outputs back, every step
+    pin = {k: v.pin_memory() for k, v in cpu.items()}
+    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in out.values())
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(3):
+        for k, v in pin.items():
+            t[k].copy_(v, non_blocking=True)
+        step(t, out)
+        for k, v in out.items():
+            host[k].copy_(v, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / 3, world, dev)
+    # parity: one query / key head group against the oracle
+    G = cfg["value_heads"] // cfg["nheads"]
+    bb, h = cfg["batch"] - 1, cfg["nheads"] // 2
+    vs = slice(h * G, (h + 1) * G)
+    sub = {"q": cpu["q"][bb:bb + 1, :, h:h + 1], "k": cpu["k"][bb:bb + 1, :, h:h + 1]}
+    for n in ("v", "g", "beta", "do"):
+        sub[n] = cpu[n][bb:bb + 1, :, vs]
+    for n in ("s0", "ds_final"):
+        sub[n] = cpu[n][bb:bb + 1, vs]
+    f = synth.as_float64(sub)
+    t0 = time.perf_counter()
+    ref = kda_forward(f["q"], f["k"], f["v"], f["g"], f["beta"], f["s0"], scale)
+    ref.update(kda_backward(f["do"], f["ds_final"], f["q"], f["k"], f["v"], f["g"], f["beta"], f["s0"], scale))
+    oracle_s = time.perf_counter() - t0
+    errs = {}
+    for k in ("o", "s_final", "dq", "dk", "dv", "dg", "dbeta", "ds0"):
+        x = out[k]
+        x = (x[bb:bb + 1, :, h:h + 1] if k in ("dq", "dk") else x[bb:bb + 1, vs] if k in ("s_final", "ds0")
+             else x[bb:bb + 1, :, vs])
+        r = ref[k]
+        errs[k] = float(np.max(np.abs(x.double().cpu().numpy() - r)) / max(np.max(np.abs(r)), 1e-30))
+    tok = cfg["batch"] * cfg["seqlen"]
+    pk = peaks()
+    fb, bwb = kda_algorithmic_bytes(cfg)
+    dom = max(per.items(), key=lambda kv: kv[1][1])[0]
+    dom_ms = per[dom][1] / per[dom][0]
+    dom_bytes = (fb if dom == "k_kda_forward" else bwb)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    line = {"metric": "KDA fwd+bwd tokens/s on 1 GB300", "value": world * tok / (med / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": med,
+            "ms_per_step_stat": "median of the timed steps", "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+            "config": {"workload": f"{args.workload}: b={cfg['batch']} T={cfg['seqlen']} H={cfg['nheads']} "
+                                   f"HV={cfg['value_heads']} K={cfg['key_dim']} V={cfg['value_dim']}",
+                       "global_batch": cfg["batch"] * world, "seq_len": cfg["seqlen"],
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "flushed before every timed step (516 MB write, outside the timed interval)"},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                         "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                         "note": "a sequential recurrence over T with b*HV independent chains: bound by the "
+                                 "latency of its per-step chain, far from the HBM roof"},
+            "per_kernel_ms": {k: {"launches": v[0], "total_ms": v[1]} for k, v in sorted(per.items())},
+            "gpu_launches": int(round(sum(v[0] for v in per.values()) / 3 * steps)),
+            "clocks": clk.summary(),
+            "e2e": {"value": world * tok / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "parity": dict(errs, metric="max|gpu - oracle| / max|oracle| per output, one query / key head group",
+                           tolerance=1e-4, ok=max(errs.values()) <= 1e-4)}
+    if rank == 0 and world == 1:
+        groups = cfg["batch"] * cfg["nheads"]
+        line["cpu_baseline"] = {"value": tok / (oracle_s * groups), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"one query / key head group of {groups} (T {cfg['seqlen']}), "
+                                          "forward + backward once; tokens/s extrapolated to the batch"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(CONFIGS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(CONFIGS) + sorted(KDA_CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for ncu captures; not a bench line)")
@@ -689,6 +864,8 @@ def main():
         return run_once(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in KDA_CONFIGS:
+        return run_kda(args)
     cfg = CONFIGS[args.workload]
     if args.batch is not None:
         cfg = scaled(cfg, batch=args.batch)
