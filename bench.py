@@ -106,13 +106,15 @@ def kda_kernel_bytes(name, cfg):
     ins = 2 * t["q"] + t["v"] + t["g"] + t["beta"] + t["s"]
     ckpt = b * HV * (-(-T // 16)) * K * V * 4
     per_head = b * T * HV * K * 4  # dq or dk per value head
+    nsplit = -(-(-(-cfg["value_dim"] // 8)) // 4)
+    rows = b * T * HV * nsplit * (4 * K + 1) * 4  # the backward CTAs' per-step row sums
     table = {
         "k_kda_forward": ins + t["v"] + t["s"],
         "k_kda_checkpoints": ins + ckpt,
         # the replay and the reverse pass read the step inputs twice; do, ds_final and the checkpoints in;
-        # dv, dg, dbeta, ds0 and the per-value-head dq, dk out (the replay scratch stays in L2)
-        "k_kda_backward": 2 * (ins - t["s"]) + t["v"] + t["s"] + ckpt + t["v"] + t["g"] + t["beta"] + t["s"]
-                          + 2 * per_head,
+        # dv, ds0 and the CTAs' row sums out (the replay scratch stays in L2)
+        "k_kda_backward": 2 * (ins - t["s"]) + t["v"] + t["s"] + ckpt + t["v"] + t["s"] + rows,
+        "k_kda_rows": rows + t["beta"] + 2 * per_head + t["g"] + t["beta"],
         "k_kda_gva": 2 * per_head + 2 * t["q"],
     }
     return table.get(name)

@@ -6,19 +6,25 @@
 // its K x 8 slice of S in registers: lane l holds rows l, l + 32, l + 64,
 // l + 96.  Column work (p = k^T S_dec, o = q^T S, dr) reduces over the key
 // rows of a column: a warp reduction.  Row work of the backward (dq, da, dk,
-// dg) reduces over the value columns: each warp writes its 8-column partial
-// sums to shared memory, and after one barrier per step the CTA's first K
-// threads add the partials of every warp, in warp order.
+// dg) reduces over the value columns: each warp's 8-column partial sums are
+// added over the warps of its CTA in warp order (shared memory, one barrier
+// per step), then over the CTAs of the (b, hv) in CTA order (a small kernel).
+// Every warp loads the next step's inputs while it computes the current one,
+// so their global latency is off the recurrence's critical path.
 //
 //   forward   k_kda_forward<false>: o and s_final, every warp on its own.
 //   backward  1. k_kda_forward<true> replays the forward from the leaf inputs
-//                and keeps the state entering every 16th step (checkpoints);
-//             2. k_kda_backward, one CTA per (b, hv) with all its column
-//                warps, walks the 16-step segments from the last: it replays
+//                and keeps the state entering every 16th step (checkpoints,
+//                stored lane-major so every store is one coalesced line);
+//             2. k_kda_backward, CTAs of up to four column warps of one
+//                (b, hv), walks the 16-step segments from the last: it replays
 //                the segment from its checkpoint (S_dec and r of every step to
-//                a per-CTA scratch), then runs steps 1-6 backwards through it,
-//                carrying dS_acc in registers across segments;
-//             3. k_kda_gva adds the per-value-head dq, dk onto their query /
+//                a per-CTA scratch that stays in L2), then runs steps 1-6
+//                backwards through it, carrying dS_acc in registers across
+//                segments, and writes the CTA's row sums per step;
+//             3. k_kda_rows adds the CTAs' row sums in CTA order (dq, dk, dg,
+//                dbeta per value head);
+//             4. k_kda_gva adds the per-value-head dq, dk onto their query /
 //                key head in a fixed order (the page's view + sum) and scales
 //                dq.
 #include <math.h>
@@ -32,22 +38,26 @@
 namespace ssd {
 namespace {
 
-constexpr int kRows = 4;    // key rows per lane: K <= 128
-constexpr int kCols = 8;    // value columns per warp: V <= 128 in at most 16 warps
-constexpr int kSeg = 16;    // steps per checkpoint segment
-constexpr int kMaxWarps = 16;
+constexpr int kRows = 4;       // key rows per lane: K <= 128
+constexpr int kCols = 8;       // value columns per warp: V <= 128 in at most 16 warps
+constexpr int kSeg = 16;       // steps per checkpoint segment
+constexpr int kMaxWarps = 16;  // column warps of a (b, hv)
+constexpr int kCtaWarps = 4;   // column warps of a backward CTA
+constexpr int kSlice = 32 * kRows * kCols;  // floats of one warp's state slice
 
 struct KdaDims {
   int b, T, H, HV, G, K, V;
-  int nw;    // column warps per (b, hv): ceil(V / 8)
-  int nseg;  // checkpoint segments: ceil(T / 16)
+  int nw;     // column warps per (b, hv): ceil(V / 8)
+  int nseg;   // checkpoint segments: ceil(T / 16)
+  int wpc;    // column warps per backward CTA: min(nw, 4)
+  int nsplit; // backward CTAs per (b, hv): ceil(nw / wpc)
 };
 
 struct KdaIn {
-  const float* q;  // [b,T,H,K]
-  const float* k;  // [b,T,H,K]
-  const float* v;  // [b,T,HV,V]
-  const float* g;  // [b,T,HV,K]
+  const float* q;     // [b,T,H,K]
+  const float* k;     // [b,T,H,K]
+  const float* v;     // [b,T,HV,V]
+  const float* g;     // [b,T,HV,K]
   const float* beta;  // [b,T,HV]
   float scale;
 };
@@ -58,7 +68,9 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// The per-step inputs of one warp: its rows of q (scaled), k and exp(g), beta, and its columns of v.
+// The per-step inputs of one warp: its rows of q, k, g, beta, and its columns of v, as loaded (load_step), then
+// finished (finish_step: q scaled, g -> exp(g)).  Rows and columns outside K, V read 0 (exp(0) = 1 keeps those
+// state entries at 0).
 struct StepIn {
   float q[kRows], k[kRows], eg[kRows], v[kCols], beta;
 };
@@ -71,13 +83,21 @@ __device__ __forceinline__ void load_step(const KdaIn& in, const KdaDims& d, int
   for (int i = 0; i < kRows; ++i) {
     const int r = lane + 32 * i;
     const bool ok = r < d.K;
-    s.q[i] = ok ? in.q[qk * d.K + r] * in.scale : 0.f;
+    s.q[i] = ok ? in.q[qk * d.K + r] : 0.f;
     s.k[i] = ok ? in.k[qk * d.K + r] : 0.f;
-    s.eg[i] = ok ? __expf(in.g[gv * d.K + r]) : 1.f;
+    s.eg[i] = ok ? in.g[gv * d.K + r] : 0.f;
   }
 #pragma unroll
   for (int j = 0; j < kCols; ++j) s.v[j] = col0 + j < d.V ? in.v[gv * d.V + col0 + j] : 0.f;
   s.beta = in.beta[gv];
+}
+
+__device__ __forceinline__ void finish_step(StepIn& s, float scale) {
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    s.q[i] *= scale;
+    s.eg[i] = __expf(s.eg[i]);
+  }
 }
 
 // F1-F5 on this warp's slice: S <- S_dec + beta k (x) (v - k^T S_dec); returns r (all lanes).
@@ -101,8 +121,13 @@ __device__ __forceinline__ void delta_step(float (&S)[kRows][kCols], const StepI
   }
 }
 
+// Checkpoint slot of warp w's slice: [unit][seg][w][i * 8 + j][lane] (lane-major: one coalesced line per store)
+__device__ __forceinline__ size_t ckpt_slot(const KdaDims& d, int unit, int seg, int w) {
+  return (((size_t)unit * d.nseg + seg) * d.nw + w) * kSlice;
+}
+
 // Forward: one warp per 8 columns of one (b, hv); grid (b * HV, ceil(nw / 2)), two warps per CTA.
-// kCkpt: the backward's replay, which writes only the state entering every 16th step (ckpt [b*HV][nseg][K][V]);
+// kCkpt: the backward's replay, which writes only the state entering every 16th step (checkpoints);
 // otherwise o [b,T,HV,V] and s_final [b,HV,K,V].
 template <bool kCkpt>
 __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const float* __restrict__ s0, float* o,
@@ -121,19 +146,19 @@ __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const f
       const int r = lane + 32 * i, c = col0 + j;
       S[i][j] = s0 && r < d.K && c < d.V ? s0[sbase + (size_t)r * d.V + c] : 0.f;
     }
+  StepIn nx;
+  load_step(in, d, b, hv, 0, lane, col0, nx);
   for (int t = 0; t < d.T; ++t) {
     if (kCkpt && t % kSeg == 0) {
-      float* dst = ckpt + ((size_t)unit * d.nseg + t / kSeg) * d.K * d.V;
+      float* dst = ckpt + ckpt_slot(d, unit, t / kSeg, w);
 #pragma unroll
       for (int i = 0; i < kRows; ++i)
 #pragma unroll
-        for (int j = 0; j < kCols; ++j) {
-          const int r = lane + 32 * i, c = col0 + j;
-          if (r < d.K && c < d.V) dst[(size_t)r * d.V + c] = S[i][j];
-        }
+        for (int j = 0; j < kCols; ++j) dst[(i * kCols + j) * 32 + lane] = S[i][j];
     }
-    StepIn s;
-    load_step(in, d, b, hv, t, lane, col0, s);
+    StepIn s = nx;
+    if (t + 1 < d.T) load_step(in, d, b, hv, t + 1, lane, col0, nx);
+    finish_step(s, in.scale);
     float r[kCols];
     delta_step(S, s, r);
     if (!kCkpt) {
@@ -163,59 +188,57 @@ __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const f
 struct KdaBwdOut {
   const float* dout;      // do [b,T,HV,V]
   const float* ds_final;  // [b,HV,K,V]
-  float* dq_e;            // [b,T,HV,K]: per value head, w.r.t. the scaled q
-  float* dk_e;            // [b,T,HV,K]
+  float* part;            // [b,T,HV][nsplit][dq, da, dk_r, dg rows (4 K), then dbeta]: row sums of each CTA
   float* dv;              // [b,T,HV,V]
-  float* dg;              // [b,T,HV,K]
-  float* dbeta;           // [b,T,HV]
   float* ds0;             // [b,HV,K,V]
-  const float* ckpt;      // [b*HV][nseg][K][V]
-  float* scratch;         // per CTA: kSeg steps x (nw warps x 32 values x 32 lanes of S_dec, then V values of r)
+  const float* ckpt;      // checkpoints (ckpt_slot)
+  float* scratch;         // per CTA: kSeg steps x (wpc slices of S_dec, then 8 wpc values of r)
 };
 
-// Backward: one CTA per (b, hv), d.nw warps (32 * nw threads).  Dynamic shared memory: the per-step row
-// partials of the column warps, double-buffered, [buf][warp][dq, da, dk_r, dg][row 0..127], then the dbeta
-// partial of each warp, [buf][warp].
-__global__ void __launch_bounds__(32 * kMaxWarps) k_kda_backward(KdaIn in, KdaDims d, KdaBwdOut out) {
-  extern __shared__ float kda_smem[];
+// Backward: CTA (unit, split) runs column warps split * wpc .. + wpc - 1 of (b, hv) = unit (the warps past nw
+// only join the barriers).  Static shared memory: the per-step row partials of its warps, double-buffered,
+// [buf][warp][dq, da, dk_r, dg][row 0..127], and their dbeta partials [buf][warp].
+__global__ void __launch_bounds__(32 * kCtaWarps) k_kda_backward(KdaIn in, KdaDims d, KdaBwdOut out) {
   constexpr int kPartRow = 32 * kRows;
-  auto part = [&](int buf, int w, int m) { return kda_smem + ((size_t)(buf * d.nw + w) * 4 + m) * kPartRow; };
-  float* dbp = kda_smem + (size_t)2 * d.nw * 4 * kPartRow;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int unit = blockIdx.x, b = unit / d.HV, hv = unit - b * d.HV;
+  __shared__ float part[2][kCtaWarps][4][kPartRow];
+  __shared__ float dbp[2][kCtaWarps];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int unit = blockIdx.x, split = blockIdx.y, b = unit / d.HV, hv = unit - b * d.HV;
+  const int w = split * d.wpc + wl;  // the warp's column block of the (b, hv)
+  const bool live = wl < d.wpc && w < d.nw;
+  const int nlive = min(d.wpc, d.nw - split * d.wpc);
   const int col0 = kCols * w;
   const size_t sbase = (size_t)unit * d.K * d.V;
-  const size_t step_floats = (size_t)d.nw * 32 * kRows * kCols + d.V;  // one step of the scratch
-  float* scr = out.scratch + (size_t)unit * kSeg * step_floats;
-  // this lane's S_dec of row slot i, column j, in scratch step st: lane-contiguous, so a warp's access is coalesced
-  auto sd_at = [&](float* st, int i, int j) -> float& {
-    return st[(size_t)w * 32 * kRows * kCols + (i * kCols + j) * 32 + lane];
-  };
+  const size_t step_floats = (size_t)d.wpc * kSlice + kCols * d.wpc;  // one step of the scratch
+  float* scr = out.scratch + ((size_t)unit * d.nsplit + split) * kSeg * step_floats;
+  auto sd_at = [&](float* st, int i, int j) -> float& { return st[(size_t)wl * kSlice + (i * kCols + j) * 32 + lane]; };
+  auto r_at = [&](float* st, int j) -> float& { return st[(size_t)d.wpc * kSlice + kCols * wl + j]; };
+  const int rstride = 4 * d.K + 1;
   float dS[kRows][kCols];  // dS_acc, seeded with ds_final
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
 #pragma unroll
     for (int j = 0; j < kCols; ++j) {
       const int r = lane + 32 * i, c = col0 + j;
-      dS[i][j] = r < d.K && c < d.V ? out.ds_final[sbase + (size_t)r * d.V + c] : 0.f;
+      dS[i][j] = live && r < d.K && c < d.V ? out.ds_final[sbase + (size_t)r * d.V + c] : 0.f;
     }
   int step = 0;  // steps done, for the double buffer
   for (int sg = d.nseg - 1; sg >= 0; --sg) {
     const int t0 = sg * kSeg, t1 = min(d.T, t0 + kSeg);
     // replay the segment from its checkpoint: S_dec and r of every step to the scratch
-    {
+    if (live) {
       float S[kRows][kCols];
-      const float* src = out.ckpt + ((size_t)unit * d.nseg + sg) * d.K * d.V;
+      const float* src = out.ckpt + ckpt_slot(d, unit, sg, w);
 #pragma unroll
       for (int i = 0; i < kRows; ++i)
 #pragma unroll
-        for (int j = 0; j < kCols; ++j) {
-          const int r = lane + 32 * i, c = col0 + j;
-          S[i][j] = r < d.K && c < d.V ? src[(size_t)r * d.V + c] : 0.f;
-        }
+        for (int j = 0; j < kCols; ++j) S[i][j] = src[(i * kCols + j) * 32 + lane];
+      StepIn nx;
+      load_step(in, d, b, hv, t0, lane, col0, nx);
       for (int t = t0; t < t1; ++t) {
-        StepIn s;
-        load_step(in, d, b, hv, t, lane, col0, s);
+        StepIn s = nx;
+        if (t + 1 < t1) load_step(in, d, b, hv, t + 1, lane, col0, nx);
+        finish_step(s, in.scale);
         float r[kCols];
         float* st = scr + (size_t)(t - t0) * step_floats;
 #pragma unroll
@@ -227,102 +250,139 @@ __global__ void __launch_bounds__(32 * kMaxWarps) k_kda_backward(KdaIn in, KdaDi
 #pragma unroll
         for (int j = 1; j < kCols; ++j)
           if (lane == j) rv = r[j];
-        if (lane < kCols && col0 + lane < d.V) st[(size_t)d.nw * 32 * kRows * kCols + col0 + lane] = rv;
+        if (lane < kCols) r_at(st, lane) = rv;
       }
     }
     __syncwarp();  // the r values of the warp's columns, written by lanes 0-7, are read by every lane
     // steps 1-6 backwards through the segment
+    StepIn nx;
+    if (live) load_step(in, d, b, hv, t1 - 1, lane, col0, nx);
     for (int t = t1 - 1; t >= t0; --t, ++step) {
-      StepIn s;
-      load_step(in, d, b, hv, t, lane, col0, s);
-      float* st = scr + (size_t)(t - t0) * step_floats;
-      const size_t gv = ((size_t)b * d.T + t) * d.HV + hv;
-      float r[kCols], dov[kCols], u[kCols];
-#pragma unroll
-      for (int j = 0; j < kCols; ++j) {
-        const bool ok = col0 + j < d.V;
-        r[j] = ok ? st[(size_t)d.nw * 32 * kRows * kCols + col0 + j] : 0.f;
-        dov[j] = ok ? out.dout[gv * d.V + col0 + j] : 0.f;
-      }
       const int pb = step & 1;
-      // step 1: dS_acc += q (x) do;  dq = S_t do with S_t = S_dec + beta k (x) r;  step 2: da = dS_acc r
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        const float a = s.beta * s.k[i];
-        float xq = 0.f, xa = 0.f;
-#pragma unroll
-        for (int j = 0; j < kCols; ++j) {
-          dS[i][j] = fmaf(s.q[i], dov[j], dS[i][j]);
-          xq = fmaf(dov[j], fmaf(a, r[j], sd_at(st, i, j)), xq);
-          xa = fmaf(r[j], dS[i][j], xa);
-        }
-        part(pb, w, 0)[lane + 32 * i] = xq;
-        part(pb, w, 1)[lane + 32 * i] = xa;
-      }
-      // step 2: dr = a^T dS_acc = beta u with u = k^T dS_acc per column (a warp reduction);
-      // step 3: dbeta = sum_k k da = sum_v r u
-      float dbw = 0.f;
-#pragma unroll
-      for (int j = 0; j < kCols; ++j) {
-        float x = 0.f;
-#pragma unroll
-        for (int i = 0; i < kRows; ++i) x = fmaf(s.k[i], dS[i][j], x);
-        u[j] = warp_sum(x);
-        dbw = fmaf(r[j], u[j], dbw);
-      }
-      // step 4: dv = dr,  dk_r = -S_dec dr;  step 5: dS_dec = dS_acc - k (x) dr (both paths),
-      // dg = rowsum(S_dec o dS_dec),  dS_{t-1} = exp(g) o dS_dec
-      float dvo = 0.f;
-#pragma unroll
-      for (int j = 0; j < kCols; ++j)
-        if (lane == j) dvo = s.beta * u[j];
-      if (lane < kCols && col0 + lane < d.V) out.dv[gv * d.V + col0 + lane] = dvo;
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        float xk = 0.f, xg = 0.f;
+      const size_t gv = ((size_t)b * d.T + t) * d.HV + hv;
+      StepIn s = nx;
+      if (live) {
+        if (t > t0) load_step(in, d, b, hv, t - 1, lane, col0, nx);
+        finish_step(s, in.scale);
+        float* st = scr + (size_t)(t - t0) * step_floats;
+        float r[kCols], dov[kCols], u[kCols];
 #pragma unroll
         for (int j = 0; j < kCols; ++j) {
-          const float dr = s.beta * u[j];
-          const float sdv = sd_at(st, i, j);
-          xk = fmaf(-sdv, dr, xk);
-          const float tot = fmaf(-s.k[i], dr, dS[i][j]);
-          xg = fmaf(sdv, tot, xg);
-          dS[i][j] = s.eg[i] * tot;
+          r[j] = r_at(st, j);
+          dov[j] = col0 + j < d.V ? out.dout[gv * d.V + col0 + j] : 0.f;
         }
-        part(pb, w, 2)[lane + 32 * i] = xk;
-        part(pb, w, 3)[lane + 32 * i] = xg;
+        // step 1: dS_acc += q (x) do;  dq = S_t do with S_t = S_dec + beta k (x) r;  step 2: da = dS_acc r
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          const float a = s.beta * s.k[i];
+          float xq = 0.f, xa = 0.f;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) {
+            dS[i][j] = fmaf(s.q[i], dov[j], dS[i][j]);
+            xq = fmaf(dov[j], fmaf(a, r[j], sd_at(st, i, j)), xq);
+            xa = fmaf(r[j], dS[i][j], xa);
+          }
+          part[pb][wl][0][lane + 32 * i] = xq;
+          part[pb][wl][1][lane + 32 * i] = xa;
+        }
+        // step 2: dr = a^T dS_acc = beta u with u = k^T dS_acc per column (a warp reduction);
+        // step 3: dbeta = sum_k k da = sum_v r u
+        float dbw = 0.f;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          float x = 0.f;
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) x = fmaf(s.k[i], dS[i][j], x);
+          u[j] = warp_sum(x);
+          dbw = fmaf(r[j], u[j], dbw);
+        }
+        // step 4: dv = dr,  dk_r = -S_dec dr;  step 5: dS_dec = dS_acc - k (x) dr (both paths),
+        // dg = rowsum(S_dec o dS_dec),  dS_{t-1} = exp(g) o dS_dec
+        float dvo = 0.f;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j)
+          if (lane == j) dvo = s.beta * u[j];
+        if (lane < kCols && col0 + lane < d.V) out.dv[gv * d.V + col0 + lane] = dvo;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          float xk = 0.f, xg = 0.f;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) {
+            const float dr = s.beta * u[j];
+            const float sdv = sd_at(st, i, j);
+            xk = fmaf(-sdv, dr, xk);
+            const float tot = fmaf(-s.k[i], dr, dS[i][j]);
+            xg = fmaf(sdv, tot, xg);
+            dS[i][j] = s.eg[i] * tot;
+          }
+          part[pb][wl][2][lane + 32 * i] = xk;
+          part[pb][wl][3][lane + 32 * i] = xg;
+        }
+        if (lane == 0) dbp[pb][wl] = dbw;
       }
-      if (lane == 0) dbp[pb * d.nw + w] = dbw;
       __syncthreads();
-      // the rows: partials of every column warp added in warp order
+      // this CTA's row sums: its live warps added in warp order
+      float* dst = out.part + (gv * d.nsplit + split) * rstride;
       for (int row = threadIdx.x; row < d.K; row += blockDim.x) {
         float q_ = 0.f, a_ = 0.f, k_ = 0.f, g_ = 0.f;
-        for (int ww = 0; ww < d.nw; ++ww) {
-          q_ += part(pb, ww, 0)[row];
-          a_ += part(pb, ww, 1)[row];
-          k_ += part(pb, ww, 2)[row];
-          g_ += part(pb, ww, 3)[row];
+        for (int ww = 0; ww < nlive; ++ww) {
+          q_ += part[pb][ww][0][row];
+          a_ += part[pb][ww][1][row];
+          k_ += part[pb][ww][2][row];
+          g_ += part[pb][ww][3][row];
         }
-        const size_t gk = gv * d.K + row;
-        out.dq_e[gk] = q_;
-        out.dk_e[gk] = fmaf(s.beta, a_, k_);  // step 6: dk = beta da + dk_r
-        out.dg[gk] = g_;
+        dst[row] = q_;
+        dst[d.K + row] = a_;
+        dst[2 * d.K + row] = k_;
+        dst[3 * d.K + row] = g_;
       }
       if (threadIdx.x == 0) {
         float x = 0.f;
-        for (int ww = 0; ww < d.nw; ++ww) x += dbp[pb * d.nw + ww];
-        out.dbeta[gv] = x;
+        for (int ww = 0; ww < nlive; ++ww) x += dbp[pb][ww];
+        dst[4 * d.K] = x;
       }
     }
     __syncwarp();  // this segment's scratch has been read before the next replay overwrites it
   }
+  if (live) {
 #pragma unroll
-  for (int i = 0; i < kRows; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
-    for (int j = 0; j < kCols; ++j) {
-      const int r = lane + 32 * i, c = col0 + j;
-      if (r < d.K && c < d.V) out.ds0[sbase + (size_t)r * d.V + c] = dS[i][j];
+      for (int j = 0; j < kCols; ++j) {
+        const int r = lane + 32 * i, c = col0 + j;
+        if (r < d.K && c < d.V) out.ds0[sbase + (size_t)r * d.V + c] = dS[i][j];
+      }
+  }
+}
+
+// Per (b, t, hv): the CTAs' row sums added in CTA order; dk = beta da + dk_r (step 6), dq per value head (w.r.t.
+// the scaled q), dg and dbeta.  One block of 128 threads per (b, t, hv), thread = key row.
+__global__ void __launch_bounds__(128) k_kda_rows(const float* __restrict__ part, const float* __restrict__ beta,
+                                                  float* dq_e, float* dk_e, float* dg, float* dbeta, long long n,
+                                                  int K, int nsplit) {
+  const int rstride = 4 * K + 1;
+  for (long long gv = blockIdx.x; gv < n; gv += gridDim.x) {
+    const float* p = part + (size_t)gv * nsplit * rstride;
+    const float bt = beta[gv];
+    for (int row = threadIdx.x; row < K; row += blockDim.x) {
+      float q_ = 0.f, a_ = 0.f, k_ = 0.f, g_ = 0.f;
+      for (int s = 0; s < nsplit; ++s) {
+        const float* ps = p + (size_t)s * rstride;
+        q_ += ps[row];
+        a_ += ps[K + row];
+        k_ += ps[2 * K + row];
+        g_ += ps[3 * K + row];
+      }
+      dq_e[(size_t)gv * K + row] = q_;
+      dk_e[(size_t)gv * K + row] = fmaf(bt, a_, k_);
+      dg[(size_t)gv * K + row] = g_;
     }
+    if (threadIdx.x == 0) {
+      float x = 0.f;
+      for (int s = 0; s < nsplit; ++s) x += p[(size_t)s * rstride + 4 * K];
+      dbeta[gv] = x;
+    }
+  }
 }
 
 // dq[b,t,h,:] = scale * sum_{j < G} dq_e[b,t,h*G+j,:],  dk[b,t,h,:] = sum_{j < G} dk_e[b,t,h*G+j,:]  (j ascending)
@@ -361,20 +421,25 @@ ssd_status kda_dims(const ssd_kda_problem* p, KdaDims* d) {
   d->V = (int)p->value_dim;
   d->nw = (d->V + kCols - 1) / kCols;
   d->nseg = (d->T + kSeg - 1) / kSeg;
+  d->wpc = d->nw < kCtaWarps ? d->nw : kCtaWarps;
+  d->nsplit = (d->nw + d->wpc - 1) / d->wpc;
   return SSD_OK;
 }
 
 struct KdaWs {
-  float *ckpt, *scratch, *dq_e, *dk_e;
+  float *ckpt, *scratch, *part, *dq_e, *dk_e;
 };
 
+// Backward workspace: checkpoints (units x nseg x nw slices), the replay scratch of every backward CTA (16 steps
+// of wpc slices and 8 wpc values of r), the CTAs' per-step row sums, and the per-value-head dq, dk.
 KdaWs kda_carve(const KdaDims& d, Carver& cv) {
   KdaWs w;
-  const size_t units = (size_t)d.b * d.HV;
-  w.ckpt = cv.take<float>(units * d.nseg * d.K * d.V);
-  w.scratch = cv.take<float>(units * kSeg * ((size_t)d.nw * 32 * kRows * kCols + d.V));
-  w.dq_e = cv.take<float>((size_t)d.b * d.T * d.HV * d.K);
-  w.dk_e = cv.take<float>((size_t)d.b * d.T * d.HV * d.K);
+  const size_t units = (size_t)d.b * d.HV, rows = (size_t)d.b * d.T * d.HV;
+  w.ckpt = cv.take<float>(units * d.nseg * d.nw * kSlice);
+  w.scratch = cv.take<float>(units * d.nsplit * kSeg * ((size_t)d.wpc * kSlice + kCols * d.wpc));
+  w.part = cv.take<float>(rows * d.nsplit * (4 * (size_t)d.K + 1));
+  w.dq_e = cv.take<float>(rows * d.K);
+  w.dk_e = cv.take<float>(rows * d.K);
   return w;
 }
 
@@ -442,11 +507,13 @@ ssd_status ssd_kda_backward(const ssd_kda_problem* prob, const float* dout, cons
   const KdaIn in{q, k, v, g, beta, scale};
   const dim3 grid((unsigned)(d.b * d.HV), (unsigned)((d.nw + 1) / 2));
   SSD_LAUNCH("k_kda_checkpoints", st, k_kda_forward<true><<<grid, 64, 0, st>>>(in, d, s0, nullptr, nullptr, w.ckpt));
-  const KdaBwdOut out{dout, ds_final, w.dq_e, w.dk_e, dv, dg, dbeta, ds0, w.ckpt, w.scratch};
-  const int smem = (int)(((size_t)2 * d.nw * 4 * 32 * kRows + 2 * d.nw) * sizeof(float));
-  if (cudaFuncSetAttribute(k_kda_backward, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return SSD_ERR_CUDA;
-  SSD_LAUNCH("k_kda_backward", st, k_kda_backward<<<(unsigned)(d.b * d.HV), 32 * d.nw, smem, st>>>(in, d, out));
+  const KdaBwdOut out{dout, ds_final, w.part, dv, ds0, w.ckpt, w.scratch};
+  SSD_LAUNCH("k_kda_backward", st,
+             k_kda_backward<<<dim3((unsigned)(d.b * d.HV), (unsigned)d.nsplit), 32 * kCtaWarps, 0, st>>>(in, d, out));
+  const long long rows = (long long)d.b * d.T * d.HV;
+  const unsigned rblocks = (unsigned)(rows < 65535 * 8 ? rows : 65535 * 8);
+  SSD_LAUNCH("k_kda_rows", st,
+             k_kda_rows<<<rblocks, 128, 0, st>>>(w.part, beta, w.dq_e, w.dk_e, dg, dbeta, rows, d.K, d.nsplit));
   const long long n = (long long)d.b * d.T * d.H * d.K;
   const unsigned blocks = (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
   SSD_LAUNCH("k_kda_gva", st, k_kda_gva<<<blocks, 256, 0, st>>>(w.dq_e, w.dk_e, dq, dk, n, d.G, d.K, scale));

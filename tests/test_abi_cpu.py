@@ -223,8 +223,13 @@ def test_kda_validation(cuda_lib):
     assert binding.ssd_kda_workspace_size(p, False) == 256
     b, T, HV, K, V = c["batch"], c["seqlen"], c["value_heads"], c["key_dim"], c["value_dim"]
     need = binding.ssd_kda_workspace_size(p, True)
-    floats = b * HV * (-(-T // 16)) * K * V + b * HV * 16 * ((V // 8) * 32 * 32 + V) + 2 * b * T * HV * K
-    assert floats * 4 <= need <= floats * 4 + 256 * 5
+    nw = V // 8          # column warps of 8 value columns
+    nsplit = nw // 4     # backward CTAs of four column warps
+    floats = (b * HV * (-(-T // 16)) * nw * 1024           # lane-major checkpoints of every warp slice
+              + b * HV * nsplit * 16 * (4 * 1024 + 32)     # replay scratch: 16 steps of S_dec and r per CTA
+              + b * T * HV * nsplit * (4 * K + 1)          # the CTAs' row sums
+              + 2 * b * T * HV * K)                        # dq, dk per value head
+    assert floats * 4 <= need <= floats * 4 + 256 * 6
     n = ctypes.c_size_t(0)
     for over, code in [(dict(key_dim=129), 2), (dict(value_dim=129), 2), (dict(value_heads=6, nheads=4), 2),
                        (dict(seqlen=0), 1), (dict(key_dim=0), 1)]:

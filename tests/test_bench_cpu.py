@@ -56,7 +56,7 @@ def test_every_launch_has_a_byte_count():
     names = _launch_names()
     assert {"k_tc_bwd_chunk", "k_tc_fwd_chunk", "k_tc_scan_pair_cb", "k_m1_backward", "k_chunk_bwd"} <= names
     kda = {n for n in names if n.startswith("k_kda")}
-    assert kda == {"k_kda_forward", "k_kda_checkpoints", "k_kda_backward", "k_kda_gva"}
+    assert kda == {"k_kda_forward", "k_kda_checkpoints", "k_kda_backward", "k_kda_rows", "k_kda_gva"}
     for cfg in CONFIGS.values():
         for n in names - kda:
             assert bench.kernel_bytes(n, cfg) is not None, (n, cfg["variant"])
