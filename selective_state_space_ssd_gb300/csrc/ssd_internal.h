@@ -146,6 +146,27 @@ size_t m1_backward_ws(const Dims& d);
 cudaError_t m1_forward(const Dims& d, const FwdArgs& a, void* ws, cudaStream_t st);
 cudaError_t m1_backward(const Dims& d, const BwdArgs& a, void* ws, cudaStream_t st);
 
+// Launches `kernel` with programmatic stream serialization: it may be scheduled
+// while the previous kernel on `st` finishes, and must call pdl_wait() (the
+// device side, tc_common.cuh) before it touches global memory.  Used for the
+// second and later kernels of one call, whose prologue (barrier set-up, TMEM
+// allocation) then overlaps the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                         Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Per-launch event timing (see ssd_profile_start in ssd.h).  SSD_LAUNCH wraps
 // every kernel launch of the library.
 void prof_begin(const char* name, cudaStream_t st);

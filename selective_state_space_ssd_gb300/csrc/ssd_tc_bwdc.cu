@@ -182,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();     // the chunk states, dS and C B^T tiles of the scan launch before this kernel
+  pdl_trigger();  // the sums kernel may be scheduled as this kernel's CTAs finish
   const uint32_t tmem = sm.tmem_slot;
   const uint32_t ACC_B = tmem, ACC_C = tmem + 64u;                  // dB^T, dC^T (M = 128, lane n)
   auto TW = [&](int j) { return tmem + 128u + 192u * j; };         // dW~ (M = 64), then dv_or (M = 128, lane s)
@@ -646,6 +648,7 @@ __global__ void __launch_bounds__(256) k_bwdc_sums(const float* __restrict__ dB_
                                                    int hpg, int T, int G, int nc, int b, int H) {
   const long long nb = 4 * nchunks;
   const int lane = threadIdx.x & 31;
+  pdl_wait();  // the partials of the chunk kernel before this one
   if ((long long)blockIdx.x >= nb) {
     const int h = (int)(((long long)blockIdx.x - nb) * 8) + (threadIdx.x >> 5);
     if (h >= H) return;
@@ -779,17 +782,20 @@ cudaError_t tc_backward(const Dims& problem, const BwdArgs& a, void* ws, cudaStr
   const int smem = (int)sizeof(BwdcSmem) + 1024;
   e = cudaFuncSetAttribute(k_tc_bwdc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  SSD_LAUNCH("k_tc_bwd_chunk", st, k_tc_bwdc<<<l.grid, kThreads, smem, st>>>(tx, tdy, tdx, tb, tcm, ts, tds, prm));
+  SSD_LAUNCH("k_tc_bwd_chunk", st,
+             e = launch_after(k_tc_bwdc, l.grid, kThreads, smem, st, tx, tdy, tdx, tb, tcm, ts, tds, prm));
+  if (e != cudaSuccess) return e;
   // dB, dC blocks unless the chunk kernel wrote them; dA blocks unless there is no A (MIMO)
   const long long nchunks_sum = direct ? 0 : l.nchunks;
   const long long sum_blocks = 4 * nchunks_sum + (a.dA ? (d.H + 7) / 8 : 0);
   if (sum_blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   if (sum_blocks > 0)
     SSD_LAUNCH("k_tc_bwd_sums", st,
-               k_bwdc_sums<<<(unsigned)sum_blocks, 256, 0, st>>>(
-                   w.dB_part, w.dC_part, static_cast<__nv_bfloat16*>(a.dB), static_cast<__nv_bfloat16*>(a.dC),
-                   w.dA_part, a.dA, nchunks_sum, lmax.nseg, l.total, l.grid, d.hpg, d.T, d.G, d.nc, d.b, d.H));
-  return cudaGetLastError();
+               e = launch_after(k_bwdc_sums, (unsigned)sum_blocks, 256, 0, st, (const float*)w.dB_part,
+                                (const float*)w.dC_part, static_cast<__nv_bfloat16*>(a.dB),
+                                static_cast<__nv_bfloat16*>(a.dC), (const float*)w.dA_part, a.dA, nchunks_sum,
+                                lmax.nseg, l.total, (long long)l.grid, d.hpg, d.T, d.G, d.nc, d.b, d.H));
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ssd

@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the chunk states and C B^T tiles of the scan launch before this kernel
   const uint32_t tmem = sm.tmem_slot;
   auto TYD = [&](int r) { return tmem + 256u * r; };          // y_diag of the pair (M = 128, 128 columns)
   auto TYO = [&](int r) { return tmem + 256u * r + 128u; };   // y_off of the pair
@@ -480,8 +481,8 @@ cudaError_t tc_forward(const Dims& problem, const FwdArgs& a, void* ws, cudaStre
   const int smem = (int)sizeof(FwdcSmem) + 1024;
   e = cudaFuncSetAttribute(k_tc_fwdc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  SSD_LAUNCH("k_tc_fwd_chunk", st, k_tc_fwdc<<<grid, kThreads, smem, st>>>(tx, tcm, ts, ty, prm));
-  return cudaGetLastError();
+  SSD_LAUNCH("k_tc_fwd_chunk", st, e = launch_after(k_tc_fwdc, grid, kThreads, smem, st, tx, tcm, ts, ty, prm));
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ssd

@@ -448,6 +448,7 @@ template <int kStU>
 __global__ void __launch_bounds__(kThreads, 3) k_scan(const __grid_constant__ ScanLaunch job) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  pdl_trigger();  // the chunk kernel after this launch may take SMs as they free up (it waits for this launch)
   int i = blockIdx.x;
   if (job.rev_first) {
     if (i < job.n_rev) {

@@ -317,6 +317,15 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t w) {
   return __bfloat1622float2(h);
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization (launch_after) may start while the kernel before it on
+// the stream still runs: pdl_wait() blocks until that kernel has completed and its memory is visible (a no-op for
+// a kernel launched without the attribute), so everything before it may touch only shared memory, TMEM and
+// barriers.  pdl_trigger() lets the next kernel's CTAs be scheduled once every CTA of this one has triggered or
+// exited (they still wait in pdl_wait for this kernel's results).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------ shared helpers
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // Named barrier that also ORs a predicate over the participating threads, so
