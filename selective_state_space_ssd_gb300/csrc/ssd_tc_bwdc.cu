@@ -266,10 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = n - 1, jm = m & 1;
           if (!mbar_wait(&sm.e_done[jm], (m >> 1) & 1, status, 133)) break;
           tc_fence_after();
-#pragma unroll 1
-          for (int kk = 0; kk < kL; kk += 16)  // dv_or[s][p] = sum_t W[t][s] dy[t][p]  (rows s in lanes 0-63)
-            mma_bf16(TW(jm), mdesc(sm.W[jm], kL, kk), mdesc(sm.xy[m % 3].dy, kL, kk), idesc_bf16(128, 64, true, true),
-                     kk > 0);
+          // dv_or[s][p] = sum_t W[t][s] dy[t][p]  (rows s in lanes 0-63).  These four MMAs sit between E and the
+          // next O phase, so they are issued unrolled from precomputed descriptors; the other loops stay rolled
+          // (issued faster, their MMAs run beside the pool's shared-memory work and slow it more than they gain)
+          const uint64_t wa = mdesc(sm.W[jm], kL, 0), wb = mdesc(sm.xy[m % 3].dy, kL, 0);
+#pragma unroll
+          for (int kk = 0; kk < kL; kk += 16)
+            mma_bf16(TW(jm), wa + mdesc_step(kk), wb + mdesc_step(kk), idesc_bf16(128, 64, true, true), kk > 0);
           if (c2.last(geo, q1)) {
             // dB^T[n][s] += sum_t C[t][n] dCBsum[t][s],  dC^T[n][t] += sum_s B[s][n] dCBsum[t][s]
 #pragma unroll 1
