@@ -193,16 +193,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (u.a.first(q0)) ++seg;
         tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kN; kk += 16)  // y_off[t][p] = sum_n C[t][n] S[n][p], both heads
-          mma_bf16(TYO(r), kdesc(sm.CC[0], 2 * kL, kk), mdesc(sm.S[r][0], kN, kk), idesc_bf16(128, 128, false, true),
-                   kk > 0);
+        // y_off[t][p] = sum_n C[t][n] S[n][p], both heads (unrolled, precomputed descriptors)
+        const uint64_t cd = kdesc(sm.CC[0], 2 * kL, 0), sd = mdesc(sm.S[r][0], kN, 0);
+#pragma unroll
+        for (int kk = 0; kk < kN; kk += 16)
+          mma_bf16(TYO(r), cd + kdesc_step(2 * kL, kk), sd + mdesc_step(kk), idesc_bf16(128, 128, false, true), kk > 0);
         if (!mbar_wait(&sm.w_ready[r], ph, status, 206)) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kL; kk += 16)  // y_diag[t][p] = sum_s W'[t][s] x[s][p], both heads
-          mma_bf16(TYD(r), kdesc(sm.W[r][0], 2 * kL, kk), mdesc(sm.x[r][0], kL, kk), idesc_bf16(128, 128, false, true),
-                   kk > 0);
+        // y_diag[t][p] = sum_s W'[t][s] x[s][p], both heads: after W' is ready, on the pair's critical path, so
+        // issued unrolled from precomputed descriptors
+        const uint64_t wd = kdesc(sm.W[r][0], 2 * kL, 0), xd = mdesc(sm.x[r][0], kL, 0);
+#pragma unroll
+        for (int kk = 0; kk < kL; kk += 16)
+          mma_bf16(TYD(r), wd + kdesc_step(2 * kL, kk), xd + mdesc_step(kk), idesc_bf16(128, 128, false, true), kk > 0);
         mma_commit(&sm.mma_done[r]);
         mma_commit(&sm.slot_empty[r]);
         if (u.last(geo, q1)) mma_commit(&sm.chunk_empty);

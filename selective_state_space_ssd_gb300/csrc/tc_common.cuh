@@ -351,6 +351,10 @@ __device__ __forceinline__ uint64_t mdesc(const void* tile, int krows, int kk) {
 // The MN-major descriptor at K offset kk as an increment of the kk = 0 one, in the 16-byte units of the address
 // field (which cannot carry into the next field: shared memory addresses stay below 256 KB).
 __host__ __device__ constexpr uint64_t mdesc_step(int kk) { return (uint64_t)kk * 8u; }
+// The same for the K-major descriptor of a tile with `rows` rows (kdesc).
+__host__ __device__ constexpr uint64_t kdesc_step(int rows, int kk) {
+  return (uint64_t)((((kk >> 6) * rows * 128) + (kk & 63) * 2) >> 4);
+}
 
 // Stores nchunks x 8 floats as bf16 into row `row` of a SW128 tile, from
 // 16-byte chunk chunk0 on.
