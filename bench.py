@@ -139,7 +139,8 @@ def kernel_bytes(name, cfg):
     part = b * T * H * N * 4 if m2 else 0
     G = cfg.get("ngroups", 1) if m2 else H
     sbf = b * H * nc * P * N * 2                 # bf16 chunk states
-    cbb = b * nc * G * L * L * 4                 # fp32 C B^T per (chunk, group)
+    cbb = b * nc * G * L * L * (2 if tc_path(cfg) and cfg["variant"] == "mimo" else 4)  # C B^T per (chunk, group):
+                                                 # fp32, bf16 for MIMO on the tensor-core kernels (a tile per head)
     cpart = b * nc * G * L * N * 4               # fp32 dB (or dC) partial, one slot per chunk
     dvws = b * T * H * P * 4 if m2 else 0
     # Mamba-1 backward: 128-thread blocks of 128 / w channels (w = threads per channel, 2 states each), a

@@ -103,7 +103,7 @@ struct alignas(1024) BwdcSmem {
 struct BwdcParams {
   const float* dt_raw;
   const float* A;
-  const float* CB;  // [b, nc, G, L, L] fp32
+  const float* CB;  // [b, nc, G, L, L]: fp32, bf16 for MIMO (load_cb8)
   float* ddt_raw;
   float* dA_part;  // [b, H, nc]
   float* dB_part;  // [chunks][nseg][L][N]
@@ -505,11 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool first = has_cur && ce.first(q0), last = has_cur && ce.last(geo, q1);
         if (has_cur && e_warp && first) {
           ++seg_e;
-          const float* cbrow = prm.CB + ((size_t)ce.k * kL + 16 * qd + (lane & 15)) * kL + 16 * gi + 8 * (lane >> 4);
-          const float4 u = __ldg(reinterpret_cast<const float4*>(cbrow));
-          const float4 v = __ldg(reinterpret_cast<const float4*>(cbrow + 4));
-          cbv[0] = u.x, cbv[1] = u.y, cbv[2] = u.z, cbv[3] = u.w;
-          cbv[4] = v.x, cbv[5] = v.y, cbv[6] = v.z, cbv[7] = v.w;
+          load_cb8(prm.CB, ((size_t)ce.k * kL + 16 * qd + (lane & 15)) * kL + 16 * gi + 8 * (lane >> 4), prm.mimo, cbv);
         }
         const int k4w = (warp == 8 || warp == 9 || warp == 12 || warp == 13) ? 2 * ((warp >> 2) - 2) + (warp & 1) : -1;
         bool ok = true;

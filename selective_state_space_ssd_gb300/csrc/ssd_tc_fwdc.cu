@@ -80,7 +80,7 @@ struct alignas(1024) FwdcSmem {
 struct FwdcParams {
   const float* dt_raw;
   const float* A;
-  const float* CB;  // [b, nc, G, L, L] fp32
+  const float* CB;  // [b, nc, G, L, L]: fp32, bf16 for MIMO (load_cb8)
   int* status;
   int T, H, G, hpg, nc;
   int total;     // items b * nc * G * hpg (< 2^31)
@@ -340,14 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = k & 1, sc = k % kSc;
       if (has_w && uw.a.first(q0)) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const float* cbrow =
-              prm.CB + ((size_t)uw.a.k * kL + 16 * tq[m] + (lane & 15)) * kL + 16 * tj[m] + 8 * (lane >> 4);
-          const float4 c0 = __ldg(reinterpret_cast<const float4*>(cbrow));
-          const float4 c1 = __ldg(reinterpret_cast<const float4*>(cbrow + 4));
-          cbv[8 * m + 0] = c0.x, cbv[8 * m + 1] = c0.y, cbv[8 * m + 2] = c0.z, cbv[8 * m + 3] = c0.w;
-          cbv[8 * m + 4] = c1.x, cbv[8 * m + 5] = c1.y, cbv[8 * m + 6] = c1.z, cbv[8 * m + 7] = c1.w;
-        }
+        for (int m = 0; m < 2; ++m)
+          load_cb8(prm.CB, ((size_t)uw.a.k * kL + 16 * tq[m] + (lane & 15)) * kL + 16 * tj[m] + 8 * (lane >> 4),
+                   prm.mimo, cbv + 8 * m);
       }
       bool ok = true;
       if (tid == kLead) {  // one thread waits; the named barrier passes the inputs to the pool

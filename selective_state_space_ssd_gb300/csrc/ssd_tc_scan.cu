@@ -366,9 +366,10 @@ __device__ __forceinline__ void scan_chain(const ScanJob& job, int h, int b, int
 // M = 64, N = 64 MMA, and warps 0-3 write the accumulator rows out; the other warps only join the barriers.
 struct CbJob {
   CUtensorMap c, b;
-  float* CB;  // [b, nc, G, L, L]
+  float* CB;  // [b, nc, G, L, L]: fp32, or bf16 when bf16 is set (MIMO: one tile per head, twice the bytes of y)
   int* status;
   int G, nc;
+  int bf16;
 };
 
 struct alignas(1024) CbSmem {
@@ -420,11 +421,22 @@ __device__ __forceinline__ void cb_tile(const CbJob& job, int k, uint8_t* smem) 
       uint32_t v[32];
       tmem_ld_pair32(taddr(tmem, 32 * warp, 0), v);
       tmem_wait_ld();
-      float4* out = reinterpret_cast<float4*>(job.CB + ((size_t)k * kL + t) * kL + s0);
+      const size_t o = ((size_t)k * kL + t) * kL + s0;
+      if (job.bf16) {
+        uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(job.CB) + o);
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        out[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
-                             __uint_as_float(v[4 * e + 3]));
+        for (int e = 0; e < 4; ++e)
+          out[e] = make_uint4(pack_bf16(__uint_as_float(v[8 * e]), __uint_as_float(v[8 * e + 1])),
+                              pack_bf16(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3])),
+                              pack_bf16(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5])),
+                              pack_bf16(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7])));
+      } else {
+        float4* out = reinterpret_cast<float4*>(job.CB + o);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          out[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
+                               __uint_as_float(v[4 * e + 3]));
+      }
     }
   }
   tc_fence_before();
@@ -539,6 +551,7 @@ cudaError_t tc_scans(const Dims& d, const ScanSide* fwd, const ScanSide* rev, co
   job.cb.status = status;
   job.cb.G = d.G;
   job.cb.nc = d.nc;
+  job.cb.bf16 = d.variant == kMimo;
   job.n_fwd = (int)fwd_blocks;
   job.n_rev = rev ? (int)chains : 0;
   job.nk = segmented ? nk : 1;

@@ -321,6 +321,23 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t w) {
   __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
   return __bfloat1622float2(h);
 }
+// Eight consecutive C B^T values of a tile row as fp32: fp32 tiles, or bf16 tiles (bf16 set; MIMO).
+__device__ __forceinline__ void load_cb8(const float* CB, size_t o, bool bf16, float* v) {
+  if (bf16) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(CB) + o));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16(u[e]);
+      v[2 * e] = f.x;
+      v[2 * e + 1] = f.y;
+    }
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(CB + o));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(CB + o + 4));
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+  }
+}
 
 // ------------------------------------------------------------ programmatic dependent launch
 // A kernel launched with programmatic stream serialization (launch_after) may start while the kernel before it on
