@@ -3,8 +3,10 @@
 // state).  Per (batch, channel d, state n):
 //     s_t[n] = exp(dt'_t A[d,n]) s_{t-1}[n] + dt'_t x_t B_t[n],   y_t = sum_n s_t[n] C_t[n],
 // a serial recurrence in t with no chunkwise shortcut (the decay differs per
-// state), so the work is laid out for latency: one thread carries kS states of
-// one channel, the Wc threads of a channel are adjacent lanes (y and the other
+// state), so the work is laid out for latency and issue: one thread carries
+// kS = 4 states of one channel (the step's shared-memory loads and the lane
+// shuffles of a channel serve four states; with two a thread both kernels were
+// issue-bound), the Wc threads of a channel are adjacent lanes (y and the other
 // sums over n are Wc-lane shuffles), and a block of 128 threads holds cpb =
 // 128 / Wc consecutive channels of one sequence.  The block walks the sequence
 // in chunks (32 steps in the forward, 8 in the backward) whose inputs (x, dt,
@@ -13,8 +15,9 @@
 //
 // The backward replays the forward once to keep the state entering every
 // chunk (a checkpoint in global memory), then walks the chunks in reverse:
-// each is replayed from its checkpoint into registers (states and decays of
-// its 8 steps) and walked backwards, carrying dS from the ds_final seed (the
+// each is replayed from its checkpoint into registers (the states of its 8
+// steps; the walk recomputes each decay, with the same bits, rather than keep
+// 32 of them in registers) and walked backwards, carrying dS from the ds_final seed (the
 // same page, "Two things that are easy to get wrong": the nonzero seed, and
 // s_{t-1} recomputed for d(dt)).  dB_t and dC_t are sums over every channel:
 // each block adds its channels in ascending order in shared memory and writes
@@ -31,7 +34,7 @@ namespace ssd {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kS = 2;        // states per thread
+constexpr int kS = 4;        // states per thread
 constexpr int kTcF = 32;     // steps per chunk, forward
 constexpr int kTc = 8;       // steps per chunk, backward (its replay keeps a chunk's states in registers)
 constexpr int kStages = 3;   // chunk buffers: the one in use and two in flight
@@ -75,14 +78,16 @@ struct Geo {
   static constexpr int cpb = kThreads / kWc, NP = kS * kWc;
 };
 
-// kS consecutive floats of shared memory (8-byte aligned)
-__device__ __forceinline__ void lds2(const float* p, float (&v)[kS]) {
-  const float2 w = *reinterpret_cast<const float2*>(p);
+// kS consecutive floats of shared memory (16-byte aligned)
+__device__ __forceinline__ void ldsk(const float* p, float (&v)[kS]) {
+  const float4 w = *reinterpret_cast<const float4*>(p);
   v[0] = w.x;
   v[1] = w.y;
+  v[2] = w.z;
+  v[3] = w.w;
 }
-__device__ __forceinline__ void sts2(float* p, const float (&v)[kS]) {
-  *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+__device__ __forceinline__ void stsk(float* p, const float (&v)[kS]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
 // One chunk's inputs in shared memory: per step t of the chunk, the block's
@@ -179,8 +184,8 @@ __global__ void __launch_bounds__(kThreads) k_m1_forward(M1 m, float* y, float* 
     for (int tt = 0; tt < kTcF; ++tt) {
       const float dp = dtp[tt * cpb + c], u = dp * cur.x[tt * cpb + c];
       float Bj[kS], Cj[kS];
-      lds2(cur.B + tt * NP + kS * l, Bj);
-      lds2(cur.C + tt * NP + kS * l, Cj);
+      ldsk(cur.B + tt * NP + kS * l, Bj);
+      ldsk(cur.C + tt * NP + kS * l, Cj);
       float yp = 0.f;
 #pragma unroll
       for (int j = 0; j < kS; ++j) {
@@ -218,7 +223,7 @@ struct M1Bwd {
 };
 
 template <int kWc>
-__global__ void __launch_bounds__(kThreads, 6) k_m1_backward(M1 m, M1Bwd g) {
+__global__ void __launch_bounds__(kThreads, 4) k_m1_backward(M1 m, M1Bwd g) {
   constexpr int cpb = Geo<kWc>::cpb, NP = Geo<kWc>::NP;
   constexpr size_t sf = stage_floats(cpb, NP, kTc, true);
   extern __shared__ float smf[];
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_m1_backward(M1 m, M1Bwd g) {
     for (int tt = 0; tt < kTc; ++tt) {
       const float dp = dtp[tt * cpb + c], u = dp * cur.x[tt * cpb + c];
       float Bj[kS];
-      lds2(cur.B + tt * NP + kS * l, Bj);
+      ldsk(cur.B + tt * NP + kS * l, Bj);
 #pragma unroll
       for (int j = 0; j < kS; ++j) s[j] = decay(dp, A2[j]) * s[j] + u * Bj[j];
     }
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_m1_backward(M1 m, M1Bwd g) {
                            true);
     cp_async_commit();
     // the chunk's entering state, from its checkpoint
-    float S[kTc + 1][kS], a[kTc][kS];
+    float S[kTc + 1][kS];
 #pragma unroll
     for (int j = 0; j < kS; ++j) S[0][j] = act[j] ? *ck_at(k, j) : 0.f;
     cp_async_wait_stages();
@@ -312,11 +317,10 @@ __global__ void __launch_bounds__(kThreads, 6) k_m1_backward(M1 m, M1Bwd g) {
     for (int tt = 0; tt < kTc; ++tt) {
       const float dp = dtp[tt * cpb + c], u = dp * cur.x[tt * cpb + c];
       float Bj[kS];
-      lds2(cur.B + tt * NP + kS * l, Bj);
+      ldsk(cur.B + tt * NP + kS * l, Bj);
 #pragma unroll
       for (int j = 0; j < kS; ++j) {
-        a[tt][j] = decay(dp, A2[j]);
-        S[tt + 1][j] = a[tt][j] * S[tt][j] + u * Bj[j];
+        S[tt + 1][j] = decay(dp, A2[j]) * S[tt][j] + u * Bj[j];
       }
     }
     // walk it backwards
@@ -325,19 +329,20 @@ __global__ void __launch_bounds__(kThreads, 6) k_m1_backward(M1 m, M1Bwd g) {
       const int ic = tt * cpb + c;
       const float dp = dtp[ic], xv = cur.x[ic], dyv = cur.dy[ic];
       float Bj[kS], Cj[kS];
-      lds2(cur.B + tt * NP + kS * l, Bj);
-      lds2(cur.C + tt * NP + kS * l, Cj);
+      ldsk(cur.B + tt * NP + kS * l, Bj);
+      ldsk(cur.C + tt * NP + kS * l, Cj);
       float up = 0.f, ddp = 0.f, tB[kS], tC[kS];
 #pragma unroll
       for (int j = 0; j < kS; ++j) {
+        const float aj = decay(dp, A2[j]);  // recomputed (the same bits as the replay's): registers for 4 states
         dS[j] += dyv * Cj[j];        // y_t = s_t . C_t
         tC[j] = dyv * S[tt + 1][j];  // dC_t uses s_t
         up += dS[j] * Bj[j];         // d(dt' x) direction
         tB[j] = dp * xv * dS[j];
-        const float dda = a[tt][j] * dS[j] * S[tt][j];  // the decay path, with s_{t-1}
+        const float dda = aj * dS[j] * S[tt][j];  // the decay path, with s_{t-1}
         dA[j] += dp * dda;
         ddp += A[j] * dda;
-        dS[j] *= a[tt][j];
+        dS[j] *= aj;
       }
       const float u = group_sum<kWc>(up);
       const float dd = u * xv + group_sum<kWc>(ddp);
@@ -345,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 6) k_m1_backward(M1 m, M1Bwd g) {
         dxs[ic] = dp * u;
         dds[ic] = dd * sig[ic];
       }
-      sts2(rB + (size_t)ic * NP + kS * l, tB);
-      sts2(rC + (size_t)ic * NP + kS * l, tC);
+      stsk(rB + (size_t)ic * NP + kS * l, tB);
+      stsk(rC + (size_t)ic * NP + kS * l, tC);
     }
     __syncthreads();  // also: the chunk's buffers are free for the copies issued next
     const int t0 = k * kTc;
@@ -493,7 +498,7 @@ cudaError_t m1_forward(const Dims& d, const FwdArgs& a, void*, cudaStream_t st) 
   const M1 m = make_m1(d, a.x, a.dt_raw, a.A, a.B, a.C, a.s0);
   if ((long long)m.b * m.nblk > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   float* y = static_cast<float*>(a.y);
-  switch (m.Wc) {  // N <= 32 and two states a thread: 1 to 16 threads a channel
+  switch (m.Wc) {  // N <= 32 and four states a thread: 1 to 8 threads a channel
     case 1: return launch_fwd<1>(m, y, a.s_final, st);
     case 2: return launch_fwd<2>(m, y, a.s_final, st);
     case 4: return launch_fwd<4>(m, y, a.s_final, st);
