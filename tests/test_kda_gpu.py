@@ -4,8 +4,8 @@ within the fp32 bound 1e-4 for every output.
 
 Cases cover: the tiny shape of the oracle's pins; key and value widths that
 are not multiples of the warp layout (masked rows and columns) with T not a
-multiple of the 16-step checkpoint segment; a zero initial state; one value
-head per query / key head and four; head dimension 128.  At the full
+multiple of the 16-step checkpoint segment; a zero initial state; one, two
+and four value heads per query / key head; head dimension 128.  At the full
 workload size (b=2, T=1024, 16 value heads, K=V=128) one query / key head
 group is checked against the oracle (its G value heads are independent of
 the rest), and the Euler identities of the recurrence hold over all of it.
@@ -31,6 +31,7 @@ CASES = {
     "ragged": dict(BASE, batch=2, seqlen=37, nheads=1, value_heads=2, key_dim=40, value_dim=20),
     "gva4": dict(BASE, batch=1, seqlen=48, nheads=1, value_heads=4, key_dim=32, value_dim=16),
     "dim128": dict(BASE, batch=1, seqlen=100, nheads=2, value_heads=4, key_dim=128, value_dim=128),
+    "one_value_head": dict(BASE, batch=2, seqlen=50, nheads=3, value_heads=3, key_dim=64, value_dim=40),
 }
 OUT_F = ("o", "s_final")
 OUT_B = ("dq", "dk", "dv", "dg", "dbeta", "ds0")
