@@ -40,11 +40,17 @@ constexpr int kTc = 8;       // steps per chunk, backward (its replay keeps a ch
 constexpr int kStages = 3;   // chunk buffers: the one in use and two in flight
 constexpr float kLog2e = 1.4426950408889634f;
 
-// exp(dp * A) as exp2f(dp * A2) with A2 = A log2(e) formed once per state: the
-// exponent's rounding adds a relative error below 1e-6 over the arguments the
-// scan meets (|dp A| <= 5), far inside the fp32 path's 1e-4 bound, for a few
-// instructions instead of an accurate expf.
-__device__ __forceinline__ float decay(float dp, float A2) { return exp2f(dp * A2); }
+// exp(dp * A) as 2^(dp * A2) with A2 = A log2(e) formed once per state, on the
+// hardware's approximate exp2 (ex2.approx.ftz: relative error about 2^-22; the
+// decays lie in (2^-8, 1], far from the flushed subnormals).  The exponent's
+// rounding adds a relative error below 1e-6 over the arguments the scan meets
+// (|dp A| <= 5), far inside the fp32 path's 1e-4 bound, for two instructions
+// instead of an accurate expf or the subnormal-safe exp2f.
+__device__ __forceinline__ float decay(float dp, float A2) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(dp * A2));
+  return r;
+}
 
 struct M1 {
   const float *x, *dt, *A, *B, *C, *s0;
