@@ -655,6 +655,22 @@ def run_once(args):
     from selective_state_space_ssd_gb300 import binding
     from selective_state_space_ssd_gb300 import inputs as synth
 
+    if args.workload in KDA_CONFIGS:
+        cfg = dict(KDA_CONFIGS[args.workload])
+        if args.batch is not None:
+            cfg["batch"] = args.batch
+        if args.seqlen is not None:
+            cfg["seqlen"] = args.seqlen
+        binding.load()
+        dev = torch.device("cuda", 0)
+        t = {k: (None if v is None else v.to(dev)) for k, v in synth.make_kda_inputs(cfg, seed=0).items()}
+        o, sf = binding.kda_forward(cfg, t["q"], t["k"], t["v"], t["g"], t["beta"], t["s0"])
+        grads = binding.kda_backward(cfg, t["do"], t["ds_final"], t["q"], t["k"], t["v"], t["g"], t["beta"], t["s0"])
+        torch.cuda.synchronize()
+        print(json.dumps({"once": args.workload, "batch": cfg["batch"], "seqlen": cfg["seqlen"],
+                          "o_finite": bool(torch.isfinite(o).all()),
+                          "dq_finite": bool(torch.isfinite(grads["dq"]).all())}), flush=True)
+        return 0
     cfg = CONFIGS[args.workload]
     if args.batch is not None:
         cfg = scaled(cfg, batch=args.batch)

@@ -2,11 +2,11 @@
 // "sec-10.tex", section "反向传播推导": forward F1-F6, reverse steps 1-6), fp32.
 //
 // Per batch element b and value head hv (query / key head h = hv / G), the
-// state S is K x V.  Each warp owns 8 value columns of one (b, hv) and keeps
-// its K x 8 slice of S in registers: lane l holds rows l, l + 32, l + 64,
+// state S is K x V.  Each warp owns 4 value columns of one (b, hv) and keeps
+// its K x 4 slice of S in registers: lane l holds rows l, l + 32, l + 64,
 // l + 96.  Column work (p = k^T S_dec, o = q^T S, dr) reduces over the key
 // rows of a column: a warp reduction.  Row work of the backward (dq, da, dk,
-// dg) reduces over the value columns: each warp's 8-column partial sums are
+// dg) reduces over the value columns: each warp's 4-column partial sums are
 // added over the warps of its CTA in warp order (shared memory, one barrier
 // per step), then over the CTAs of the (b, hv) in CTA order (a small kernel).
 // Every warp loads the next step's inputs while it computes the current one,
@@ -16,7 +16,7 @@
 //   backward  1. k_kda_forward<true> replays the forward from the leaf inputs
 //                and keeps the state entering every 16th step (checkpoints,
 //                stored lane-major so every store is one coalesced line);
-//             2. k_kda_backward, CTAs of up to four column warps of one
+//             2. k_kda_backward, CTAs of up to eight column warps of one
 //                (b, hv), walks the 16-step segments from the last: it replays
 //                the segment from its checkpoint (S_dec and r of every step to
 //                a per-CTA scratch that stays in L2), then runs steps 1-6
@@ -39,10 +39,10 @@ namespace ssd {
 namespace {
 
 constexpr int kRows = 4;       // key rows per lane: K <= 128
-constexpr int kCols = 8;       // value columns per warp: V <= 128 in at most 16 warps
+constexpr int kCols = 4;       // value columns per warp: V <= 128 in at most 32 warps
 constexpr int kSeg = 16;       // steps per checkpoint segment
-constexpr int kMaxWarps = 16;  // column warps of a (b, hv)
-constexpr int kCtaWarps = 4;   // column warps of a backward CTA
+constexpr int kMaxWarps = 32;  // column warps of a (b, hv)
+constexpr int kCtaWarps = 8;   // column warps of a backward CTA
 constexpr int kSlice = 32 * kRows * kCols;  // floats of one warp's state slice
 
 struct KdaDims {
@@ -121,12 +121,12 @@ __device__ __forceinline__ void delta_step(float (&S)[kRows][kCols], const StepI
   }
 }
 
-// Checkpoint slot of warp w's slice: [unit][seg][w][i * 8 + j][lane] (lane-major: one coalesced line per store)
+// Checkpoint slot of warp w's slice: [unit][seg][w][i * kCols + j][lane] (lane-major: one coalesced line per store)
 __device__ __forceinline__ size_t ckpt_slot(const KdaDims& d, int unit, int seg, int w) {
   return (((size_t)unit * d.nseg + seg) * d.nw + w) * kSlice;
 }
 
-// Forward: one warp per 8 columns of one (b, hv); grid (b * HV, ceil(nw / 2)), two warps per CTA.
+// Forward: one warp per 4 columns of one (b, hv); grid (b * HV, ceil(nw / 2)), two warps per CTA.
 // kCkpt: the backward's replay, which writes only the state entering every 16th step (checkpoints);
 // otherwise o [b,T,HV,V] and s_final [b,HV,K,V].
 template <bool kCkpt>
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const f
     float r[kCols];
     delta_step(S, s, r);
     if (!kCkpt) {
-      float out = 0.f;  // o[col0 + lane] for lanes 0-7
+      float out = 0.f;  // o[col0 + lane] for lanes 0 .. kCols - 1
 #pragma unroll
       for (int j = 0; j < kCols; ++j) {
         float x = 0.f;
@@ -192,7 +192,7 @@ struct KdaBwdOut {
   float* dv;              // [b,T,HV,V]
   float* ds0;             // [b,HV,K,V]
   const float* ckpt;      // checkpoints (ckpt_slot)
-  float* scratch;         // per CTA: kSeg steps x (wpc slices of S_dec, then 8 wpc values of r)
+  float* scratch;         // per CTA: kSeg steps x (wpc slices of S_dec, then kCols wpc values of r)
 };
 
 // Backward: CTA (unit, split) runs column warps split * wpc .. + wpc - 1 of (b, hv) = unit (the warps past nw
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(32 * kCtaWarps) k_kda_backward(KdaIn in, KdaDi
         if (lane < kCols) r_at(st, lane) = rv;
       }
     }
-    __syncwarp();  // the r values of the warp's columns, written by lanes 0-7, are read by every lane
+    __syncwarp();  // the r values of the warp's columns, written by lanes 0 .. kCols - 1, are read by every lane
     // steps 1-6 backwards through the segment
     StepIn nx;
     if (live) load_step(in, d, b, hv, t1 - 1, lane, col0, nx);
@@ -431,7 +431,7 @@ struct KdaWs {
 };
 
 // Backward workspace: checkpoints (units x nseg x nw slices), the replay scratch of every backward CTA (16 steps
-// of wpc slices and 8 wpc values of r), the CTAs' per-step row sums, and the per-value-head dq, dk.
+// of wpc slices and kCols wpc values of r), the CTAs' per-step row sums, and the per-value-head dq, dk.
 KdaWs kda_carve(const KdaDims& d, Carver& cv) {
   KdaWs w;
   const size_t units = (size_t)d.b * d.HV, rows = (size_t)d.b * d.T * d.HV;
