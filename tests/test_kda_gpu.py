@@ -3,8 +3,9 @@ float64 oracle (oracle/kda.py), element by element, max|gpu - ref| / max|ref|
 within the fp32 bound 1e-4 for every output.
 
 Cases cover: the tiny shape of the oracle's pins; key and value widths that
-are not multiples of the warp layout (masked rows and columns) with T not a
-multiple of the 16-step checkpoint segment; a zero initial state; one, two
+are not multiples of the warp layout (masked key rows past K; V = 45: a last
+column warp with one live column of four, and two backward CTAs, the second
+with idle warps) with T not a multiple of the 16-step checkpoint segment; a zero initial state; one, two
 and four value heads per query / key head; head dimension 128.  At the full
 workload size (b=2, T=1024, 16 value heads, K=V=128) one query / key head
 group is checked against the oracle (its G value heads are independent of
@@ -29,6 +30,7 @@ BASE = KDA_CONFIGS["kda_tiny_fp32"]
 CASES = {
     "tiny": BASE,
     "ragged": dict(BASE, batch=2, seqlen=37, nheads=1, value_heads=2, key_dim=40, value_dim=20),
+    "ragged_cols": dict(BASE, batch=1, seqlen=29, nheads=1, value_heads=2, key_dim=37, value_dim=45),
     "gva4": dict(BASE, batch=1, seqlen=48, nheads=1, value_heads=4, key_dim=32, value_dim=16),
     "dim128": dict(BASE, batch=1, seqlen=100, nheads=2, value_heads=4, key_dim=128, value_dim=128),
     "one_value_head": dict(BASE, batch=2, seqlen=50, nheads=3, value_heads=3, key_dim=64, value_dim=40),
