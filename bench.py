@@ -631,7 +631,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
 
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(1, min(args.steps, 30))  # the pipeline's fill and drain (one copy each way) spread over 30
     e2e_run(2)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
