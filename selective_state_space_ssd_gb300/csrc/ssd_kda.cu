@@ -14,12 +14,12 @@
 //
 //   forward   k_kda_forward<false>: o and s_final, every warp on its own.
 //   backward  1. k_kda_forward<true> replays the forward from the leaf inputs
-//                and keeps the state entering every 16th step (checkpoints,
+//                and keeps the state entering every 8th step (checkpoints,
 //                stored lane-major so every store is one coalesced line);
 //             2. k_kda_backward, CTAs of up to eight column warps of one
-//                (b, hv), walks the 16-step segments from the last: it replays
+//                (b, hv), walks the 8-step segments from the last: it replays
 //                the segment from its checkpoint (S_dec and r of every step to
-//                a per-CTA scratch that stays in L2), then runs steps 1-6
+//                shared memory), then runs steps 1-6
 //                backwards through it, carrying dS_acc in registers across
 //                segments, and writes the CTA's row sums per step;
 //             3. k_kda_rows adds the CTAs' row sums in CTA order (dq, dk, dg,
@@ -40,10 +40,12 @@ namespace {
 
 constexpr int kRows = 4;       // key rows per lane: K <= 128
 constexpr int kCols = 4;       // value columns per warp: V <= 128 in at most 32 warps
-constexpr int kSeg = 16;       // steps per checkpoint segment
+constexpr int kSeg = 8;        // steps per checkpoint segment
 constexpr int kMaxWarps = 32;  // column warps of a (b, hv)
 constexpr int kCtaWarps = 8;   // column warps of a backward CTA
 constexpr int kSlice = 32 * kRows * kCols;  // floats of one warp's state slice
+// dynamic shared memory of a backward CTA: the replay scratch of a segment for kCtaWarps warps
+constexpr size_t kBwdSmem = (size_t)kSeg * (kCtaWarps * kSlice + kCols * kCtaWarps) * sizeof(float);
 
 struct KdaDims {
   int b, T, H, HV, G, K, V;
@@ -127,7 +129,7 @@ __device__ __forceinline__ size_t ckpt_slot(const KdaDims& d, int unit, int seg,
 }
 
 // Forward: one warp per 4 columns of one (b, hv); grid (b * HV, ceil(nw / 2)), two warps per CTA.
-// kCkpt: the backward's replay, which writes only the state entering every 16th step (checkpoints);
+// kCkpt: the backward's replay, which writes only the state entering every kSeg-th step (checkpoints);
 // otherwise o [b,T,HV,V] and s_final [b,HV,K,V].
 template <bool kCkpt>
 __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const float* __restrict__ s0, float* o,
@@ -192,7 +194,6 @@ struct KdaBwdOut {
   float* dv;              // [b,T,HV,V]
   float* ds0;             // [b,HV,K,V]
   const float* ckpt;      // checkpoints (ckpt_slot)
-  float* scratch;         // per CTA: kSeg steps x (wpc slices of S_dec, then kCols wpc values of r)
 };
 
 // Backward: CTA (unit, split) runs column warps split * wpc .. + wpc - 1 of (b, hv) = unit (the warps past nw
@@ -209,8 +210,9 @@ __global__ void __launch_bounds__(32 * kCtaWarps) k_kda_backward(KdaIn in, KdaDi
   const int nlive = min(d.wpc, d.nw - split * d.wpc);
   const int col0 = kCols * w;
   const size_t sbase = (size_t)unit * d.K * d.V;
+  // the replay scratch, in shared memory: kSeg steps x (wpc slices of S_dec, then kCols wpc values of r)
+  extern __shared__ float scr[];
   const size_t step_floats = (size_t)d.wpc * kSlice + kCols * d.wpc;  // one step of the scratch
-  float* scr = out.scratch + ((size_t)unit * d.nsplit + split) * kSeg * step_floats;
   auto sd_at = [&](float* st, int i, int j) -> float& { return st[(size_t)wl * kSlice + (i * kCols + j) * 32 + lane]; };
   auto r_at = [&](float* st, int j) -> float& { return st[(size_t)d.wpc * kSlice + kCols * wl + j]; };
   const int rstride = 4 * d.K + 1;
@@ -427,16 +429,15 @@ ssd_status kda_dims(const ssd_kda_problem* p, KdaDims* d) {
 }
 
 struct KdaWs {
-  float *ckpt, *scratch, *part, *dq_e, *dk_e;
+  float *ckpt, *part, *dq_e, *dk_e;
 };
 
-// Backward workspace: checkpoints (units x nseg x nw slices), the replay scratch of every backward CTA (16 steps
-// of wpc slices and kCols wpc values of r), the CTAs' per-step row sums, and the per-value-head dq, dk.
+// Backward workspace: checkpoints (units x nseg x nw slices), the CTAs' per-step row sums, and the per-value-head
+// dq, dk.
 KdaWs kda_carve(const KdaDims& d, Carver& cv) {
   KdaWs w;
   const size_t units = (size_t)d.b * d.HV, rows = (size_t)d.b * d.T * d.HV;
   w.ckpt = cv.take<float>(units * d.nseg * d.nw * kSlice);
-  w.scratch = cv.take<float>(units * d.nsplit * kSeg * ((size_t)d.wpc * kSlice + kCols * d.wpc));
   w.part = cv.take<float>(rows * d.nsplit * (4 * (size_t)d.K + 1));
   w.dq_e = cv.take<float>(rows * d.K);
   w.dk_e = cv.take<float>(rows * d.K);
@@ -507,9 +508,11 @@ ssd_status ssd_kda_backward(const ssd_kda_problem* prob, const float* dout, cons
   const KdaIn in{q, k, v, g, beta, scale};
   const dim3 grid((unsigned)(d.b * d.HV), (unsigned)((d.nw + 1) / 2));
   SSD_LAUNCH("k_kda_checkpoints", st, k_kda_forward<true><<<grid, 64, 0, st>>>(in, d, s0, nullptr, nullptr, w.ckpt));
-  const KdaBwdOut out{dout, ds_final, w.part, dv, ds0, w.ckpt, w.scratch};
+  const KdaBwdOut out{dout, ds_final, w.part, dv, ds0, w.ckpt};
+  if (cudaFuncSetAttribute(k_kda_backward, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem) != cudaSuccess)
+    return SSD_ERR_CUDA;
   SSD_LAUNCH("k_kda_backward", st,
-             k_kda_backward<<<dim3((unsigned)(d.b * d.HV), (unsigned)d.nsplit), 32 * kCtaWarps, 0, st>>>(in, d, out));
+             k_kda_backward<<<dim3((unsigned)(d.b * d.HV), (unsigned)d.nsplit), 32 * kCtaWarps, kBwdSmem, st>>>(in, d, out));
   const long long rows = (long long)d.b * d.T * d.HV;
   const unsigned rblocks = (unsigned)(rows < 65535 * 8 ? rows : 65535 * 8);
   SSD_LAUNCH("k_kda_rows", st,

@@ -5,7 +5,7 @@ within the fp32 bound 1e-4 for every output.
 Cases cover: the tiny shape of the oracle's pins; key and value widths that
 are not multiples of the warp layout (masked key rows past K; V = 45: a last
 column warp with one live column of four, and two backward CTAs, the second
-with idle warps) with T not a multiple of the 16-step checkpoint segment; a zero initial state; one, two
+with idle warps) with T not a multiple of the 8-step checkpoint segment; a zero initial state; one, two
 and four value heads per query / key head; head dimension 128.  At the full
 workload size (b=2, T=1024, 16 value heads, K=V=128) one query / key head
 group is checked against the oracle (its G value heads are independent of
