@@ -216,17 +216,17 @@ def test_checkpoint_validation(cuda_lib):
 
 def test_kda_validation(cuda_lib):
     """KDA sizes: the forward needs only the status word; the backward's workspace holds the checkpoints every
-    16 steps, the 16-step replay scratch and the per-value-head dq, dk; bad sizes are refused on the host."""
+    8 steps, the CTAs' row sums and the per-value-head dq, dk (the replay scratch is in shared memory); bad sizes
+    are refused on the host."""
     from selective_state_space_ssd_gb300.configs import KDA_CONFIGS
     c = KDA_CONFIGS["kda_fp32"]
     p = binding.kda_problem(c)
     assert binding.ssd_kda_workspace_size(p, False) == 256
     b, T, HV, K, V = c["batch"], c["seqlen"], c["value_heads"], c["key_dim"], c["value_dim"]
     need = binding.ssd_kda_workspace_size(p, True)
-    nw = V // 8          # column warps of 8 value columns
-    nsplit = nw // 4     # backward CTAs of four column warps
-    floats = (b * HV * (-(-T // 16)) * nw * 1024           # lane-major checkpoints of every warp slice
-              + b * HV * nsplit * 16 * (4 * 1024 + 32)     # replay scratch: 16 steps of S_dec and r per CTA
+    nw = V // 4          # column warps of 4 value columns
+    nsplit = nw // 8     # backward CTAs of eight column warps
+    floats = (b * HV * (-(-T // 8)) * nw * 512             # lane-major checkpoints of every warp slice (K x 4)
               + b * T * HV * nsplit * (4 * K + 1)          # the CTAs' row sums
               + 2 * b * T * HV * K)                        # dq, dk per value head
     assert floats * 4 <= need <= floats * 4 + 256 * 6
