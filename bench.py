@@ -105,15 +105,15 @@ def kda_kernel_bytes(name, cfg):
     t = kda_tensor_bytes(cfg)
     b, T, HV, K, V = (cfg[k] for k in ("batch", "seqlen", "value_heads", "key_dim", "value_dim"))
     ins = 2 * t["q"] + t["v"] + t["g"] + t["beta"] + t["s"]
-    ckpt = b * HV * (-(-T // 16)) * K * V * 4
+    ckpt = b * HV * (-(-T // 8)) * K * V * 4  # the state every 8 steps
     per_head = b * T * HV * K * 4  # dq or dk per value head
-    nsplit = -(-(-(-cfg["value_dim"] // 8)) // 4)
+    nsplit = -(-(-(-cfg["value_dim"] // 4)) // 8)  # backward CTAs: eight warps of four value columns
     rows = b * T * HV * nsplit * (4 * K + 1) * 4  # the backward CTAs' per-step row sums
     table = {
         "k_kda_forward": ins + t["v"] + t["s"],
         "k_kda_checkpoints": ins + ckpt,
         # the replay and the reverse pass read the step inputs twice; do, ds_final and the checkpoints in;
-        # dv, ds0 and the CTAs' row sums out (the replay scratch stays in L2)
+        # dv, ds0 and the CTAs' row sums out (the replay scratch is in shared memory)
         "k_kda_backward": 2 * (ins - t["s"]) + t["v"] + t["s"] + ckpt + t["v"] + t["s"] + rows,
         "k_kda_rows": rows + t["beta"] + 2 * per_head + t["g"] + t["beta"],
         "k_kda_gva": 2 * per_head + 2 * t["q"],
