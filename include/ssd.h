@@ -347,9 +347,9 @@ ssd_status ssd_wait_selftest(void* ws, uint32_t limit_us, void* cuda_stream);
  *
  * ssd_kda_workspace_size: device workspace of the forward (backward == 0) or
  *   backward; host-only.  The backward's holds fp32 checkpoints of the state
- *   every 16 steps (b*HV*ceil(T/16)*K*V*4 bytes), a replay scratch of 16
- *   steps per (b, hv) and the per-value-head dq, dk.  Its first 4 bytes are
- *   the device status word, as for ssd_forward.
+ *   every 8 steps (b*HV*ceil(T/8)*K*V*4 bytes), the per-step row sums of its
+ *   CTAs and the per-value-head dq, dk.  Its first 4 bytes are the device
+ *   status word, as for ssd_forward.
  * ssd_kda_forward: o and s_final.
  * ssd_kda_backward: dq, dk, dv, dg, dbeta and ds0 of <do, o> + <ds_final,
  *   s_final> (ds_final required); recomputes the states from the leaf inputs
