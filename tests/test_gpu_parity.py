@@ -59,6 +59,11 @@ SMALL = {
     "mimo_tc_tail": scaled(MIMO, batch=2, seqlen=50, nheads=3, ngroups=3),
     "mimo_tc_r2": scaled(MIMO, batch=1, seqlen=96, nheads=2, ngroups=2, mimo_rank=2),
     "mimo_tc_r1": scaled(MIMO, batch=2, seqlen=80, nheads=2, ngroups=2, mimo_rank=1),
+    # the degenerate sequence of one step: a single chunk with 63 (tensor-core) or chunk - 1 empty steps
+    "tiny_fp32_one_step": dict(CONFIGS["mamba2_tiny_fp32"], seqlen=1),
+    "m2_bf16_one_step": scaled(M2_BF16, batch=2, seqlen=1, nheads=3),
+    "m1_one_step": scaled(M1, batch=1, seqlen=1, nheads=40),
+    "mimo_tc_one_step": scaled(MIMO, batch=1, seqlen=1, nheads=2, ngroups=2),
 }
 
 
