@@ -301,6 +301,42 @@ def test_mimo_rank_one_is_mamba2():
     assert rel(gm["ds0"], g2["ds0"]) < 1e-12
 
 
+def test_mimo_closed_form_da_zero_all_ranks_of_a_step():
+    """da = 0: the MIMO state is a running sum of every rank's v (x) B, and y_{t,r} reads the state after ALL R
+    rank terms of step t (ranks r' > r included), so a within-step causal mask (r' <= r) fails this; the
+    backward's dS_t = ds_final + sum_{tau >= t, r} dy (x) C gives dv, dB, dC, ds0 and dda = <dS_t, s_{t-1}>."""
+    rng = np.random.default_rng(21)
+    b, T, R, H, P, N = 2, 7, 3, 2, 3, 4
+    v = rng.standard_normal((b, T, R, H, P))
+    B = rng.standard_normal((b, T, R, H, N)) / 2
+    C = rng.standard_normal((b, T, R, H, N)) / 2
+    s0 = 0.1 * rng.standard_normal((b, H, P, N))
+    dy = rng.standard_normal((b, T, R, H, P))
+    dsf = rng.standard_normal((b, H, P, N))
+    da = np.zeros((b, T, H))
+    incr = np.einsum("btrhp,btrhn->bthpn", v, B)                      # all R ranks of step t
+    S = s0[:, None] + np.cumsum(incr, axis=1)                          # [b,T,H,P,N]: state after step t
+    y = np.einsum("bthpn,btrhn->btrhp", S, C)
+    f = oracle.mimo_forward(v, da, B, C, s0)
+    assert rel(f["y"], y) < 1e-13
+    assert rel(f["s_final"], S[:, -1]) < 1e-13
+    outer = np.einsum("btrhp,btrhn->bthpn", dy, C)
+    dS = dsf[:, None] + np.cumsum(outer[:, ::-1], axis=1)[:, ::-1]    # gradient of the state after step t
+    S_prev = np.concatenate([s0[:, None], S[:, :-1]], axis=1)
+    g = oracle.mimo_backward(dy, dsf, v, da, B, C, s0)
+    assert rel(g["dv"], np.einsum("bthpn,btrhn->btrhp", dS, B)) < 1e-13
+    assert rel(g["dB"], np.einsum("bthpn,btrhp->btrhn", dS, v)) < 1e-13
+    assert rel(g["dC"], np.einsum("bthpn,btrhp->btrhn", S, dy)) < 1e-13
+    assert rel(g["ds0"], dS[:, 0]) < 1e-13
+    assert rel(g["dda"], np.einsum("bthpn,bthpn->bth", dS, S_prev)) < 1e-12
+    # the within-step causal reading differs at every rank but the last: the pin has power
+    # (rank r sees the state before step t plus ranks q <= r of it)
+    causal = np.einsum("bthpn,btrhn->btrhp", S_prev, C) + np.einsum(
+        "btqhp,btqhn,btrhn,rq->btrhp", v, B, C, np.tril(np.ones((R, R))))
+    assert rel(causal[:, :, :-1], y[:, :, :-1]) > 1e-3
+    assert rel(causal[:, :, -1], y[:, :, -1]) < 1e-13
+
+
 def test_mamba2_width_one_is_mamba1_with_flat_decay():
     m1 = M1_TINY
     inp1 = f64(m1)
