@@ -203,6 +203,35 @@ def test_forward_equals_unrolled_sum():
     assert rel(oracle.forward("mamba2", inp)["y"], y) < 1e-13
 
 
+def test_mamba1_forward_equals_unrolled_sum():
+    """Mamba-1, one decay per state: y_t[d] = sum_n C_t[n] [exp(sum_{k<=t} dt'_k A[d,n]) s0[d,n]
+    + sum_{tau<=t} exp(sum_{tau<k<=t} dt'_k A[d,n]) dt'_tau x_tau[d] B_tau[n]], written out with no recurrence;
+    the states' decays differ, so a decay shared across n (or taken from the wrong index) fails it."""
+    cfg = scaled(M1_TINY, batch=1, seqlen=9, nheads=3, dstate=3)
+    inp = f64(cfg)
+    x, B, C, s0, A = inp["x"], inp["B"], inp["C"], inp["s0"], inp["A"]
+    d = _softplus(inp["dt_raw"])                                      # [b,T,D]
+    b, T, D = x.shape
+    N = A.shape[1]
+    assert np.ptp(A, axis=1).min() > 0                                # distinct decays per state
+    y = np.zeros_like(x)
+    sf = np.zeros((b, D, N))
+    for bb in range(b):
+        for dd in range(D):
+            for t in range(T):
+                for n in range(N):
+                    st = math.exp(sum(d[bb, k, dd] * A[dd, n] for k in range(t + 1))) * s0[bb, dd, n]
+                    for tau in range(t + 1):
+                        w = math.exp(sum(d[bb, k, dd] * A[dd, n] for k in range(tau + 1, t + 1)))
+                        st += w * d[bb, tau, dd] * x[bb, tau, dd] * B[bb, tau, n]
+                    y[bb, t, dd] += C[bb, t, n] * st
+                    if t == T - 1:
+                        sf[bb, dd, n] = st
+    f = oracle.forward("mamba1", inp)
+    assert rel(f["y"], y) < 1e-13
+    assert rel(f["s_final"], sf) < 1e-13
+
+
 def test_hand_worked_two_steps():
     with open(os.path.join(GOLDEN, "hand_worked_T2.json")) as f:
         gold = json.load(f)
