@@ -173,6 +173,32 @@ def test_closed_form_A_zero_is_prefix_sum():
     assert rel(g["dx"], d[..., None] * np.einsum("bthpn,btn->bthp", dS, B[:, :, 0])) < 1e-13
 
 
+def test_mamba1_closed_form_A_zero():
+    """Mamba-1 at A = 0 (every decay 1): s_t = s0 + sum_{tau<=t} dt' x (x) B per channel, and the backward is made
+    of running sums: dS_t = ds_final + sum_{tau>=t} dy C; dx = dt' <dS_t, B_t>, dB_t = sum_d dS_t dt' x,
+    dC_t = sum_d s_t dy, ds0 = dS_0, dA[d,n] = sum_t dt' dS_t s_{t-1}, ddt_raw = sigmoid(z) x <dS_t, B_t>."""
+    cfg = scaled(M1_TINY, batch=2, seqlen=11, nheads=3, dstate=4)
+    inp = f64(cfg)
+    inp["A"] = np.zeros_like(inp["A"])
+    x, B, C, s0, dy, dsf = inp["x"], inp["B"], inp["C"], inp["s0"], inp["dy"], inp["ds_final"]
+    z = inp["dt_raw"]
+    d = _softplus(z)                                                  # [b,T,D]
+    S = s0[:, None] + np.cumsum(np.einsum("btd,btn->btdn", d * x, B), axis=1)   # [b,T,D,N]
+    f = oracle.forward("mamba1", inp)
+    assert rel(f["y"], np.einsum("btdn,btn->btd", S, C)) < 1e-13
+    assert rel(f["s_final"], S[:, -1]) < 1e-13
+    dS = dsf[:, None] + np.cumsum(np.einsum("btd,btn->btdn", dy, C)[:, ::-1], axis=1)[:, ::-1]
+    S_prev = np.concatenate([s0[:, None], S[:, :-1]], axis=1)
+    g = oracle.backward("mamba1", inp)
+    dSB = np.einsum("btdn,btn->btd", dS, B)
+    assert rel(g["dx"], d * dSB) < 1e-13
+    assert rel(g["dB"], np.einsum("btdn,btd->btn", dS, d * x)) < 1e-13
+    assert rel(g["dC"], np.einsum("btdn,btd->btn", S, dy)) < 1e-13
+    assert rel(g["ds0"], dS[:, 0]) < 1e-13
+    assert rel(g["dA"], np.einsum("btd,btdn,btdn->dn", d, dS, S_prev)) < 1e-12
+    assert rel(g["ddt_raw"], x * dSB / (1.0 + np.exp(-z))) < 1e-12
+
+
 def test_closed_form_dy_zero_is_pure_decay():
     inp = f64(TINY)
     inp["dy"] = np.zeros_like(inp["dy"])
