@@ -31,6 +31,9 @@ CASES = {
     "tiny": BASE,
     "ragged": dict(BASE, batch=2, seqlen=37, nheads=1, value_heads=2, key_dim=40, value_dim=20),
     "ragged_cols": dict(BASE, batch=1, seqlen=29, nheads=1, value_heads=2, key_dim=37, value_dim=45),
+    # degenerate: one step; widths below one warp's layout (5 key rows, 3 of a warp's 4 value columns)
+    "one_step": dict(BASE, batch=2, seqlen=1),
+    "narrow": dict(BASE, batch=1, seqlen=3, nheads=1, value_heads=1, key_dim=5, value_dim=3),
     "gva4": dict(BASE, batch=1, seqlen=48, nheads=1, value_heads=4, key_dim=32, value_dim=16),
     "dim128": dict(BASE, batch=1, seqlen=100, nheads=2, value_heads=4, key_dim=128, value_dim=128),
     "one_value_head": dict(BASE, batch=2, seqlen=50, nheads=3, value_heads=3, key_dim=64, value_dim=40),
