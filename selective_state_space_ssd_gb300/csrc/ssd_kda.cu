@@ -19,9 +19,9 @@
 //             2. k_kda_backward, CTAs of up to eight column warps of one
 //                (b, hv), walks the 8-step segments from the last: it replays
 //                the segment from its checkpoint (S_dec and r of every step to
-//                shared memory), then runs steps 1-6
-//                backwards through it, carrying dS_acc in registers across
-//                segments, and writes the CTA's row sums per step;
+//                shared memory), then runs steps 1-6 backwards through it,
+//                carrying dS_acc in registers across segments, and writes the
+//                CTA's row sums per step;
 //             3. k_kda_rows adds the CTAs' row sums in CTA order (dq, dk, dg,
 //                dbeta per value head);
 //             4. k_kda_gva adds the per-value-head dq, dk onto their query /
