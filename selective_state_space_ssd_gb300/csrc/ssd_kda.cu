@@ -123,6 +123,50 @@ __device__ __forceinline__ void delta_step(float (&S)[kRows][kCols], const StepI
   }
 }
 
+// F1-F6 on this warp's slice for the forward, with o_j = q^T S_t[:, j] = q^T S_dec[:, j] + (q . a) r_j (F5): the
+// column sums q^T S_dec reduce beside k^T S_dec and q . k needs no state, so the only work after the state update
+// is one FMA per column (reduced after F5, o's warp sums had held each step up).  Lanes 0 .. kCols - 1 return
+// o[col0 + lane].
+__device__ __forceinline__ float delta_step_o(float (&S)[kRows][kCols], const StepIn& s, int lane) {
+  float qk = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) qk = fmaf(s.q[i], s.k[i], qk);
+#pragma unroll
+  for (int i = 0; i < kRows; ++i)
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) S[i][j] *= s.eg[i];  // F1
+  float p[kCols], qs[kCols];
+#pragma unroll
+  for (int j = 0; j < kCols; ++j) {
+    p[j] = 0.f, qs[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      p[j] = fmaf(s.k[i], S[i][j], p[j]);
+      qs[j] = fmaf(s.q[i], S[i][j], qs[j]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    qk += __shfl_xor_sync(0xffffffffu, qk, o);
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) {
+      p[j] += __shfl_xor_sync(0xffffffffu, p[j], o);
+      qs[j] += __shfl_xor_sync(0xffffffffu, qs[j], o);
+    }
+  }
+  const float qa = s.beta * qk;  // q . a with a = beta k (F4)
+  float out = 0.f;
+#pragma unroll
+  for (int j = 0; j < kCols; ++j) {
+    const float r = s.v[j] - p[j];  // F2, F3
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) S[i][j] = fmaf(s.beta * s.k[i], r, S[i][j]);  // F5
+    const float oj = fmaf(qa, r, qs[j]);                                           // F6
+    if (lane == j) out = oj;
+  }
+  return out;
+}
+
 // Checkpoint slot of warp w's slice: [unit][seg][w][i * kCols + j][lane] (lane-major: one coalesced line per store)
 __device__ __forceinline__ size_t ckpt_slot(const KdaDims& d, int unit, int seg, int w) {
   return (((size_t)unit * d.nseg + seg) * d.nw + w) * kSlice;
@@ -161,18 +205,11 @@ __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const f
     StepIn s = nx;
     if (t + 1 < d.T) load_step(in, d, b, hv, t + 1, lane, col0, nx);
     finish_step(s, in.scale);
-    float r[kCols];
-    delta_step(S, s, r);
-    if (!kCkpt) {
-      float out = 0.f;  // o[col0 + lane] for lanes 0 .. kCols - 1
-#pragma unroll
-      for (int j = 0; j < kCols; ++j) {
-        float x = 0.f;
-#pragma unroll
-        for (int i = 0; i < kRows; ++i) x = fmaf(s.q[i], S[i][j], x);  // F6
-        x = warp_sum(x);
-        if (lane == j) out = x;
-      }
+    if (kCkpt) {
+      float r[kCols];
+      delta_step(S, s, r);
+    } else {
+      const float out = delta_step_o(S, s, lane);  // o[col0 + lane] for lanes 0 .. kCols - 1
       if (lane < kCols && col0 + lane < d.V) o[(((size_t)b * d.T + t) * d.HV + hv) * d.V + col0 + lane] = out;
     }
   }
