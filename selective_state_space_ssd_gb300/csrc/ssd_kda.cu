@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const f
     }
   StepIn nx;
   load_step(in, d, b, hv, 0, lane, col0, nx);
-  for (int t = 0; t < d.T; ++t) {
+  auto step = [&](int t) {
     if (kCkpt && t % kSeg == 0) {
       float* dst = ckpt + ckpt_slot(d, unit, t / kSeg, w);
 #pragma unroll
@@ -212,6 +212,14 @@ __global__ void __launch_bounds__(64) k_kda_forward(KdaIn in, KdaDims d, const f
       const float out = delta_step_o(S, s, lane);  // o[col0 + lane] for lanes 0 .. kCols - 1
       if (lane < kCols && col0 + lane < d.V) o[(((size_t)b * d.T + t) * d.HV + hv) * d.V + col0 + lane] = out;
     }
+  };
+  if (kCkpt) {
+    // the replay unrolled by two: a step's loads and exponentials overlap the previous step's reductions (the
+    // forward with o measured slower unrolled)
+#pragma unroll 2
+    for (int t = 0; t < d.T; ++t) step(t);
+  } else {
+    for (int t = 0; t < d.T; ++t) step(t);
   }
   if (!kCkpt) {
 #pragma unroll
