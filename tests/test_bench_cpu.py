@@ -106,3 +106,23 @@ def test_mimo_executed_flops_count_the_fused_sequence():
     assert bench.tensor_flops(cfg, executed=True) < bench.tensor_flops(cfg)
     m2 = CONFIGS["mamba2_2p7b_bf16"]
     assert bench.tensor_flops(m2, executed=True) == bench.tensor_flops(m2)
+
+
+@pytest.mark.parametrize("dt,steps", [(40.0, 3), (0.5, 200), (2.0, 60)])
+def test_reference_arm_caps_its_timed_passes(dt, steps, monkeypatch, capsys):
+    """The reference arm's steps are whole-workload oracle passes: it times at most REF_BUDGET_S of them (at least
+    3, at most --steps) and reports how many ran.  The oracle is replaced by a stub that reports dt seconds."""
+    calls = []
+
+    def fake_time_oracle(cfg, inputs=None, whole=False, **kw):
+        calls.append(whole)
+        return 1.0, dt, 4, "stub", cfg, inputs, None
+
+    monkeypatch.setattr(bench, "time_oracle", fake_time_oracle)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "200", "--warmup", "3"])
+    monkeypatch.delenv("RANK", raising=False)
+    assert bench.main() == 0
+    line = __import__("json").loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == steps and line["steps_requested"] == 200
+    assert len(calls) == 3 + steps and all(calls)
+    assert line["ms_per_step"] == pytest.approx(1e3 * dt)
