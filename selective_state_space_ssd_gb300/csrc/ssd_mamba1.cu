@@ -254,37 +254,48 @@ __global__ void __launch_bounds__(kThreads, 4) k_m1_backward(M1 m, M1Bwd g) {
   }
   auto ck_at = [&](int k, int j) { return g.ck + (((size_t)b * m.nck + k) * m.D + d) * m.N + kS * l + j; };
 
-  // ---- forward replay: the state entering every chunk
-  for (int k = 0; k < kStages - 1; ++k) {
-    if (k < m.nck) stage_load<kWc, kTc>(stage_at<kWc, kTc, true>(smf + k * sf), m, nullptr, b, d0, k, false);
-    cp_async_commit();
-  }
-  for (int k = 0; k < m.nck; ++k) {
-    const int kf = k + kStages - 1;
-    if (kf < m.nck)
-      stage_load<kWc, kTc>(stage_at<kWc, kTc, true>(smf + (kf % kStages) * sf), m, nullptr, b, d0, kf, false);
-    cp_async_commit();
-#pragma unroll
-    for (int j = 0; j < kS; ++j)
-      if (act[j]) *ck_at(k, j) = s[j];
-    cp_async_wait_stages();
-    __syncthreads();
-    const Stage cur = stage_at<kWc, kTc, true>(smf + (k % kStages) * sf);
-#pragma unroll
-    for (int i = tid; i < kTc * cpb; i += kThreads) dtp[i] = softplus_f(cur.dt[i]);
-    __syncthreads();
-#pragma unroll
-    for (int tt = 0; tt < kTc; ++tt) {
-      const float dp = dtp[tt * cpb + c], u = dp * cur.x[tt * cpb + c];
-      float Bj[kS];
-      ldsk(cur.B + tt * NP + kS * l, Bj);
-#pragma unroll
-      for (int j = 0; j < kS; ++j) s[j] = decay(dp, A2[j]) * s[j] + u * Bj[j];
+  // ---- forward replay: the state entering every kTc-step chunk (its checkpoint), walking the sequence in
+  //      staged chunks of kTcF steps as the forward does (a quarter of the barriers and dt' passes of kTc-step
+  //      chunks); its buffers alias the reverse walk's, which are not in use yet
+  {
+    constexpr size_t sfr = stage_floats(cpb, NP, kTcF, false);
+    float* dtr = smf + kStages * sfr;  // [kTcF][cpb] dt' of the chunk
+    for (int k = 0; k < kStages - 1; ++k) {
+      if (k < m.nckf) stage_load<kWc, kTcF>(stage_at<kWc, kTcF, false>(smf + k * sfr), m, nullptr, b, d0, k, false);
+      cp_async_commit();
     }
-    __syncthreads();  // the chunk's buffers are free for the copies issued next
+    for (int k = 0; k < m.nckf; ++k) {
+      const int kf = k + kStages - 1;
+      if (kf < m.nckf)
+        stage_load<kWc, kTcF>(stage_at<kWc, kTcF, false>(smf + (kf % kStages) * sfr), m, nullptr, b, d0, kf, false);
+      cp_async_commit();
+      cp_async_wait_stages();
+      __syncthreads();
+      const Stage cur = stage_at<kWc, kTcF, false>(smf + (k % kStages) * sfr);
+#pragma unroll
+      for (int i = tid; i < kTcF * cpb; i += kThreads) dtr[i] = softplus_f(cur.dt[i]);
+      __syncthreads();
+#pragma unroll
+      for (int tt = 0; tt < kTcF; ++tt) {
+        if (tt % kTc == 0) {  // the state entering backward chunk ck (chunks past the sequence are not stored)
+          const int ck = (k * kTcF + tt) / kTc;
+          if (ck < m.nck) {
+#pragma unroll
+            for (int j = 0; j < kS; ++j)
+              if (act[j]) *ck_at(ck, j) = s[j];
+          }
+        }
+        const float dp = dtr[tt * cpb + c], u = dp * cur.x[tt * cpb + c];
+        float Bj[kS];
+        ldsk(cur.B + tt * NP + kS * l, Bj);
+#pragma unroll
+        for (int j = 0; j < kS; ++j) s[j] = decay(dp, A2[j]) * s[j] + u * Bj[j];
+      }
+      __syncthreads();  // the chunk's buffers are free for the copies issued next
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();
 
   // ---- reverse walk over the chunks
   float dS[kS], dA[kS];
@@ -452,8 +463,10 @@ size_t fwd_smem() {
 template <int kWc>
 size_t bwd_smem() {
   constexpr int cpb = Geo<kWc>::cpb, NP = Geo<kWc>::NP;
-  return (kStages * stage_floats(cpb, NP, kTc, true) + 4 * (size_t)kTc * cpb + 2 * (size_t)kTc * cpb * NP) *
-         sizeof(float);
+  // the reverse walk's buffers, or the forward replay's (kTcF-step stages and their dt'), which alias them
+  const size_t walk = kStages * stage_floats(cpb, NP, kTc, true) + 4 * (size_t)kTc * cpb + 2 * (size_t)kTc * cpb * NP;
+  const size_t replay = kStages * stage_floats(cpb, NP, kTcF, false) + (size_t)kTcF * cpb;
+  return (walk > replay ? walk : replay) * sizeof(float);
 }
 
 template <int kWc>
