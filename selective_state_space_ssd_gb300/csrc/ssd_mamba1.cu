@@ -9,9 +9,10 @@
 // issue-bound), the Wc threads of a channel are adjacent lanes (y and the other
 // sums over n are Wc-lane shuffles), and a block of 128 threads holds cpb =
 // 128 / Wc consecutive channels of one sequence.  The block walks the sequence
-// in chunks (32 steps in the forward, 8 in the backward) whose inputs (x, dt,
-// dy for its channels; B, C of the step) are staged in shared memory by
-// cp.async kStages - 1 chunks ahead, so a step reads shared memory only.
+// in chunks (32 steps in the forward and the backward's replay, 8 in its
+// reverse walk) whose inputs (x, dt, dy for its channels; B, C of the step)
+// are staged in shared memory by cp.async kStages - 1 chunks ahead, so a step
+// reads shared memory only.
 //
 // The backward replays the forward once to keep the state entering every
 // chunk (a checkpoint in global memory), then walks the chunks in reverse:
