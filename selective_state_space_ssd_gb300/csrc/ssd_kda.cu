@@ -301,23 +301,35 @@ __global__ void __launch_bounds__(32 * kCtaWarps) k_kda_backward(KdaIn in, KdaDi
       }
     }
     __syncwarp();  // the r values of the warp's columns, written by lanes 0 .. kCols - 1, are read by every lane
-    // steps 1-6 backwards through the segment
+    // steps 1-6 backwards through the segment; a step's inputs and do are loaded one step ahead
     StepIn nx;
-    if (live) load_step(in, d, b, hv, t1 - 1, lane, col0, nx);
+    float dnx[kCols];
+    auto load_do = [&](int t, float (&x)[kCols]) {
+      const size_t g = ((size_t)b * d.T + t) * d.HV + hv;
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) x[j] = col0 + j < d.V ? out.dout[g * d.V + col0 + j] : 0.f;
+    };
+    if (live) {
+      load_step(in, d, b, hv, t1 - 1, lane, col0, nx);
+      load_do(t1 - 1, dnx);
+    }
     for (int t = t1 - 1; t >= t0; --t, ++step) {
       const int pb = step & 1;
       const size_t gv = ((size_t)b * d.T + t) * d.HV + hv;
       StepIn s = nx;
+      float dov[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) dov[j] = dnx[j];
       if (live) {
-        if (t > t0) load_step(in, d, b, hv, t - 1, lane, col0, nx);
+        if (t > t0) {
+          load_step(in, d, b, hv, t - 1, lane, col0, nx);
+          load_do(t - 1, dnx);
+        }
         finish_step(s, in.scale);
         float* st = scr + (size_t)(t - t0) * step_floats;
-        float r[kCols], dov[kCols], u[kCols];
+        float r[kCols], u[kCols];
 #pragma unroll
-        for (int j = 0; j < kCols; ++j) {
-          r[j] = r_at(st, j);
-          dov[j] = col0 + j < d.V ? out.dout[gv * d.V + col0 + j] : 0.f;
-        }
+        for (int j = 0; j < kCols; ++j) r[j] = r_at(st, j);
         // step 1: dS_acc += q (x) do;  dq = S_t do with S_t = S_dec + beta k (x) r;  step 2: da = dS_acc r
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
