@@ -8,7 +8,8 @@
   delta-rule path -k (x) dr from dS_dec) must fail that check by more than 100x
   its gate.
 * Closed forms: beta = 0 leaves pure per-row decay of s0; with one-hot keys
-  and beta = 1 the delta rule overwrites row j of the state with v_t exactly.
+  and beta = 1 the delta rule overwrites row j of the state with v_t exactly;
+  a two-step example worked by hand fixes that o_t reads the updated state.
 * Euler identities (o is linear in q; o and s_final are jointly linear in
   (v, s0)), chaining two calls through s_final / ds0, and the GVA sum against
   explicitly repeated query / key heads.
@@ -122,6 +123,35 @@ def test_one_hot_keys_with_beta_one_overwrite_a_row():
                 else:
                     want = np.exp(np.sum(inp["g"][bb, :, hv, j])) * inp["s0"][bb, hv, j]
                 np.testing.assert_allclose(f["s_final"][bb, hv, j], want, rtol=1e-12, atol=1e-14)
+
+
+def test_output_reads_the_updated_state():
+    """F6 reads S_t, after the delta-rule update F5: with s0 = 0, one-hot key e_j and beta = 1 at the first step,
+    S_1 = e_j (x) v_1, so o_1 = scale q_1[j] v_1 (reading S_dec instead would give 0).  A second step with key
+    e_i (i != j), beta = 1/2 and log-decay g keeps row j decayed by exp(g_2[j]) and writes half of v_2 into row i:
+    o_2 = scale (q_2[j] exp(g_2[j]) v_1 + q_2[i] v_2 / 2); all worked out by hand here."""
+    b, T, H, HV, K, V = 1, 2, 1, 1, 3, 2
+    j, i = 2, 0
+    q = np.zeros((b, T, H, K))
+    q[0, 0] = [0.3, -0.7, 1.5]
+    q[0, 1] = [2.0, 0.4, -1.1]
+    k = np.zeros((b, T, H, K))
+    k[0, 0, 0, j] = 1.0
+    k[0, 1, 0, i] = 1.0
+    v = np.array([[[[0.8, -1.2]], [[0.5, 2.0]]]])                     # [b,T,HV,V]
+    g = np.zeros((b, T, HV, K))
+    g[0, 1, 0] = [-0.2, -0.3, -0.6]
+    beta = np.array([[[1.0], [0.5]]])                                  # [b,T,HV]
+    scale = 0.25
+    f = kda_forward(q, k, v, g, beta, None, scale)
+    o1 = scale * q[0, 0, 0, j] * v[0, 0, 0]
+    o2 = scale * (q[0, 1, 0, j] * np.exp(g[0, 1, 0, j]) * v[0, 0, 0] + q[0, 1, 0, i] * 0.5 * v[0, 1, 0])
+    np.testing.assert_allclose(f["o"][0, 0, 0], o1, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(f["o"][0, 1, 0], o2, rtol=0, atol=1e-15)
+    S = np.zeros((K, V))
+    S[j] = np.exp(g[0, 1, 0, j]) * v[0, 0, 0]
+    S[i] = 0.5 * v[0, 1, 0]
+    np.testing.assert_allclose(f["s_final"][0, 0], S, rtol=0, atol=1e-15)
 
 
 def test_euler_identities():
